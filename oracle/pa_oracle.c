@@ -1,0 +1,327 @@
+/*
+ * pa_oracle.c -- plain fp64 CPU oracle for paged-attention decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or constant with the CUDA path.
+ *
+ * What it computes (the plain definition; tiling, online softmax and
+ * split-context partitions only reorder it):
+ *
+ *   For sequence s, query position i, query head h, KV head hkv = h / G and
+ *   L = context_lens[s]:
+ *     L == 0  -> out = 0        ("[FlyDSL] pa_decode: MXFP4 K/V in the shared
+ *                                 PA tile kernel", plan-free commit: context-0
+ *                                 rows are zero-filled on both paths)
+ *     for t in [0, L): blk = block_tables[s, t / S], slot = t mod S
+ *        (only owned rows are read: "[FlyDSL] pa_decode: zero V rows past the
+ *         context before PV", Root cause / Fix -- rows at or past the context
+ *         length never reach the output)
+ *     x_t = softmax_scale * q_scale * sum_d q[d] * k_t[d]
+ *     out = sum_t exp(x_t - M) v_t / sum_t exp(x_t - M),  M = max_t x_t
+ *   computed in two passes, in double precision.
+ *
+ * Storage formats are decoded from their definitions:
+ *   bf16      : the high half of an IEEE binary32
+ *   e4m3 (OCP): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0
+ *               is subnormal m/8 * 2^-6; S.1111.111 is NaN; there is no Inf
+ *               (the first page's Tests section: the "inf" fill of e4m3 is the
+ *               finite +-448)
+ *   e2m1      : 1 sign, 2 exponent bits (bias 1), 1 mantissa bit
+ *   e8m0      : 2^(b - 127); b = 255 is NaN
+ *   MXFP4 row : "[FlyDSL] pa_decode: MXFP4 K/V ...", Summary: data uint8
+ *               [pages, kv_heads, 128, 64] (two e2m1 per byte), scales uint8
+ *               e8m0 [pages, kv_heads, 128, 4], one scale per 32 values along
+ *               head_dim.  Element 2j is the low nibble of byte j, 2j+1 the
+ *               high nibble (the OCP MX packing; the pages do not say).
+ *
+ * All tensors are dense and contiguous:
+ *   query        [B, qlen, Hq, D]        bf16 or e4m3 bytes
+ *   q_scale      scalar or [B, qlen, Hq] fp32 (e4m3 query only)
+ *   key/value    [NB, Hkv, S, row_bytes] (row_bytes = 2D bf16, D e4m3, D/2 MXFP4)
+ *   scales       per-tensor: fp32 [1]; per-token: fp32 [NB, Hkv, S];
+ *                e8m0: uint8 [NB, Hkv, S, D/32]
+ *   block_tables [B, max_blocks_per_seq] int32; context_lens [B] int32
+ *   out          [B, qlen, Hq, D] double
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_KV_BF16 = 0, ORC_KV_E4M3 = 1, ORC_KV_MXFP4 = 2 };
+enum { ORC_SCALE_NONE = 0, ORC_SCALE_TENSOR = 1, ORC_SCALE_TOKEN = 2, ORC_SCALE_E8M0 = 3 };
+enum { ORC_Q_BF16 = 0, ORC_Q_E4M3 = 1 };
+
+typedef struct {
+  int32_t batch, qlen, num_q_heads, num_kv_heads, head_dim, page_size;
+  int32_t num_blocks, max_blocks_per_seq;
+  int32_t kv_format, scale_kind, q_format, q_scale_per_row;
+  double softmax_scale;
+  const void* query;
+  const float* q_scale;
+  const void* key_cache;
+  const void* value_cache;
+  const void* key_scale;
+  const void* value_scale;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+} orc_args;
+
+/* ---- format decoders ---------------------------------------------------- */
+
+double orc_bf16(uint16_t bits) {
+  uint32_t w = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+double orc_e4m3(uint8_t b) {
+  int sign = b >> 7;
+  int e = (b >> 3) & 15;
+  int m = b & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, -6);
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+double orc_e2m1(uint8_t nibble) {
+  int sign = (nibble >> 3) & 1;
+  int e = (nibble >> 1) & 3;
+  int m = nibble & 1;
+  double mag;
+  if (e == 0)
+    mag = 0.5 * (double)m;
+  else
+    mag = ldexp(1.0 + 0.5 * (double)m, e - 1);
+  return sign ? -mag : mag;
+}
+
+double orc_e8m0(uint8_t b) {
+  if (b == 255) return NAN;
+  return ldexp(1.0, (int)b - 127);
+}
+
+/* ---- element access ------------------------------------------------------ */
+
+static int64_t row_bytes(const orc_args* a) {
+  if (a->kv_format == ORC_KV_BF16) return 2 * (int64_t)a->head_dim;
+  if (a->kv_format == ORC_KV_E4M3) return a->head_dim;
+  return a->head_dim / 2;
+}
+
+/* Dequantized element d of token slot `slot` in page `blk`, KV head `hkv`. */
+static double kv_elem(const orc_args* a, const void* cache, const void* scale, int64_t blk,
+                      int hkv, int slot, int d) {
+  const int64_t rb = row_bytes(a);
+  const int64_t token = (blk * a->num_kv_heads + hkv) * a->page_size + slot;
+  const uint8_t* row = (const uint8_t*)cache + token * rb;
+  double v;
+  if (a->kv_format == ORC_KV_BF16) {
+    uint16_t bits;
+    memcpy(&bits, row + 2 * d, 2);
+    v = orc_bf16(bits);
+  } else if (a->kv_format == ORC_KV_E4M3) {
+    v = orc_e4m3(row[d]);
+  } else {
+    uint8_t byte = row[d / 2];
+    uint8_t nib = (d % 2 == 0) ? (byte & 15) : (byte >> 4);
+    v = orc_e2m1(nib);
+  }
+  switch (a->scale_kind) {
+    case ORC_SCALE_TENSOR:
+      v *= (double)((const float*)scale)[0];
+      break;
+    case ORC_SCALE_TOKEN:
+      v *= (double)((const float*)scale)[token];
+      break;
+    case ORC_SCALE_E8M0: {
+      const int nblk = a->head_dim / 32;
+      v *= orc_e8m0(((const uint8_t*)scale)[token * nblk + d / 32]);
+      break;
+    }
+    default:
+      break;
+  }
+  return v;
+}
+
+static double q_elem(const orc_args* a, int s, int i, int h, int d) {
+  const int64_t qrow = ((int64_t)s * a->qlen + i) * a->num_q_heads + h;
+  if (a->q_format == ORC_Q_BF16) {
+    uint16_t bits;
+    memcpy(&bits, (const uint8_t*)a->query + 2 * (qrow * a->head_dim + d), 2);
+    return orc_bf16(bits);
+  }
+  double q = orc_e4m3(((const uint8_t*)a->query)[qrow * a->head_dim + d]);
+  double qs = a->q_scale_per_row ? (double)a->q_scale[qrow] : (double)a->q_scale[0];
+  return q * qs;
+}
+
+/* ---- attention over a token range ---------------------------------------- */
+
+/*
+ * Softmax attention of one (s, hkv) group over owned tokens [t0, t1), for every
+ * query row of the group (qlen * G rows).  Writes, per row r:
+ *   m[r] = max_t x_t, l[r] = sum_t exp(x_t - m[r]), o[r][:] = sum_t exp(x_t - m) v_t / l.
+ * An empty range gives m = -inf, l = 0, o = 0.
+ */
+static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, double* m,
+                         double* l, double* o, double* x, double* qv, double* kv) {
+  const int G = a->num_q_heads / a->num_kv_heads;
+  const int R = a->qlen * G;
+  const int D = a->head_dim;
+  const int S = a->page_size;
+  const int32_t* bt = a->block_tables + (int64_t)s * a->max_blocks_per_seq;
+  const int n = t1 - t0;
+
+  for (int r = 0; r < R; ++r) {
+    int i = r / G, h = hkv * G + r % G;
+    for (int d = 0; d < D; ++d) qv[(int64_t)r * D + d] = q_elem(a, s, i, h, d);
+  }
+  /* pass 1: scores */
+  for (int r = 0; r < R; ++r) m[r] = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    int t = t0 + j;
+    int64_t blk = bt[t / S];
+    for (int d = 0; d < D; ++d) kv[d] = kv_elem(a, a->key_cache, a->key_scale, blk, hkv, t % S, d);
+    for (int r = 0; r < R; ++r) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qv[(int64_t)r * D + d] * kv[d];
+      double xs = a->softmax_scale * dot;
+      x[(int64_t)r * n + j] = xs;
+      if (xs > m[r]) m[r] = xs;
+    }
+  }
+  /* pass 2: weights and the weighted sum of V */
+  for (int r = 0; r < R; ++r) {
+    l[r] = 0.0;
+    for (int d = 0; d < D; ++d) o[(int64_t)r * D + d] = 0.0;
+  }
+  for (int j = 0; j < n; ++j) {
+    int t = t0 + j;
+    int64_t blk = bt[t / S];
+    for (int d = 0; d < D; ++d)
+      kv[d] = kv_elem(a, a->value_cache, a->value_scale, blk, hkv, t % S, d);
+    for (int r = 0; r < R; ++r) {
+      double w = exp(x[(int64_t)r * n + j] - m[r]);
+      l[r] += w;
+      for (int d = 0; d < D; ++d) o[(int64_t)r * D + d] += w * kv[d];
+    }
+  }
+  for (int r = 0; r < R; ++r)
+    if (l[r] > 0.0)
+      for (int d = 0; d < D; ++d) o[(int64_t)r * D + d] /= l[r];
+}
+
+static int check_args(const orc_args* a) {
+  if (a->batch < 0 || a->qlen < 1 || a->num_kv_heads < 1 || a->num_q_heads < 1) return -1;
+  if (a->num_q_heads % a->num_kv_heads) return -1;
+  if (a->head_dim < 1 || a->page_size < 1) return -1;
+  if (a->kv_format == ORC_KV_MXFP4 && (a->head_dim % 32 || a->scale_kind != ORC_SCALE_E8M0))
+    return -1;
+  for (int s = 0; s < a->batch; ++s) {
+    int L = a->context_lens[s];
+    if (L < 0) return -1;
+    if ((int64_t)(L + a->page_size - 1) / a->page_size > a->max_blocks_per_seq) return -1;
+    for (int p = 0; p < (L + a->page_size - 1) / a->page_size; ++p) {
+      int32_t blk = a->block_tables[(int64_t)s * a->max_blocks_per_seq + p];
+      if (blk < 0 || blk >= a->num_blocks) return -1;
+    }
+  }
+  return 0;
+}
+
+static int max_context(const orc_args* a) {
+  int mx = 0;
+  for (int s = 0; s < a->batch; ++s)
+    if (a->context_lens[s] > mx) mx = a->context_lens[s];
+  return mx;
+}
+
+/*
+ * Full decode.  out: [B, qlen, Hq, D] doubles.  nthreads <= 0 uses the OpenMP
+ * default.  Returns 0, or -1 on malformed arguments, -2 on allocation failure.
+ */
+int orc_pa_decode(const orc_args* a, double* out, int nthreads) {
+  if (check_args(a)) return -1;
+  const int G = a->num_q_heads / a->num_kv_heads;
+  const int R = a->qlen * G;
+  const int D = a->head_dim;
+  const int Lmax = max_context(a);
+  const int units = a->batch * a->num_kv_heads;
+  int err = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel
+  {
+    double* m = malloc(sizeof(double) * R);
+    double* l = malloc(sizeof(double) * R);
+    double* o = malloc(sizeof(double) * (size_t)R * D);
+    double* x = malloc(sizeof(double) * (size_t)R * (Lmax > 0 ? Lmax : 1));
+    double* qv = malloc(sizeof(double) * (size_t)R * D);
+    double* kv = malloc(sizeof(double) * D);
+    if (!m || !l || !o || !x || !qv || !kv) {
+#pragma omp atomic write
+      err = -2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int u = 0; u < units; ++u) {
+        int s = u / a->num_kv_heads, hkv = u % a->num_kv_heads;
+        attend_range(a, s, hkv, 0, a->context_lens[s], m, l, o, x, qv, kv);
+        for (int r = 0; r < R; ++r) {
+          int i = r / G, h = hkv * G + r % G;
+          double* dst = out + ((((int64_t)s * a->qlen + i) * a->num_q_heads + h) * D);
+          for (int d = 0; d < D; ++d) dst[d] = o[(int64_t)r * D + d];
+        }
+      }
+    }
+    free(m); free(l); free(o); free(x); free(qv); free(kv);
+  }
+  return err;
+}
+
+/*
+ * Attention of one (s, hkv) group over tokens [t0, t1) of sequence s; t1 must
+ * not exceed context_lens[s].  Writes m, l: [qlen*G]; o: [qlen*G, D]; row
+ * r = i*G + (h mod G).  Used to check the partition merge identity.
+ */
+int orc_pa_decode_range(const orc_args* a, int s, int hkv, int t0, int t1, double* m, double* l,
+                        double* o) {
+  if (check_args(a)) return -1;
+  if (s < 0 || s >= a->batch || hkv < 0 || hkv >= a->num_kv_heads) return -1;
+  if (t0 < 0 || t1 < t0 || t1 > a->context_lens[s]) return -1;
+  const int G = a->num_q_heads / a->num_kv_heads;
+  const int R = a->qlen * G;
+  const int D = a->head_dim;
+  int n = t1 - t0;
+  double* x = malloc(sizeof(double) * (size_t)R * (n > 0 ? n : 1));
+  double* qv = malloc(sizeof(double) * (size_t)R * D);
+  double* kv = malloc(sizeof(double) * D);
+  int rc = 0;
+  if (!x || !qv || !kv)
+    rc = -2;
+  else
+    attend_range(a, s, hkv, t0, t1, m, l, o, x, qv, kv);
+  free(x); free(qv); free(kv);
+  return rc;
+}
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

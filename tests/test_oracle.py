@@ -1,0 +1,294 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each check is chosen so that a plausible slip in the oracle -- a wrong exponent
+bias, a dropped scale, a swapped nibble, a transposed head mapping, a read of an
+unowned row -- fails at least one of them:
+
+* format decoders against library casts (torch float8_e4m3fn / float8_e8m0fnu /
+  bfloat16) and, for e2m1, against the value table of the OCP MX format;
+* closed forms: context 1 returns that V row; identical K rows return the mean
+  of V; context 0 returns zero;
+* a dense brute force on tiny inputs: K/V materialised by an independent
+  gather and dequantisation, ``torch.softmax`` in float64;
+* the partition merge identity over a split context;
+* the unowned-row invariant: NaN/Inf fills leave the output bit-identical.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import pa_oracle as orc
+from paged_attention_decode_02_gb300 import synth
+from tests import util
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# OCP MX e2m1 code points (magnitudes for codes 0..7; bit 3 is the sign).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+# ---- decoders ----------------------------------------------------------------
+
+def test_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([orc.decode_e4m3(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+    assert np.isfinite(got[ok]).all()  # no Inf code in e4m3fn
+
+
+def test_e2m1_all_codes_match_format_table():
+    for n in range(16):
+        mag = E2M1_TABLE[n & 7]
+        want = -mag if n & 8 else mag
+        got = orc.decode_e2m1(n)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), n
+
+
+def test_e8m0_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([orc.decode_e8m0(b) for b in range(256)])
+    assert np.isnan(got[255]) and np.isnan(ref[255])
+    assert np.array_equal(got[:255], ref[:255])
+    assert all(got[b] == math.ldexp(1.0, b - 127) for b in range(255))
+
+
+def test_bf16_matches_torch():
+    g = torch.Generator().manual_seed(3)
+    bits = torch.randint(-32768, 32768, (4096,), generator=g, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([orc.decode_bf16(int(b) & 0xFFFF) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_pages_facts_golden():
+    """Values the pages state outright (tests/golden/pages_facts.json, each cited)."""
+    with open(os.path.join(GOLDEN, "pages_facts.json")) as f:
+        facts = json.load(f)
+    # e4m3 has no Inf: its "inf" fill is the finite +-448.
+    fill = facts["e4m3_inf_fill"]
+    assert orc.decode_e4m3(fill["pos_byte"]) == fill["value"]
+    assert orc.decode_e4m3(fill["neg_byte"]) == -fill["value"]
+    # e8m0 byte 255 is not a number.
+    assert math.isnan(orc.decode_e8m0(facts["e8m0_nan_byte"]["byte"]))
+    # The plan emits ceil(context_len / 256) tiles per sequence.
+    tl = facts["tiles_per_sequence"]
+    for L, n in zip(tl["context_lens"], tl["tiles"]):
+        assert (L + tl["tile"] - 1) // tl["tile"] == n
+    # MXFP4 page layout.
+    mx = facts["mxfp4_layout"]
+    case = synth.config4(batch=2)
+    p = synth.make(case)
+    assert list(p["key_cache"].shape[1:]) == mx["data_shape_after_pages"]
+    assert list(p["key_scale"].shape[1:]) == mx["scale_shape_after_pages"]
+    assert case.head_dim // mx["values_per_scale"] == mx["scale_shape_after_pages"][-1]
+
+
+# ---- an independent dense brute force ---------------------------------------
+
+def _dequant_dense(p: dict, which: str) -> torch.Tensor:
+    """Dequantised cache [NB, Hkv, S, D] in float64, via library casts and tables."""
+    case = p["case"]
+    c = p["key_cache" if which == "k" else "value_cache"].cpu()
+    sc = p["key_scale" if which == "k" else "value_scale"]
+    sc = None if sc is None else sc.cpu()
+    if case.kv == synth.KV_BF16:
+        return c.view(torch.bfloat16).to(torch.float64)
+    if case.kv == synth.KV_FP8:
+        x = c.view(torch.float8_e4m3fn).to(torch.float64)
+        if case.scale == synth.SCALE_TENSOR:
+            return x * float(sc[0])
+        return x * sc.to(torch.float64)[..., None]
+    lo = (c & 15).long()
+    hi = (c >> 4).long()
+    nib = torch.stack([lo, hi], dim=-1).reshape(*c.shape[:-1], c.shape[-1] * 2)
+    table = torch.tensor(E2M1_TABLE + [-v for v in E2M1_TABLE], dtype=torch.float64)
+    vals = table[nib]
+    scale = sc.view(torch.float8_e8m0fnu).to(torch.float64)
+    return vals * scale.repeat_interleave(32, dim=-1)
+
+
+def _query_dense(p: dict) -> torch.Tensor:
+    case = p["case"]
+    q = p["query"].cpu()
+    if case.q == synth.Q_BF16:
+        return q.to(torch.float64)
+    return q.view(torch.float8_e4m3fn).to(torch.float64) * p["q_scale"].cpu().to(torch.float64)[..., None]
+
+
+def brute_force(p: dict, head_map=None) -> np.ndarray:
+    case = p["case"]
+    K = _dequant_dense(p, "k")
+    V = _dequant_dense(p, "v")
+    Q = _query_dense(p)
+    B, qlen, Hq, D = Q.shape
+    G = case.gqa
+    S = case.page_size
+    out = torch.zeros((B, qlen, Hq, D), dtype=torch.float64)
+    for s in range(B):
+        L = int(p["context_lens"][s])
+        if L == 0:
+            continue
+        t = torch.arange(L)
+        blk = p["block_tables"][s].long()[t // S]
+        for h in range(Hq):
+            hkv = h // G if head_map is None else head_map(h)
+            k = K[blk, hkv, t % S]          # [L, D]
+            v = V[blk, hkv, t % S]
+            for i in range(qlen):
+                x = (k @ Q[s, i, h]) * case.scale_qk()
+                w = torch.softmax(x, dim=0)
+                out[s, i, h] = w @ v
+    return out.numpy()
+
+
+def _tiny_cases():
+    return [
+        synth.config1(context_lens=[17, 40], seed=11),
+        synth.Case("t_fp8_tensor", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=3,
+                   qlen=2, num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                   context_lens=[1, 33, 50], fill=synth.FILL_INF, seed=12, kv_std=20.0),
+        synth.Case("t_fp8_token", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=2,
+                   qlen=1, num_kv_heads=2, num_q_heads=6, head_dim=64, page_size=16,
+                   context_lens=[31, 70], fill=synth.FILL_NAN, seed=13, kv_std=20.0),
+        synth.Case("t_mxfp4", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_E4M3, batch=2,
+                   qlen=1, num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
+                   context_lens=[20, 45], fill=synth.FILL_RANDOM, seed=14),
+        synth.Case("t_mxfp4_bfq", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=2,
+                   qlen=2, num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=32,
+                   context_lens=[33, 64], fill=synth.FILL_RANDOM, seed=15),
+    ]
+
+
+@pytest.mark.parametrize("case", _tiny_cases(), ids=lambda c: c.name)
+def test_bruteforce_dense(case):
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    ref = brute_force(p)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_bruteforce_detects_planted_mistakes():
+    """The brute-force pin is sensitive: planted slips on the oracle's side fail it."""
+    case = [c for c in _tiny_cases() if c.name == "t_mxfp4"][0]
+    p = synth.make(case)
+    ref = brute_force(p)
+    # (1) rolled e8m0 block scales (block/scale mix-up)
+    q = dict(p)
+    q["key_scale"] = torch.roll(p["key_scale"], 1, dims=-1)
+    assert util.rel_l2(util.oracle_decode(q), ref) > 1e-2
+    # (2) swapped nibbles (element order inside a byte)
+    q = dict(p)
+    q["value_cache"] = ((p["value_cache"] >> 4) | (p["value_cache"] << 4)).to(torch.uint8)
+    assert util.rel_l2(util.oracle_decode(q), ref) > 1e-2
+    # (3) a transposed GQA head mapping
+    c2 = synth.Case("t_gqa", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=1, qlen=1,
+                    num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                    context_lens=[40], seed=16, kv_std=20.0)
+    p2 = synth.make(c2)
+    wrong = brute_force(p2, head_map=lambda h: h % 2)
+    assert util.rel_l2(util.oracle_decode(p2), wrong) > 1e-2
+    # (4) a dropped per-tensor scale
+    q = dict(p2)
+    q["value_scale"] = torch.tensor([1.0])
+    assert util.rel_l2(util.oracle_decode(q), brute_force(p2)) > 1e-2
+
+
+# ---- closed forms -------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8, synth.KV_MXFP4])
+def test_context_one_returns_that_v_row(kv):
+    scale = {synth.KV_BF16: synth.SCALE_NONE, synth.KV_FP8: synth.SCALE_TOKEN,
+             synth.KV_MXFP4: synth.SCALE_E8M0}[kv]
+    case = synth.Case("ctx1", kv, scale, synth.Q_BF16, batch=2, qlen=1, num_kv_heads=2,
+                      num_q_heads=4, head_dim=64, page_size=16, context_lens=[1, 1],
+                      seed=21, kv_std=20.0)
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    V = _dequant_dense(p, "v")
+    for s in range(2):
+        blk = int(p["block_tables"][s, 0])
+        for h in range(4):
+            assert np.array_equal(got[s, 0, h], V[blk, h // 2, 0].numpy())
+
+
+def test_identical_keys_give_mean_of_v():
+    case = synth.Case("samek", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=1,
+                      qlen=1, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,
+                      context_lens=[37], seed=22, kv_std=20.0)
+    p = synth.make(case)
+    kc = p["key_cache"].clone()
+    row = kc[int(p["block_tables"][0, 0]), 0, 0].clone()
+    for t in range(37):
+        kc[int(p["block_tables"][0, t // 16]), 0, t % 16] = row
+    p["key_cache"] = kc
+    got = util.oracle_decode(p)
+    V = _dequant_dense(p, "v")
+    t = torch.arange(37)
+    blk = p["block_tables"][0].long()[t // 16]
+    mean = V[blk, 0, t % 16].mean(dim=0).numpy()
+    for h in range(2):
+        np.testing.assert_allclose(got[0, 0, h], mean, rtol=1e-13, atol=1e-13)
+
+
+def test_context_zero_gives_zero():
+    case = synth.config1(context_lens=[0, 17], seed=23)
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    assert np.all(got[0] == 0.0)
+    assert np.abs(got[1]).sum() > 0
+
+
+def test_split_merge_identity():
+    """Merging (m, l, o) of [0, a) and [a, L) reproduces the full softmax."""
+    case = synth.config3(qlen=2, context_lens=(60, 90), batch=2, seed=24)
+    p = synth.make(case)
+    prob = util.oracle_problem(p)
+    full = prob.decode()
+    L = int(p["context_lens"][1])
+    for a in (1, 17, L // 2, L - 1):
+        m1, l1, o1 = prob.attend_range(1, 1, 0, a)
+        m2, l2, o2 = prob.attend_range(1, 1, a, L)
+        M = np.maximum(m1, m2)
+        w1, w2 = l1 * np.exp(m1 - M), l2 * np.exp(m2 - M)
+        merged = (w1[:, None] * o1 + w2[:, None] * o2) / (w1 + w2)[:, None]
+        G = case.gqa
+        for r in range(case.qlen * G):
+            i, h = r // G, G + r % G
+            np.testing.assert_allclose(merged[r], full[1, i, h], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("make_case", [
+    lambda: synth.config1(seed=31),
+    lambda: synth.config2("a", batch=5, context_lens=[1, 17, 255, 257, 1000], seed=32),
+    lambda: synth.config3(qlen=1, batch=2, context_lens=(20, 300), seed=33),
+    lambda: synth.config4(batch=2, context_lens=[2000, 77], seed=34),
+], ids=["bf16", "fp8_tensor", "fp8_token", "mxfp4"])
+def test_unowned_rows_do_not_reach_output(make_case):
+    p = synth.make(make_case())
+    base = util.oracle_decode(synth.refill(p, synth.FILL_ZERO))
+    assert np.isfinite(base).all()
+    for fill in (synth.FILL_NAN, synth.FILL_INF, synth.FILL_RANDOM):
+        got = util.oracle_decode(synth.refill(p, fill))
+        assert np.array_equal(got, base), fill
+
+
+def test_oracle_refuses_bad_tables():
+    p = synth.make(synth.config1(seed=41))
+    bt = p["block_tables"].clone()
+    bt[0, 0] = p["num_blocks"]  # out of range
+    q = dict(p)
+    q["block_tables"] = bt
+    with pytest.raises(ValueError):
+        util.oracle_decode(q)

@@ -1,0 +1,69 @@
+"""Test helpers: hand the synthetic workload bytes to the oracle, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import pa_oracle as orc
+from paged_attention_decode_02_gb300 import synth
+
+_KV = {synth.KV_BF16: orc.KV_BF16, synth.KV_FP8: orc.KV_E4M3, synth.KV_MXFP4: orc.KV_MXFP4}
+_SC = {synth.SCALE_NONE: orc.SCALE_NONE, synth.SCALE_TENSOR: orc.SCALE_TENSOR,
+       synth.SCALE_TOKEN: orc.SCALE_TOKEN, synth.SCALE_E8M0: orc.SCALE_E8M0}
+_Q = {synth.Q_BF16: orc.Q_BF16, synth.Q_E4M3: orc.Q_E4M3}
+
+
+def cpu(t):
+    return None if t is None else t.detach().cpu()
+
+
+def oracle_problem(p: dict, seqs=None) -> orc.Problem:
+    """Oracle view of a synthetic problem; ``seqs`` restricts it to some sequences."""
+    case = p["case"]
+    bt, cl = cpu(p["block_tables"]), cpu(p["context_lens"])
+    q, qs = cpu(p["query"]), cpu(p["q_scale"])
+    batch = case.batch
+    if seqs is not None:
+        idx = torch.as_tensor(list(seqs), dtype=torch.long)
+        bt, cl, q = bt[idx], cl[idx], q[idx]
+        qs = qs[idx] if (qs is not None and qs.numel() > 1) else qs
+        batch = len(idx)
+    return orc.Problem(
+        batch=batch, qlen=case.qlen, num_q_heads=case.num_q_heads,
+        num_kv_heads=case.num_kv_heads, head_dim=case.head_dim, page_size=case.page_size,
+        num_blocks=p["num_blocks"], kv_format=_KV[case.kv], scale_kind=_SC[case.scale],
+        q_format=_Q[case.q], softmax_scale=case.scale_qk(), query=q,
+        key_cache=cpu(p["key_cache"]), value_cache=cpu(p["value_cache"]),
+        key_scale=cpu(p["key_scale"]), value_scale=cpu(p["value_scale"]), q_scale=qs,
+        block_tables=bt, context_lens=cl)
+
+
+def oracle_decode(p: dict, seqs=None, nthreads: int = 0) -> np.ndarray:
+    return oracle_problem(p, seqs).decode(nthreads)
+
+
+def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.linalg.norm(ref.ravel())
+    num = np.linalg.norm((got - ref).ravel())
+    return float(num / den) if den > 0 else float(num)
+
+
+def max_abs(got, ref) -> float:
+    d = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
+    return float(d.max()) if d.size else 0.0
+
+
+# Tolerances stated for the GPU path against the fp64 oracle.
+TOL_REL_L2 = {synth.KV_BF16: 5e-3, synth.KV_FP8: 3e-3, synth.KV_MXFP4: 3e-3}
+TOL_MAX_ABS = 3e-2
+
+
+def assert_parity(got, ref, kv: str, what: str = ""):
+    r = rel_l2(got, ref)
+    m = max_abs(got, ref)
+    assert np.isfinite(np.asarray(got, np.float64)).all(), f"{what}: non-finite output"
+    assert r <= TOL_REL_L2[kv], f"{what}: rel-L2 {r:.3e} > {TOL_REL_L2[kv]:.1e}"
+    assert m <= TOL_MAX_ABS, f"{what}: max-abs {m:.3e} > {TOL_MAX_ABS:.1e}"
+    return r, m
