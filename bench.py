@@ -1,0 +1,395 @@
+"""Benchmark of paged-attention decode on GB300 -- one JSON line on rank 0.
+
+A step is one pass of the whole decode path (plan -> tile kernel -> partition
+reduce) over the long-context decode workload, both KV variants of it:
+MXFP4 (e2m1 + e8m0 per 32) and fp8 e4m3 with per-token scales; batch 16, 1 KV
+head, GQA 16, head_dim 128, page 128, qlen 1, context lengths uniform in
+[120000, 131072], bf16 query and output.  Inputs are synthetic and seeded, resident
+in HBM before the timed region; each call streams 273 MB / 530 MB of KV, more
+than the 129 MB L2, so no flush is needed between steps.
+
+value  = algorithmic bytes of the step (owned-token KV + scales + Q + O + table)
+         / device time of the step, in GB/s, summed over ranks (replicas).
+e2e    = the same metric through the C ABI with host buffers: per step the query,
+         block tables and context lengths are copied from pinned host memory and
+         the output is copied back, inside the timed region (the KV cache is the
+         engine's resident state and stays in HBM).
+--impl reference times the fp64 CPU oracle on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_attention_decode_02_gb300 import ops, synth  # noqa: E402
+
+METRIC = "pa_decode µs/call and achieved KV GB/s (fraction of GB300 HBM peak)"
+WORKLOAD = ("long-context decode: MXFP4 and fp8-per-token KV, batch 16, 1 KV head, GQA 16, "
+            "head_dim 128, page 128, qlen 1, context_lens U[120000, 131072]")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile():
+    """dram bytes per launch of the fp8 per-token tile kernel from the committed ncu summary,
+    or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.strip().split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_attention_decode_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def make_variant(kv, device, batch=None):
+    case = synth.config5(kv) if batch is None else synth.config5(kv, batch=batch)
+    p = synth.make(case, device=device)
+    q = p["query"]
+    out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=device)
+    args = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"], p["context_lens"], out,
+                         key_scale=p["key_scale"], value_scale=p["value_scale"], q_scale=p["q_scale"],
+                         softmax_scale=case.scale_qk())
+    ws = ops.alloc_workspace(args, device)
+    lens = p["context_lens"].cpu().tolist()
+    return {"case": case, "p": p, "out": out, "args": args, "ws": ws,
+            "bytes": synth.algorithmic_bytes(case, lens), "lens": lens}
+
+
+def run_ours(a):
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_attention_decode_02_gb300 import build
+    build.build()
+    ops.load_library()
+    kinds = {"both": [synth.KV_MXFP4, synth.KV_FP8], "mxfp4": [synth.KV_MXFP4],
+             "fp8": [synth.KV_FP8]}[a.variant]
+    variants = [make_variant(k, dev, a.batch) for k in kinds]
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = peaks()
+
+    def step(ev=None):
+        for k, v in enumerate(variants):
+            ops.pa_decode_plan(v["args"], v["ws"], stream)
+            if ev is not None:
+                ev[k][0].record(stream)
+            ops.pa_decode(v["args"], v["ws"], stream)
+            if ev is not None:
+                ev[k][1].record(stream)
+            ops.pa_decode_reduce(v["args"], v["ws"], stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    for v in variants:
+        assert ops.pa_decode_read_status(v["ws"]) == 0, "device status"
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in variants]
+           for _ in range(a.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws_n > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        start.record(stream)
+        for i in range(a.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if ws_n > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(end)
+    tile_ms = [[evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(a.steps)]
+               for k in range(len(variants))]
+    if ws_n > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / a.steps
+    step_bytes = sum(v["bytes"] for v in variants)
+    value = step_bytes / (ms_step * 1e-3) / 1e9 * ws_n
+
+    # end to end through the C ABI with host buffers
+    host = []
+    for v in variants:
+        p = v["p"]
+        hq = p["query"].cpu().pin_memory()
+        hbt = p["block_tables"].cpu().pin_memory()
+        hcl = p["context_lens"].cpu().pin_memory()
+        hout = torch.empty(tuple(v["out"].shape), dtype=torch.bfloat16).pin_memory()
+        host.append((hq, hbt, hcl, hout))
+    h2d = sum(x[0].numel() * x[0].element_size() + x[1].numel() * 4 + x[2].numel() * 4 for x in host)
+    d2h = sum(x[3].numel() * 2 for x in host)
+
+    def e2e_step():
+        for v, (hq, hbt, hcl, hout) in zip(variants, host):
+            p = v["p"]
+            p["query"].copy_(hq, non_blocking=True)
+            p["block_tables"].copy_(hbt, non_blocking=True)
+            p["context_lens"].copy_(hcl, non_blocking=True)
+            ops.pa_decode_run(v["args"], v["ws"], stream)
+            hout.copy_(v["out"], non_blocking=True)
+
+    e2e = None
+    if not a.no_e2e:
+        for _ in range(a.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(a.steps):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = t0.elapsed_time(t1) / a.steps
+        e2e_val = step_bytes / (e2e_ms * 1e-3) / 1e9 * ws_n
+        e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    per = {}
+    for k, v in enumerate(variants):
+        med = statistics.median(tile_ms[k])
+        per[v["case"].name] = {
+            "tile_kernel_us": round(med * 1e3, 2),
+            "algorithmic_bytes": v["bytes"],
+            "tile_kernel_GBps": round(v["bytes"] / (med * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(v["bytes"] / (med * 1e-3) / 1e9 / peak, 4),
+        }
+    dom = variants[-1]
+    dom_ms = statistics.mean(tile_ms[-1])
+    achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_n,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 4),
+        "us_per_call": round(ms_step * 1e3 / len(variants), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; shapes and value distributions of the workload)",
+        "config": {"workload": WORKLOAD, "kv": ["mxfp4 e2m1+e8m0/32", "fp8 e4m3 per-token"],
+                   "global_batch": 16 * ws_n, "seq_len": "120000-131072",
+                   "parallelism": f"replicas x{ws_n}",
+                   "l2": "no flush: each call streams more than the 129 MB L2",
+                   "mma": "mma.sync m16n8k16 f16 x f16 -> f32"},
+        "per_variant": per,
+        "roofline": {"bound": "hbm", "kernel": f"pa_tile_kernel ({dom['case'].name})",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_from_profile()},
+        "e2e": e2e,
+        "gpu_launches": 3 * len(variants) * a.steps,
+        "clocks": clk.summary(),
+    }
+    if a.batch is not None or a.variant != "both":
+        line["config"]["note"] = "profiling subset, not the benchmark workload"
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(variants) if not a.no_cpu_baseline else None
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _oracle_problem(v, seqs):
+    """Oracle view of sequences `seqs` of a bench variant (bytes copied to the host)."""
+    from oracle import pa_oracle as orc
+    p, case = v["p"], v["case"]
+    idx = torch.as_tensor(seqs, dtype=torch.long)
+    kv = {synth.KV_MXFP4: orc.KV_MXFP4, synth.KV_FP8: orc.KV_E4M3}[case.kv]
+    sk = {synth.SCALE_E8M0: orc.SCALE_E8M0, synth.SCALE_TOKEN: orc.SCALE_TOKEN}[case.scale]
+    bt = p["block_tables"].cpu()[idx]
+    cl = p["context_lens"].cpu()[idx]
+    return orc.Problem(batch=len(seqs), qlen=case.qlen, num_q_heads=case.num_q_heads,
+                       num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+                       page_size=case.page_size, num_blocks=p["num_blocks"], kv_format=kv,
+                       scale_kind=sk, q_format=orc.Q_BF16, softmax_scale=case.scale_qk(),
+                       query=p["query"].cpu()[idx], key_cache=p["key_cache"].cpu(),
+                       value_cache=p["value_cache"].cpu(), key_scale=p["key_scale"].cpu(),
+                       value_scale=p["value_scale"].cpu(), block_tables=bt, context_lens=cl)
+
+
+def cpu_baseline(variants, nseq=None):
+    """The oracle as it stands, on the host cores, over a bounded sample of the workload."""
+    from oracle import pa_oracle as orc
+    threads = orc.max_threads()
+    nseq = nseq or max(1, min(16, threads))
+    total_bytes, total_s, lens_used = 0, 0.0, 0
+    for v in variants:
+        seqs = list(range(nseq))
+        prob = _oracle_problem(v, seqs)
+        t = time.perf_counter()
+        prob.decode()
+        total_s += time.perf_counter() - t
+        lens = [v["lens"][s] for s in seqs]
+        total_bytes += synth.algorithmic_bytes(v["case"], lens) * 0 + \
+            sum(lens) * v["case"].num_kv_heads * synth.kv_bytes_per_token(v["case"])
+        lens_used += sum(lens)
+    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"first {nseq} of 16 sequences of each KV variant ({lens_used} tokens), "
+                      f"{total_s:.1f} s of fp64 CPU work"}
+
+
+def run_reference(a):
+    """The oracle, timed on the host cores, as the reference arm."""
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import pa_oracle as orc
+    orc.build()
+    variants = []
+    for kv in (synth.KV_MXFP4, synth.KV_FP8):
+        case = synth.config5(kv)
+        p = synth.make(case)
+        variants.append({"case": case, "p": p, "lens": p["context_lens"].tolist()})
+    nseq = 2
+    probs = [_oracle_problem(v, list(range(nseq))) for v in variants]
+    sample_bytes = sum(sum(v["lens"][:nseq]) * synth.kv_bytes_per_token(v["case"]) for v in variants)
+    for _ in range(a.warmup):
+        for pr in probs:
+            pr.decode()
+    t = time.perf_counter()
+    for _ in range(a.steps):
+        for pr in probs:
+            pr.decode()
+    el = (time.perf_counter() - t) / a.steps
+    val = sample_bytes / el / 1e9
+    threads = orc.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "n_gpus": ws_n, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(el * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD, "sample": f"first {nseq} sequences of each KV variant"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"first {nseq} of 16 sequences of each KV variant per step"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", default="both", choices=["both", "mxfp4", "fp8"],
+                    help="KV variants of the long-context workload in a step (profiling: one)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller batch for profiling captures (default: the workload's 16)")
+    a = ap.parse_args()
+    if a.warmup < 3 and a.impl == "ours":
+        a.warmup = 3
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-attention decode library
+ * (libpa_decode.so).
+ *
+ * What the library computes.  For every sequence s, query position i < qlen and
+ * query head h (KV head hkv = h / G, G = num_q_heads / num_kv_heads):
+ *
+ *     out[s,i,h,:] = sum_{t < L_s} softmax_t(x_t) * v_t,
+ *     x_t = softmax_scale * q_scale * <q[s,i,h,:], k_t>,
+ *
+ * where token t of sequence s lives in page block_tables[s, t / page_size], slot
+ * t mod page_size, and L_s = context_lens[s].  Queries are not causally masked
+ * (every query position sees all L_s tokens).  References: "[FlyDSL] pa_decode:
+ * zero V rows past the context before PV" (Root cause, Fix) and "[FlyDSL]
+ * pa_decode: MXFP4 K/V in the shared PA tile kernel" (Summary, Self-Review).
+ *
+ * The work is cut into 256-token tiles (ceil(L_s / 256) per sequence); a plan
+ * groups consecutive tiles of one (sequence, KV head) into tasks, one task per
+ * partition of the context.  Tasks write partial (max, sum, output) triples
+ * that pa_decode_reduce merges; a sequence with a single partition is written
+ * directly.  Rows at or past L_s -- padded block-table columns pointing at any
+ * block and the unwritten tail of the last page -- never reach the output,
+ * whatever bytes they hold (NaN, Inf, e8m0 255): on the boundary tile their
+ * scores are replaced by -inf and their V values and per-token scales by 0.
+ *
+ * Conventions
+ *   - Every pointer in pa_decode_args is a DEVICE pointer; the caller owns all
+ *     memory, including the workspace.  The library allocates nothing.
+ *   - Calls never synchronise with the host and are stream-ordered on the given
+ *     stream (a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream).  Arguments are validated on the host before any launch; a
+ *     refused call launches nothing and returns a negative pa_status.
+ *   - Strides are in ELEMENTS for query/output/block tables and in BYTES for the
+ *     caches and scale caches.  The head_dim axis of query and output is
+ *     contiguous; one token row of a cache is contiguous (row_bytes below).
+ *
+ * Storage formats (kv_dtype, kv_scale):
+ *   PA_KV_BF16     + PA_SCALE_NONE        key/value bf16 [NB, Hkv, S, D]
+ *   PA_KV_FP8_E4M3 + PA_SCALE_PER_TENSOR  key/value OCP e4m3 bytes [NB, Hkv, S, D];
+ *                                         key_scale/value_scale fp32 [1]
+ *   PA_KV_FP8_E4M3 + PA_SCALE_PER_TOKEN   as above; key_scale/value_scale fp32
+ *                                         [NB, Hkv, S] (one per token and KV head)
+ *   PA_KV_MXFP4    + PA_SCALE_E8M0_32     key/value uint8 [NB, Hkv, S, D/2], two e2m1
+ *                                         per byte (element 2j in the low nibble);
+ *                                         key_scale/value_scale uint8 e8m0
+ *                                         [NB, Hkv, S, D/32], 2^(b-127) per 32 values
+ *   ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary: the MXFP4 page layout.)
+ *   row_bytes = 2D (bf16), D (e4m3), D/2 (MXFP4).  q_dtype PA_Q_BF16 reads a bf16
+ *   query; PA_Q_FP8_E4M3 reads e4m3 bytes multiplied by q_scale (fp32 [1], or
+ *   [B, qlen, Hq] when q_scale_per_row != 0).
+ *
+ * Supported shapes (others return PA_ERR_UNSUPPORTED): head_dim 128 or 256
+ * (MXFP4: 128); page_size 16, 32, 64, 128 or 256; G * qlen <= 32 (MXFP4: <= 16,
+ * qlen 1); kv_stride_token == row_bytes; 16-byte aligned cache, scale and
+ * stride values.
+ */
+#ifndef PA_DECODE_H_
+#define PA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pa_status;
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG (-1)   /* malformed argument: null pointer, bad shape */
+#define PA_ERR_UNSUPPORTED (-2)   /* well-formed, but not a combination this build serves */
+#define PA_ERR_WORKSPACE (-3)     /* workspace missing, too small or misaligned */
+#define PA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
+
+#define PA_KV_BF16 0
+#define PA_KV_FP8_E4M3 1
+#define PA_KV_MXFP4 2
+
+#define PA_SCALE_NONE 0
+#define PA_SCALE_PER_TENSOR 1
+#define PA_SCALE_PER_TOKEN 2
+#define PA_SCALE_E8M0_32 3
+
+#define PA_Q_BF16 0
+#define PA_Q_FP8_E4M3 1
+
+/* Device status word (first int32 of the workspace), read with pa_decode_read_status. */
+#define PA_DEVICE_OK 0
+#define PA_DEVICE_WAIT_TIMEOUT 1     /* a pipeline wait gave up; the output is not valid */
+#define PA_DEVICE_CONTEXT_CLAMPED 2  /* a context length exceeded the block table width */
+
+typedef struct pa_decode_args {
+  /* shapes */
+  int32_t batch;              /* B >= 0 sequences */
+  int32_t qlen;               /* query tokens per sequence, >= 1 */
+  int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;       /* Hkv >= 1 */
+  int32_t head_dim;           /* D */
+  int32_t page_size;          /* S, tokens per cache block */
+  int32_t num_blocks;         /* NB, blocks in each cache */
+  int32_t max_blocks_per_seq; /* block-table width W; context lengths are clamped to W*S */
+  /* formats */
+  int32_t kv_dtype;           /* PA_KV_* */
+  int32_t kv_scale;           /* PA_SCALE_* */
+  int32_t q_dtype;            /* PA_Q_* */
+  int32_t q_scale_per_row;    /* e4m3 query: 0 = q_scale[1], 1 = q_scale[B*qlen*Hq] */
+  float softmax_scale;        /* <= 0 selects 1/sqrt(head_dim) */
+  /* work split */
+  int32_t max_partitions;     /* >= 1 caps partitions per sequence; 1 = direct output, no
+                                 reduce; <= 0 picks a default from batch and the SM count */
+  int32_t task_budget;        /* target number of tasks; <= 0 picks a default */
+  int32_t reserved0;
+  /* tensors (device pointers) */
+  const void* query;          /* [B*qlen, Hq, D] bf16 or e4m3 */
+  int64_t q_stride_token;     /* elements between consecutive (s, i) rows */
+  int64_t q_stride_head;      /* elements between consecutive heads */
+  const float* q_scale;       /* e4m3 query only, else may be NULL */
+  const void* key_cache;
+  const void* value_cache;
+  int64_t kv_stride_block;    /* bytes between blocks (both caches) */
+  int64_t kv_stride_head;     /* bytes between KV heads within a block */
+  int64_t kv_stride_token;    /* bytes between token rows; must equal row_bytes */
+  const void* key_scale;      /* see the format table; NULL for PA_SCALE_NONE */
+  const void* value_scale;
+  int64_t scale_stride_block; /* per-token / e8m0 scale caches: bytes between blocks */
+  int64_t scale_stride_head;  /* bytes between KV heads; the token axis is dense */
+  const int32_t* block_tables;/* [B, W] */
+  int64_t bt_stride;          /* elements between block-table rows (>= W) */
+  const int32_t* context_lens;/* [B] */
+  void* out;                  /* [B*qlen, Hq, D] bf16 */
+  int64_t out_stride_token;
+  int64_t out_stride_head;
+} pa_decode_args;
+
+/* ABI version of this header; a mismatched library refuses nothing but reports it here. */
+#define PA_DECODE_ABI_VERSION 1
+int32_t pa_decode_abi_version(void);
+
+/* Bytes of workspace the three calls need for these shapes (plan, partition scratch,
+ * status word).  0 when the arguments are refused. Pure host arithmetic. */
+size_t pa_decode_workspace_size(const pa_decode_args* args);
+
+/* Host-side validation only (what every call checks before launching). */
+pa_status pa_decode_validate(const pa_decode_args* args);
+
+/* Builds the tile/partition work list on the device from context_lens: ceil(L/256)
+ * tiles per sequence, split into at most max_partitions near-equal tasks per
+ * (sequence, KV head) so that the total is close to task_budget.  Clears the device
+ * status word.  One launch, 1 CTA.  ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit
+ * messages: planned tasks, direct output with one partition, plan-free split.) */
+pa_status pa_decode_plan(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Runs the tile kernel over the planned tasks: block-table page gather (TMA), QK,
+ * online softmax, boundary-tile masking, PV.  Sequences with one partition get their
+ * output rows written here (context 0 gives zeros); others get partials in the
+ * workspace.  ("[FlyDSL] pa_decode: zero V rows past the context before PV", Fix.) */
+pa_status pa_decode(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* Merges the partials of every sequence with two or more partitions, in a fixed
+ * partition order: M = max_p m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
+ * A no-op launch-free return when max_partitions is 1.  ("[FlyDSL] pa_decode: MXFP4
+ * K/V ...", Self-Review: the partition reducer.) */
+pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* plan + decode + reduce in one call, on one stream. */
+pa_status pa_decode_run(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Enqueues a copy of the device status word (PA_DEVICE_*) into *host_status; the caller
+ * synchronises the stream before reading it. host_status should be pinned memory. */
+pa_status pa_decode_read_status(const void* workspace, int32_t* host_status, void* stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H_ */

@@ -1,0 +1,15 @@
+// bf16 KV specialisations of the tile kernel.
+#include "pa_configs.cuh"
+
+namespace pa {
+
+int launch_tile_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                     int grid_cap, int num_sms, void* stream) {
+  if (p.D == 128)
+    return p.R <= 16 ? launch_tile<CfgBf16D128M1>(p, tk, tv, grid_cap, num_sms, stream)
+                     : launch_tile<CfgBf16D128M2>(p, tk, tv, grid_cap, num_sms, stream);
+  return p.R <= 16 ? launch_tile<CfgBf16D256M1>(p, tk, tv, grid_cap, num_sms, stream)
+                   : launch_tile<CfgBf16D256M2>(p, tk, tv, grid_cap, num_sms, stream);
+}
+
+}  // namespace pa

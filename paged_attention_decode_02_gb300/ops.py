@@ -1,0 +1,258 @@
+"""ctypes binding of libpa_decode.so (see include/pa_decode.h).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (torch supplies device memory and the
+current stream); the library allocates nothing.  If the shared library is missing
+the calls raise -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa_decode.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1, -2, -3, -4
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_MXFP4 = 0, 1, 2
+PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN, PA_SCALE_E8M0_32 = 0, 1, 2, 3
+PA_Q_BF16, PA_Q_FP8_E4M3 = 0, 1
+PA_DEVICE_WAIT_TIMEOUT, PA_DEVICE_CONTEXT_CLAMPED = 1, 2
+
+EXPORTED = ["pa_decode_abi_version", "pa_decode_workspace_size", "pa_decode_validate",
+            "pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run",
+            "pa_decode_read_status", "pa_status_string"]
+
+
+class PaDecodeArgs(ctypes.Structure):
+    """Mirror of ``pa_decode_args``."""
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("qlen", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("kv_scale", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
+        ("q_scale_per_row", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+        ("max_partitions", ctypes.c_int32), ("task_budget", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("query", ctypes.c_void_p), ("q_stride_token", ctypes.c_int64),
+        ("q_stride_head", ctypes.c_int64), ("q_scale", ctypes.c_void_p),
+        ("key_cache", ctypes.c_void_p), ("value_cache", ctypes.c_void_p),
+        ("kv_stride_block", ctypes.c_int64), ("kv_stride_head", ctypes.c_int64),
+        ("kv_stride_token", ctypes.c_int64), ("key_scale", ctypes.c_void_p),
+        ("value_scale", ctypes.c_void_p), ("scale_stride_block", ctypes.c_int64),
+        ("scale_stride_head", ctypes.c_int64), ("block_tables", ctypes.c_void_p),
+        ("bt_stride", ctypes.c_int64), ("context_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
+        ("out_stride_head", ctypes.c_int64),
+    ]
+
+
+class PaDecodeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Open libpa_decode.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with "
+                               "paged_attention_decode_02_gb300.build.build()")
+        L = ctypes.CDLL(p)
+        A = ctypes.POINTER(PaDecodeArgs)
+        L.pa_decode_abi_version.restype = ctypes.c_int32
+        L.pa_decode_workspace_size.argtypes = [A]
+        L.pa_decode_workspace_size.restype = ctypes.c_size_t
+        L.pa_decode_validate.argtypes = [A]
+        L.pa_decode_validate.restype = ctypes.c_int32
+        for name in ("pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run"):
+            f = getattr(L, name)
+            f.argtypes = [A, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            f.restype = ctypes.c_int32
+        L.pa_decode_read_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.pa_decode_read_status.restype = ctypes.c_int32
+        L.pa_status_string.argtypes = [ctypes.c_int32]
+        L.pa_status_string.restype = ctypes.c_char_p
+        if path is None:
+            _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().pa_status_string(status).decode()
+    except Exception:  # library not built: still give a readable message
+        return {0: "ok", -1: "invalid argument", -2: "unsupported combination",
+                -3: "workspace", -4: "CUDA error"}.get(status, "unknown status")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor, out: torch.Tensor, *,
+              key_scale: Optional[torch.Tensor] = None, value_scale: Optional[torch.Tensor] = None,
+              q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
+              max_partitions: int = 0, task_budget: int = 0) -> PaDecodeArgs:
+    """Describe one decode call.
+
+    query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
+    (torch.float8_e4m3fn or uint8 bytes with ``q_scale``); out bf16.
+    key_cache / value_cache: [NB, Hkv, S, D] bf16, [NB, Hkv, S, D] e4m3 bytes
+    (uint8 / float8_e4m3fn) with fp32 scales [1] (per tensor) or [NB, Hkv, S]
+    (per token), or [NB, Hkv, S, D/2] uint8 MXFP4 with uint8 e8m0 scales
+    [NB, Hkv, S, D/32].  block_tables int32 [B, W]; context_lens int32 [B].
+    """
+    D = query.shape[-1]
+    Hq = query.shape[-2]
+    if query.dim() == 4:
+        B, qlen = query.shape[0], query.shape[1]
+        q_st, q_sh = query.stride(1), query.stride(2)
+        if query.stride(0) != qlen * q_st:
+            raise ValueError("query sequence and position axes must be fused-contiguous")
+    else:
+        B, qlen = block_tables.shape[0], query.shape[0] // max(1, block_tables.shape[0])
+        q_st, q_sh = query.stride(0), query.stride(1)
+    o_st = out.stride(-3) if out.dim() == 3 else out.stride(1)
+    o_sh = out.stride(-2)
+    NB, Hkv, S = key_cache.shape[0], key_cache.shape[1], key_cache.shape[2]
+    a = PaDecodeArgs()
+    a.batch, a.qlen, a.num_q_heads, a.num_kv_heads = B, qlen, Hq, Hkv
+    a.head_dim, a.page_size, a.num_blocks = D, S, NB
+    a.max_blocks_per_seq = block_tables.shape[1]
+    if key_cache.dtype == torch.bfloat16:
+        a.kv_dtype, a.kv_scale = PA_KV_BF16, PA_SCALE_NONE
+    elif key_cache.shape[-1] == D:
+        a.kv_dtype = PA_KV_FP8_E4M3
+        if key_scale is None or value_scale is None:
+            raise ValueError("fp8 KV needs key_scale and value_scale")
+        a.kv_scale = PA_SCALE_PER_TENSOR if key_scale.numel() == 1 else PA_SCALE_PER_TOKEN
+    elif key_cache.shape[-1] * 2 == D:
+        a.kv_dtype, a.kv_scale = PA_KV_MXFP4, PA_SCALE_E8M0_32
+    else:
+        raise ValueError(f"cannot infer the KV format from {tuple(key_cache.shape)} and D={D}")
+    a.q_dtype = PA_Q_BF16 if query.dtype == torch.bfloat16 else PA_Q_FP8_E4M3
+    a.q_scale_per_row = int(q_scale is not None and q_scale.numel() > 1)
+    a.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)
+    a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
+    a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
+    a.q_scale = _ptr(q_scale)
+    es = key_cache.element_size()
+    a.key_cache, a.value_cache = _ptr(key_cache), _ptr(value_cache)
+    if value_cache.stride() != key_cache.stride():
+        raise ValueError("key and value caches must share strides")
+    a.kv_stride_block = key_cache.stride(0) * es
+    a.kv_stride_head = key_cache.stride(1) * es
+    a.kv_stride_token = key_cache.stride(2) * es
+    a.key_scale, a.value_scale = _ptr(key_scale), _ptr(value_scale)
+    if a.kv_scale in (PA_SCALE_PER_TOKEN, PA_SCALE_E8M0_32):
+        ses = key_scale.element_size()
+        a.scale_stride_block = key_scale.stride(0) * ses
+        a.scale_stride_head = key_scale.stride(1) * ses
+    a.block_tables, a.bt_stride = _ptr(block_tables), block_tables.stride(0)
+    a.context_lens = _ptr(context_lens)
+    a.out, a.out_stride_token, a.out_stride_head = _ptr(out), o_st, o_sh
+    return a
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PaDecodeError(status, what)
+
+
+def pa_decode_validate(args: PaDecodeArgs) -> int:
+    return load_library().pa_decode_validate(ctypes.byref(args))
+
+
+def pa_decode_workspace_size(args: PaDecodeArgs) -> int:
+    n = load_library().pa_decode_workspace_size(ctypes.byref(args))
+    if n == 0:
+        _check(pa_decode_validate(args) or PA_ERR_CUDA, "pa_decode_workspace_size")
+    return n
+
+
+def alloc_workspace(args: PaDecodeArgs, device=None) -> torch.Tensor:
+    """Caller-side workspace allocation (torch memory, 256-byte aligned)."""
+    n = pa_decode_workspace_size(args)
+    return torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(workspace: torch.Tensor):
+    base = workspace.data_ptr()
+    off = (-base) % 256
+    return base + off, workspace.numel() - off
+
+
+def pa_decode_plan(args: PaDecodeArgs, workspace: torch.Tensor, stream=None):
+    p, n = _ws(workspace)
+    _check(load_library().pa_decode_plan(ctypes.byref(args), p, n, _stream_handle(stream)),
+           "pa_decode_plan")
+
+
+def pa_decode(args: PaDecodeArgs, workspace: torch.Tensor, stream=None):
+    p, n = _ws(workspace)
+    _check(load_library().pa_decode(ctypes.byref(args), p, n, _stream_handle(stream)), "pa_decode")
+
+
+def pa_decode_reduce(args: PaDecodeArgs, workspace: torch.Tensor, stream=None):
+    p, n = _ws(workspace)
+    _check(load_library().pa_decode_reduce(ctypes.byref(args), p, n, _stream_handle(stream)),
+           "pa_decode_reduce")
+
+
+def pa_decode_run(args: PaDecodeArgs, workspace: torch.Tensor, stream=None):
+    p, n = _ws(workspace)
+    _check(load_library().pa_decode_run(ctypes.byref(args), p, n, _stream_handle(stream)),
+           "pa_decode_run")
+
+
+def pa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
+    """Device status word (PA_DEVICE_* bits); synchronises the stream."""
+    host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    p, _ = _ws(workspace)
+    _check(load_library().pa_decode_read_status(p, host.data_ptr(), _stream_handle(stream)),
+           "pa_decode_read_status")
+    (stream or torch.cuda.current_stream()).synchronize()
+    return int(host.item())
+
+
+def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions: int = 0,
+           task_budget: int = 0, workspace: Optional[torch.Tensor] = None):
+    """plan + decode + reduce on a synthetic-workload dict (device tensors)."""
+    case = problem["case"]
+    q = problem["query"]
+    if q.dtype == torch.uint8:
+        q = q.view(torch.float8_e4m3fn)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    args = make_args(q, problem["key_cache"], problem["value_cache"], problem["block_tables"],
+                     problem["context_lens"], out, key_scale=problem["key_scale"],
+                     value_scale=problem["value_scale"], q_scale=problem["q_scale"],
+                     softmax_scale=case.scale_qk(), max_partitions=max_partitions,
+                     task_budget=task_budget)
+    if workspace is None:
+        workspace = alloc_workspace(args, q.device)
+    pa_decode_run(args, workspace)
+    return out, args, workspace

@@ -1,0 +1,127 @@
+"""The C ABI: the library loads, exports what include/pa_decode.h declares, and refuses
+malformed or unsupported arguments on the host (no GPU work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_attention_decode_02_gb300 import build, ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pa_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported(lib):
+    names = declared_functions()
+    assert set(ops.EXPORTED) == set(names), names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.pa_decode_abi_version() == 1
+
+
+def test_args_struct_layout_matches_header():
+    # 16 int32/float fields, then pointers and int64s
+    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 19 * 8
+    assert ops.PaDecodeArgs.query.offset == 64
+
+
+def _valid_args():
+    a = ops.PaDecodeArgs()
+    a.batch, a.qlen, a.num_q_heads, a.num_kv_heads = 4, 1, 16, 1
+    a.head_dim, a.page_size, a.num_blocks, a.max_blocks_per_seq = 128, 128, 64, 16
+    a.kv_dtype, a.kv_scale, a.q_dtype = ops.PA_KV_FP8_E4M3, ops.PA_SCALE_PER_TOKEN, ops.PA_Q_BF16
+    a.softmax_scale, a.max_partitions, a.task_budget = 0.0, 0, 152
+    fake = 1 << 20  # host-side validation never dereferences pointers
+    a.query, a.q_stride_token, a.q_stride_head = fake, 16 * 128, 128
+    a.key_cache, a.value_cache = fake, fake * 2
+    a.kv_stride_token, a.kv_stride_head = 128, 128 * 128
+    a.kv_stride_block = 128 * 128
+    a.key_scale, a.value_scale = fake * 3, fake * 4
+    a.scale_stride_head, a.scale_stride_block = 128 * 4, 128 * 4
+    a.block_tables, a.bt_stride, a.context_lens = fake * 5, 16, fake * 6
+    a.out, a.out_stride_token, a.out_stride_head = fake * 7, 16 * 128, 128
+    return a
+
+
+def test_valid_arguments_pass(lib):
+    a = _valid_args()
+    assert ops.pa_decode_validate(a) == ops.PA_OK
+    assert ops.pa_decode_workspace_size(a) > 0
+
+
+REFUSED = [
+    ("head_dim 64", dict(head_dim=64), ops.PA_ERR_UNSUPPORTED),
+    ("page 48", dict(page_size=48), ops.PA_ERR_UNSUPPORTED),
+    ("Hq not a multiple of Hkv", dict(num_q_heads=15, num_kv_heads=2), ops.PA_ERR_INVALID_ARG),
+    ("qlen 0", dict(qlen=0), ops.PA_ERR_INVALID_ARG),
+    ("G*qlen > 32", dict(qlen=3), ops.PA_ERR_UNSUPPORTED),
+    ("bf16 with scales", dict(kv_dtype=ops.PA_KV_BF16), ops.PA_ERR_UNSUPPORTED),
+    ("fp8 with e8m0", dict(kv_scale=ops.PA_SCALE_E8M0_32), ops.PA_ERR_UNSUPPORTED),
+    ("mxfp4 qlen 2", dict(kv_dtype=ops.PA_KV_MXFP4, kv_scale=ops.PA_SCALE_E8M0_32, qlen=2,
+                          kv_stride_token=64, kv_stride_head=64 * 128, kv_stride_block=64 * 128),
+     ops.PA_ERR_UNSUPPORTED),
+    ("unknown kv dtype", dict(kv_dtype=7), ops.PA_ERR_INVALID_ARG),
+    ("null query", dict(query=None), ops.PA_ERR_INVALID_ARG),
+    ("null scales", dict(key_scale=None), ops.PA_ERR_INVALID_ARG),
+    ("e4m3 query without scale", dict(q_dtype=ops.PA_Q_FP8_E4M3), ops.PA_ERR_INVALID_ARG),
+    ("non-dense token rows", dict(kv_stride_token=256, kv_stride_head=256 * 128,
+                                  kv_stride_block=256 * 128), ops.PA_ERR_UNSUPPORTED),
+    ("overlapping heads", dict(kv_stride_head=64), ops.PA_ERR_INVALID_ARG),
+    ("unaligned head stride", dict(kv_stride_head=128 * 128 + 8, kv_stride_block=2 * 128 * 128),
+     ops.PA_ERR_UNSUPPORTED),
+    ("unaligned cache", dict(key_cache=(1 << 20) + 8), ops.PA_ERR_UNSUPPORTED),
+    ("block table stride < width", dict(bt_stride=8), ops.PA_ERR_INVALID_ARG),
+    ("short scale head stride", dict(scale_stride_head=16), ops.PA_ERR_INVALID_ARG),
+    ("query head stride < D", dict(q_stride_head=64), ops.PA_ERR_INVALID_ARG),
+    ("table span beyond 2^30 tokens", dict(max_blocks_per_seq=1 << 24, bt_stride=1 << 24),
+     ops.PA_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("what,changes,status", REFUSED, ids=[r[0] for r in REFUSED])
+def test_refused_arguments(lib, what, changes, status):
+    a = _valid_args()
+    for k, v in changes.items():
+        setattr(a, k, v)
+    assert ops.pa_decode_validate(a) == status
+    assert lib.pa_decode_workspace_size(ctypes.byref(a)) == 0
+    # every entry point refuses before touching the device
+    for fn in ("pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run"):
+        assert getattr(lib, fn)(ctypes.byref(a), 1 << 20, 1 << 30, None) == status
+
+
+def test_workspace_too_small_is_refused(lib):
+    a = _valid_args()
+    n = ops.pa_decode_workspace_size(a)
+    assert lib.pa_decode_plan(ctypes.byref(a), 1 << 20, n - 1, None) == ops.PA_ERR_WORKSPACE
+    assert lib.pa_decode(ctypes.byref(a), (1 << 20) + 16, n, None) == ops.PA_ERR_WORKSPACE
+    assert lib.pa_decode_reduce(ctypes.byref(a), None, n, None) == ops.PA_ERR_WORKSPACE
+
+
+def test_workspace_grows_with_budget_and_rows(lib):
+    a = _valid_args()
+    n1 = ops.pa_decode_workspace_size(a)
+    a.task_budget = 304
+    n2 = ops.pa_decode_workspace_size(a)
+    assert n2 > n1
+    a.max_partitions = 1  # direct output needs no partial scratch
+    n3 = ops.pa_decode_workspace_size(a)
+    assert n3 < n1
+
+
+def test_status_strings(lib):
+    for s in (0, -1, -2, -3, -4):
+        assert lib.pa_status_string(s)

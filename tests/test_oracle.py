@@ -292,3 +292,24 @@ def test_oracle_refuses_bad_tables():
     q["block_tables"] = bt
     with pytest.raises(ValueError):
         util.oracle_decode(q)
+
+
+def test_parity_checker_catches_planted_errors():
+    """The comparison itself: an oracle-side perturbation of 0.05 at one element, a NaN,
+    or a dropped V scale must fail it, while the bf16 rounding of the oracle passes."""
+    p = synth.make(synth.config3(qlen=1, batch=2, context_lens=(40, 90), seed=51))
+    ref = util.oracle_decode(p)
+    rounded = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    util.assert_parity(rounded, ref, synth.KV_FP8)
+    bad = ref.copy()
+    bad[1, 0, 3, 17] += 0.05
+    with pytest.raises(AssertionError):
+        util.assert_parity(bad, ref, synth.KV_FP8)
+    bad = ref.copy()
+    bad[0, 0, 0, 0] = np.nan
+    with pytest.raises(AssertionError):
+        util.assert_parity(bad, ref, synth.KV_FP8)
+    q = dict(p)
+    q["value_scale"] = p["value_scale"] * 1.05
+    with pytest.raises(AssertionError):
+        util.assert_parity(util.oracle_decode(q), ref, synth.KV_FP8)
