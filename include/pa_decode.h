@@ -168,6 +168,22 @@ pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
 pa_status pa_decode_run(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* Fixed size of the library-owned workspace used by pa_decode_run_static. */
+#define PA_DECODE_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+/* No counterpart in the source pages.  The same plan + decode + reduce as pa_decode_run,
+ * for callers that cannot call cudaMalloc (code running inside another runtime's memory
+ * budget, or latency-critical loops where an allocation may synchronise the device): the
+ * workspace is a fixed PA_DECODE_STATIC_WORKSPACE_BYTES array in device memory that the
+ * library defines, so this call allocates nothing; the caller still passes the inputs and
+ * the output in args.  Returns PA_ERR_WORKSPACE when the problem needs more workspace than
+ * that maximum (pa_decode_workspace_size tells how much it needs).  Every GPU that loads the
+ * library holds the array until the process exits.  The first call on a device looks up the
+ * array's device address with that device current; make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the previous call's contents:
+ * calls that overlap on the GPU race on it. */
+pa_status pa_decode_run_static(const pa_decode_args* args, void* stream);
+
 /* Enqueues a copy of the device status word (PA_DEVICE_*) into *host_status; the caller
  * synchronises the stream before reading it. host_status should be pinned memory. */
 pa_status pa_decode_read_status(const void* workspace, int32_t* host_status, void* stream);

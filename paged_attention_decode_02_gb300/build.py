@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_decode.so")
-SOURCES = ["pa_decode.cu", "pa_tile_bf16.cu", "pa_tile_fp8.cu", "pa_tile_mxfp4.cu"]
+SOURCES = ["pa_decode.cu", "pa_tile_bf16.cu", "pa_tile_fp8.cu", "pa_tile_mxfp4.cu",
+           "pa_decode_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -26,7 +26,8 @@ PA_DEVICE_WAIT_TIMEOUT, PA_DEVICE_CONTEXT_CLAMPED = 1, 2
 
 EXPORTED = ["pa_decode_abi_version", "pa_decode_workspace_size", "pa_decode_validate",
             "pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run",
-            "pa_decode_read_status", "pa_status_string"]
+            "pa_decode_read_status", "pa_status_string", "pa_decode_run_static"]
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class PaDecodeArgs(ctypes.Structure):
@@ -84,6 +85,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = [A, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             f.restype = ctypes.c_int32
+        L.pa_decode_run_static.argtypes = [A, ctypes.c_void_p]
+        L.pa_decode_run_static.restype = ctypes.c_int32
         L.pa_decode_read_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.pa_decode_read_status.restype = ctypes.c_int32
         L.pa_status_string.argtypes = [ctypes.c_int32]
@@ -226,6 +229,17 @@ def pa_decode_run(args: PaDecodeArgs, workspace: torch.Tensor, stream=None):
     p, n = _ws(workspace)
     _check(load_library().pa_decode_run(ctypes.byref(args), p, n, _stream_handle(stream)),
            "pa_decode_run")
+
+
+def pa_decode_run_static(args: PaDecodeArgs, stream=None):
+    """plan + decode + reduce with the library's fixed device workspace, for callers that
+    cannot allocate device memory (see include/pa_decode.h).  Nothing is allocated."""
+    status = load_library().pa_decode_run_static(ctypes.byref(args), _stream_handle(stream))
+    if status == PA_ERR_WORKSPACE:
+        raise PaDecodeError(status, f"pa_decode_run_static: the problem needs "
+                                    f"{pa_decode_workspace_size(args)} bytes of workspace, more "
+                                    f"than the fixed {STATIC_WORKSPACE_BYTES}")
+    _check(status, "pa_decode_run_static")
 
 
 def pa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
