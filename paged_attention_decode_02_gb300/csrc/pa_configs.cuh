@@ -1,22 +1,23 @@
 // pa_configs.cuh -- the tile-kernel specialisations this library builds.
 //
-// TileCfg<format, head_dim, m-tiles (query rows / 16), token groups, warps per
-// row (head-dim split), tokens per pipeline stage, stages>.  A stage holds about
-// 32 KiB of K+V; one persistent CTA per SM.
+// TileCfg<format, scale kind, head_dim, m-tiles (query rows / 16), token groups, warps per
+// token group (head-dim split), tokens per warp slice, slots per warp ring>.  One
+// persistent CTA per SM; every warp streams its own slices.  The long-context shapes
+// (fp8 / MXFP4, head_dim 128, up to 16 query rows) run eight warps, two per scheduler.
 #pragma once
 
 #include "pa_tile.cuh"
 
 namespace pa {
 
-using CfgBf16D128M1 = TileCfg<KIND_BF16, 128, 1, 4, 1, 64, 4>;
-using CfgBf16D128M2 = TileCfg<KIND_BF16, 128, 2, 4, 1, 64, 4>;
-using CfgBf16D256M1 = TileCfg<KIND_BF16, 256, 1, 2, 2, 32, 4>;
-using CfgBf16D256M2 = TileCfg<KIND_BF16, 256, 2, 2, 2, 32, 4>;
-using CfgFp8D128M1 = TileCfg<KIND_FP8, 128, 1, 4, 1, 128, 4>;
-using CfgFp8D128M2 = TileCfg<KIND_FP8, 128, 2, 4, 1, 128, 4>;
-using CfgFp8D256M1 = TileCfg<KIND_FP8, 256, 1, 2, 2, 64, 4>;
-using CfgFp8D256M2 = TileCfg<KIND_FP8, 256, 2, 2, 2, 64, 4>;
-using CfgFp4D128M1 = TileCfg<KIND_FP4, 128, 1, 4, 1, 256, 4>;
+using CfgBf16D128M1 = TileCfg<KIND_BF16, SK_NONE, 128, 1, 8, 1, 16, 3>;
+using CfgBf16D128M2 = TileCfg<KIND_BF16, SK_NONE, 128, 2, 4, 1, 16, 4>;
+using CfgBf16D256M1 = TileCfg<KIND_BF16, SK_NONE, 256, 1, 2, 2, 16, 4>;
+using CfgBf16D256M2 = TileCfg<KIND_BF16, SK_NONE, 256, 2, 2, 2, 16, 4>;
+template <int SKT> using CfgFp8D128M1 = TileCfg<KIND_FP8, SKT, 128, 1, 8, 1, 32, 3>;
+template <int SKT> using CfgFp8D128M2 = TileCfg<KIND_FP8, SKT, 128, 2, 8, 1, 16, 4>;
+template <int SKT> using CfgFp8D256M1 = TileCfg<KIND_FP8, SKT, 256, 1, 2, 2, 32, 4>;
+template <int SKT> using CfgFp8D256M2 = TileCfg<KIND_FP8, SKT, 256, 2, 4, 2, 16, 3>;
+using CfgFp4D128M1 = TileCfg<KIND_FP4, SK_E8M0, 128, 1, 8, 1, 32, 5>;
 
 }  // namespace pa

@@ -128,43 +128,59 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   const int r = i * rp.G + h % rp.G;
   const long long base = (long long)rp.part_base[s] + (long long)hkv * P;
   const float2* ml = reinterpret_cast<const float2*>(rp.part_ml);
+  // M and the total weight: lane-strided partials, then a fixed shuffle tree
   float M = -INFINITY;
-  for (int q = 0; q < P; ++q) M = fmaxf(M, ml[(base + q) * rp.R + r].x);
+  for (int q = lane; q < P; q += 32) M = fmaxf(M, ml[(base + q) * rp.R + r].x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float mb = M == -INFINITY ? 0.f : M;
   float W = 0.f;
-  for (int q = 0; q < P; ++q) {
+  for (int q = lane; q < P; q += 32) {
     const float2 e = ml[(base + q) * rp.R + r];
     W += e.y * fast_exp2(e.x - mb);
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
   const float inv = W > 0.f ? 1.f / W : 0.f;
   __nv_bfloat16* dst = rp.out + (long long)(s * rp.qlen + i) * rp.o_st + (long long)h * rp.o_sh;
-  for (int d = lane; d < rp.D; d += 32) {
-    float acc = 0.f;
+  // each lane owns 4 consecutive dims per 128; partitions are added in a fixed order
+  for (int d0 = 4 * lane; d0 < rp.D; d0 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < P; ++q) {
       const float2 e = ml[(base + q) * rp.R + r];
-      acc += e.y * fast_exp2(e.x - mb) * rp.part_o[((base + q) * rp.R + r) * rp.D + d];
+      const float w = e.y * fast_exp2(e.x - mb);
+      const float4 v = *reinterpret_cast<const float4*>(rp.part_o + ((base + q) * rp.R + r) * rp.D + d0);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
-    dst[d] = __float2bfloat16_rn(acc * inv);
+    dst[d0] = __float2bfloat16_rn(acc.x * inv);
+    dst[d0 + 1] = __float2bfloat16_rn(acc.y * inv);
+    dst[d0 + 2] = __float2bfloat16_rn(acc.z * inv);
+    dst[d0 + 3] = __float2bfloat16_rn(acc.w * inv);
   }
 }
 
-void tile_geometry(int kind, int head_dim, int rows, int* tc, int* sub) {
+// Tokens per warp slice (the TMA box is min(S, this) rows high) and swizzle span of the
+// tile kernel that serves a format / head_dim / query-row count.
+void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub) {
   if (kind == KIND_BF16) {
     if (head_dim == 128) {
-      *tc = rows <= 16 ? CfgBf16D128M1::TC : CfgBf16D128M2::TC;
+      *tw = rows <= 16 ? CfgBf16D128M1::TW : CfgBf16D128M2::TW;
     } else {
-      *tc = rows <= 16 ? CfgBf16D256M1::TC : CfgBf16D256M2::TC;
+      *tw = rows <= 16 ? CfgBf16D256M1::TW : CfgBf16D256M2::TW;
     }
     *sub = 128;
   } else if (kind == KIND_FP8) {
     if (head_dim == 128) {
-      *tc = rows <= 16 ? CfgFp8D128M1::TC : CfgFp8D128M2::TC;
+      *tw = rows <= 16 ? CfgFp8D128M1<SK_TOKEN>::TW : CfgFp8D128M2<SK_TOKEN>::TW;
     } else {
-      *tc = rows <= 16 ? CfgFp8D256M1::TC : CfgFp8D256M2::TC;
+      *tw = rows <= 16 ? CfgFp8D256M1<SK_TOKEN>::TW : CfgFp8D256M2<SK_TOKEN>::TW;
     }
     *sub = 128;
   } else {
-    *tc = CfgFp4D128M1::TC;
+    *tw = CfgFp4D128M1::TW;
     *sub = CfgFp4D128M1::SUB;
   }
 }

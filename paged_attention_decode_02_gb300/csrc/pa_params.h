@@ -90,8 +90,8 @@ int launch_tile_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensor
 int launch_tile_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                       int grid_cap, int num_sms, void* stream);
 
-// Tokens per pipeline stage and swizzle span (bytes) of the tile kernel chosen for a
-// format / head_dim / query-row count; the TMA box is min(S, stage tokens) rows high.
-void tile_geometry(int kind, int head_dim, int rows, int* stage_tokens, int* swizzle_bytes);
+// Tokens per warp slice and swizzle span (bytes) of the tile kernel chosen for a
+// format / head_dim / query-row count; the TMA box is min(S, slice tokens) rows high.
+void tile_geometry(int kind, int head_dim, int rows, int* slice_tokens, int* swizzle_bytes);
 
 }  // namespace pa

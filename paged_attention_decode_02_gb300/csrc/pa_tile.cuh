@@ -1,19 +1,20 @@
 // pa_tile.cuh -- the sm_103a paged-attention decode tile kernel.
 //
 // One persistent CTA walks planned tasks (runs of 256-token tiles of one sequence
-// and KV head).  A producer warp gathers the pages of each pipeline stage through the
-// block table with TMA (K and V sub-tiles land 128-/64-byte swizzled; per-token or
-// e8m0 scales arrive by 1-D bulk copy) into a ring of mbarrier-guarded stages.
-// Consumer warps each own a token slice of every stage, so softmax state and the
-// output accumulators are warp-private; they compute QK^T and PV with mma.sync
-// (m16n8k16, fp32 accumulate), converting fp8 / fp4 operands to f16 in registers.
-// Only a stage holding tokens at or past the context length runs the masked path:
-// scores there become -inf, and V values and per-token scales become 0 by select,
-// so unowned rows never reach the output whatever bytes they hold
-// ("[FlyDSL] pa_decode: zero V rows past the context before PV", Fix).
-// At the end of a task the warps merge their (max, sum, output) in a fixed order and
-// either store the final bf16 row (single-partition sequences) or a partial for the
-// reduce kernel ("[FlyDSL] pa_decode: MXFP4 K/V ...", direct output commit).
+// and KV head).  Every warp owns a token slice of each CTA stage and runs its own
+// pipeline: it gathers its slice's pages through the block table with TMA (K and V
+// land 128- or 64-byte swizzled; per-token or e8m0 scales arrive by 1-D bulk copy)
+// into a private ring of mbarrier-guarded slots, NSTAGE slices ahead of the one it
+// computes, so no warp ever waits for another inside a task.  Softmax state and the
+// output accumulators are warp-private; QK^T and PV run on mma.sync (m16n8k16, fp32
+// accumulate) with fp8 / fp4 operands widened to f16 in registers.  Only a slice
+// holding tokens at or past the context length runs the masked path: scores there
+// become -inf, and V values and per-token scales become 0 by select, so unowned rows
+// never reach the output whatever bytes they hold ("[FlyDSL] pa_decode: zero V rows
+// past the context before PV", Fix).  At the end of a task the warps merge their
+// (max, sum, output) in a fixed order and store either the final bf16 row (sequences
+// with one partition) or a partial for the reduce kernel ("[FlyDSL] pa_decode: MXFP4
+// K/V ...", direct output commit).
 #pragma once
 
 #include "pa_params.h"
@@ -25,30 +26,39 @@ enum { KIND_BF16 = 0, KIND_FP8 = 1, KIND_FP4 = 2 };
 enum { SK_NONE = 0, SK_TENSOR = 1, SK_TOKEN = 2, SK_E8M0 = 3 };
 enum { ST_OK = 0, ST_TIMEOUT = 1, ST_CLAMPED = 2 };
 
-template <int KIND_, int D_, int MT_, int NTG_, int NDW_, int TC_, int NSTAGE_>
+// TileCfg<format, scale kind, head_dim, m-tiles (query rows / 16), token groups, warps per
+// token group (head-dim split), tokens per warp slice, slots per warp ring, CTAs per SM>.
+template <int KIND_, int SKT_, int D_, int MT_, int NTG_, int NDW_, int TW_, int NSTAGE_,
+          int MINB_ = 1>
 struct TileCfg {
-  static constexpr int KIND = KIND_, D = D_, MT = MT_, NTG = NTG_, NDW = NDW_, TC = TC_;
-  static constexpr int NSTAGE = NSTAGE_;
-  static constexpr int NCW = NTG * NDW;            // consumer warps
-  static constexpr int NTHREADS = (NCW + 1) * 32;  // plus one producer warp
-  static constexpr int TW = TC / NTG;              // tokens per warp slice per stage
-  static constexpr int NT = TW / 8;                // QK n-tiles per slice
-  static constexpr int NKC = TW / 16;              // PV k-chunks per slice
+  static constexpr int KIND = KIND_, SKT = SKT_, D = D_, MT = MT_, NTG = NTG_, NDW = NDW_;
+  static constexpr int TW = TW_, NSTAGE = NSTAGE_, MINB = MINB_;
+  static constexpr bool TOK_SCALE = SKT == SK_TOKEN;                 // fp8 per-token scales
+  static constexpr bool SCALES = SKT == SK_TOKEN || SKT == SK_E8M0;  // staged per slice
+  static constexpr int NCW = NTG * NDW;  // warps (all compute; each loads its own slices)
+  static constexpr int NTHREADS = NCW * 32;
+  static constexpr int TC = TW * NTG;    // tokens per CTA stage
+  static constexpr int NT = TW / 8;      // QK n-tiles per slice
+  static constexpr int NKC = TW / 16;    // PV k-chunks per slice
   static constexpr int RPAD = MT * 16;
   static constexpr int ROW_BYTES = KIND == KIND_BF16 ? 2 * D : (KIND == KIND_FP8 ? D : D / 2);
   static constexpr int SUB = KIND == KIND_FP4 ? 64 : 128;  // swizzle span = sub-tile row
   static constexpr int NSUB = ROW_BYTES / SUB;
-  static constexpr int WBYTES = ROW_BYTES / NDW;  // row bytes one warp reads
-  static constexpr int NGRP = WBYTES / 64;        // ldmatrix.x4 groups per slice row
-  static constexpr int DW = D / NDW;              // head dims one warp owns
-  static constexpr int NKCH = DW / 16;            // QK k-chunks per warp
-  static constexpr int NTD = DW / 8;              // PV n-tiles per warp
+  static constexpr int NSUBW = NSUB / NDW;  // sub-tiles one warp loads and reads
+  static constexpr int WBYTES = ROW_BYTES / NDW;
+  static constexpr int NGRP = WBYTES / 64;  // ldmatrix.x4 groups per slice row
+  static constexpr int NCP = WBYTES / 32;   // ldmatrix.x4.trans per 16-token chunk
+  static constexpr int DW = D / NDW;        // head dims one warp owns
+  static constexpr int NKCH = DW / 16;      // QK k-chunks per warp
+  static constexpr int NTD = DW / 8;        // PV n-tiles per warp
   static constexpr int NBLK = KIND == KIND_FP4 ? D / 32 : 1;
-  static constexpr int KV_STAGE = NSUB * TC * SUB;
-  static constexpr int SC_STAGE = TC * 4;
-  static constexpr int STAGE_BYTES = ((2 * KV_STAGE + 2 * SC_STAGE) + 1023) / 1024 * 1024;
+  static constexpr int SLOT_V = NSUBW * TW * SUB;  // V offset inside a slot
+  static constexpr int SLOT_KV = 2 * SLOT_V;       // K + V bytes of one slot
+  static constexpr int SLOT_SC = 8 * TW;           // K then V scales (fp32 or 4 e8m0 bytes)
   static constexpr bool Q_IN_REGS = MT * NKCH * 4 <= 32;
-  static constexpr int OFF_Q = NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_SC = OFF_RING + NCW * NSTAGE * SLOT_KV;
+  static constexpr int OFF_Q = OFF_SC + NCW * NSTAGE * SLOT_SC;
   static constexpr int OFF_CR = OFF_Q + RPAD * D * 2;
   static constexpr int OFF_X = OFF_CR + RPAD * 4;
   static constexpr int XW = MT * NT * 4 * 32;  // floats per warp per exchange buffer
@@ -56,30 +66,26 @@ struct TileCfg {
   static constexpr int OFF_OB = OFF_X + X_BYTES;
   static constexpr int OFF_ML = OFF_OB + RPAD * D * 4;
   static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;
-  static constexpr int OFF_BAR = OFF_FIN + RPAD * 8;
-  static constexpr int OFF_FLAG = OFF_BAR + 2 * NSTAGE * 8;
+  static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 6 : 0;  // e8m0 factor tables
+  static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
+  static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
+  static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + slack to align the base to 1 KiB
   static_assert(TW % 16 == 0, "a warp slice holds whole 16-token k-chunks");
   static_assert(WBYTES % 64 == 0, "a warp row slice is whole ldmatrix.x4 groups");
-  static_assert(KIND != KIND_FP4 || (D == 128 && NDW == 1), "MXFP4 path: D 128, one warp per row");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(NSUB % NDW == 0, "head-dim split on sub-tile boundaries");
+  static_assert(SLOT_V % 1024 == 0, "swizzled TMA destinations are 1 KiB aligned");
+  static_assert(KIND != KIND_FP4 || (D == 128 && NDW == 1 && TW == 32),
+                "MXFP4 path: D 128, one warp per row, one lane per slice token");
+  static_assert(SMEM * MINB <= 227 * 1024, "shared memory budget");
   static_assert(NTG + 1 < 16, "named barrier ids");
 };
 
-constexpr int BAR_CONSUMERS = 15;  // named barrier id for all consumer warps
+constexpr int BAR_CONSUMERS = 15;  // named barrier id for all warps of the CTA
 
 template <class C>
 __device__ __forceinline__ int swz(int row) {
   return C::SUB == 128 ? (row & 7) : ((row >> 1) & 3);
-}
-
-// Address of the 16-byte chunk holding byte `off` of token row `row` in a swizzled
-// K or V stage buffer.
-template <class C>
-__device__ __forceinline__ uint32_t chunk_addr(const uint8_t* base, int row, int off) {
-  const int sub = off / C::SUB;
-  const int cin = (off % C::SUB) >> 4;
-  return smem_u32(base + sub * (C::TC * C::SUB) + row * C::SUB + ((cin ^ swz<C>(row)) << 4));
 }
 
 __device__ __forceinline__ int clamped_context(const DecodeParams& p, int s) {
@@ -204,90 +210,538 @@ __device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int
   }
 }
 
+// Where a warp's loads stand: the next (task, slice) it will load.  The warp walks the
+// same sequence of slices for loading and for computing, the loads NSTAGE ahead.  The
+// block-table entries of the next slice are fetched one slice early (blk, one per box,
+// held by lanes 0..nbox-1) so that no refill waits on a dependent global load.
+struct SliceIt {
+  int task, c0, t1, s, hkv, L;
+  const int32_t* btrow;
+  int blk;
+  bool done;
+};
+
+__device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p) {
+  const PlanTask tk = p.tasks[it.task];
+  it.s = tk.seq;
+  it.hkv = tk.hkv_part & 0xFFFF;
+  it.L = clamped_context(p, it.s);
+  it.c0 = tk.tile_begin * kTileTokens;
+  const int t1 = tk.tile_end * kTileTokens;
+  it.t1 = t1 < it.L ? t1 : it.L;
+  it.btrow = p.bt + (int64_t)it.s * p.bt_stride;
+}
+
+// Advance to the first slice at or after the current one that holds tokens, and start
+// the block-table loads of its boxes.
 template <class C>
-__device__ void producer(const DecodeParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                         uint8_t* smem, uint64_t* full, uint64_t* empty,
-                         volatile int* abort_flag, int ntasks, int lane) {
-  if (lane == 0) {
-    tma_prefetch_desc(tmk);
-    tma_prefetch_desc(tmv);
+__device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, int ntasks, int r0,
+                                          int lane, int box_shift, int page_shift) {
+  while (!it.done && it.c0 + r0 >= it.t1) {
+    it.task += gridDim.x;
+    if (it.task >= ntasks) {
+      it.done = true;
+      return;
+    }
+    it_load_task(it, p);
   }
-  const bool scales = p.scale_kind == SK_TOKEN || p.scale_kind == SK_E8M0;
-  const int box = p.S < C::TC ? p.S : C::TC;
-  const uint32_t box_bytes = (uint32_t)box * (2 * C::ROW_BYTES + (scales ? 8 : 0));
-  int stage = 0;
-  uint32_t phase = 0;
-  uint32_t issued = 0;      // stages issued at least once
-  uint32_t last_par = 0;    // parity of the last issue per stage
-  bool dead = false;
-  for (int task = blockIdx.x; task < ntasks && !dead; task += gridDim.x) {
-    const PlanTask tk = p.tasks[task];
-    const int s = tk.seq, hkv = tk.hkv_part & 0xFFFF;
-    const int L = clamped_context(p, s);
-    const int t0 = tk.tile_begin * kTileTokens;
-    int t1 = tk.tile_end * kTileTokens;
-    t1 = t1 < L ? t1 : L;
-    const int32_t* btrow = p.bt + (int64_t)s * p.bt_stride;
-    for (int c0 = t0; c0 < t1; c0 += C::TC) {
-      if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
-        *abort_flag = 1;
-        if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
-        dead = true;
-        break;
-      }
-      const int ntok = (L - c0) < C::TC ? (L - c0) : C::TC;
-      const int nbox = (ntok + box - 1) / box;
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], nbox * box_bytes);
-      __syncwarp();
-      uint8_t* st = smem + stage * C::STAGE_BYTES;
-      for (int j = lane; j < nbox; j += 32) {
-        const int tok = c0 + j * box;
-        int blk = btrow[tok / p.S];
-        blk = blk < 0 ? 0 : (blk >= p.NB ? p.NB - 1 : blk);
-        const int slot = tok % p.S;
+  if (!it.done) {
+    const int tok = it.c0 + r0 + (lane << box_shift);
+    if (lane < (C::TW >> box_shift) && tok < it.L) it.blk = it.btrow[tok >> page_shift];
+  }
+}
+
+// Issue the TMA / bulk copies of one warp slice (tokens [a, min(a + TW, L)) of the
+// iterator's sequence and KV head) into ring slot `kv` / `sc`, completing on `bar`.
+template <class C>
+__device__ __forceinline__ void issue_slice(const DecodeParams& p, const CUtensorMap* tmk,
+                                            const CUtensorMap* tmv, uint8_t* kv, uint8_t* sc,
+                                            uint64_t* bar, const SliceIt& it, int r0, int dw,
+                                            int lane, int box_shift, int page_mask) {
+  const int a = it.c0 + r0;
+  const int ntok = (it.L - a) < C::TW ? (it.L - a) : C::TW;
+  const int box = 1 << box_shift;
+  const int nbox = (ntok + box - 1) >> box_shift;
+  if (lane == 0)
+    mbar_arrive_expect_tx(
+        bar, (uint32_t)((nbox << box_shift) * (2 * C::NSUBW * C::SUB + (C::SCALES ? 8 : 0))));
+  __syncwarp();
+  if (lane < nbox) {
+    fence_proxy_async();  // the slot was last read through the generic proxy
+    const int tok = a + (lane << box_shift);
+    int blk = it.blk;
+    blk = blk < 0 ? 0 : (blk >= p.NB ? p.NB - 1 : blk);
+    const int slot = tok & page_mask;
 #pragma unroll
-        for (int sub = 0; sub < C::NSUB; ++sub) {
-          const int dst = sub * (C::TC * C::SUB) + j * box * C::SUB;
-          tma_load_4d(st + dst, tmk, &full[stage], sub * C::SUB, slot, hkv, blk);
-          tma_load_4d(st + C::KV_STAGE + dst, tmv, &full[stage], sub * C::SUB, slot, hkv, blk);
-        }
-        if (scales) {
-          const int64_t off = (int64_t)blk * p.sc_sb + (int64_t)hkv * p.sc_sh + (int64_t)slot * 4;
-          bulk_load(st + 2 * C::KV_STAGE + j * box * 4, p.k_scale + off, box * 4, &full[stage]);
-          bulk_load(st + 2 * C::KV_STAGE + C::SC_STAGE + j * box * 4, p.v_scale + off, box * 4,
-                    &full[stage]);
-        }
+    for (int u = 0; u < C::NSUBW; ++u) {
+      const int sub = dw * C::NSUBW + u;
+      const int dst = u * (C::TW * C::SUB) + ((lane << box_shift) * C::SUB);
+      tma_load_4d(kv + dst, tmk, bar, sub * C::SUB, slot, it.hkv, blk);
+      tma_load_4d(kv + C::SLOT_V + dst, tmv, bar, sub * C::SUB, slot, it.hkv, blk);
+    }
+    if constexpr (C::SCALES) {
+      const int64_t off = (int64_t)blk * p.sc_sb + (int64_t)it.hkv * p.sc_sh + (int64_t)slot * 4;
+      bulk_load(sc + (lane << box_shift) * 4, p.k_scale + off, box * 4, bar);
+      bulk_load(sc + 4 * C::TW + (lane << box_shift) * 4, p.v_scale + off, box * 4, bar);
+    }
+  }
+}
+
+// Per-warp softmax and accumulator state of one task.
+template <class C>
+struct WarpAcc {
+  float o[C::MT][C::NTD][4];
+  float m[C::MT][2];  // running max (log2 units); probabilities are exp2(s - m) <= 2^kLazyLog2
+  float l[C::MT][2];  // thread-partial running sum
+  float vref;         // fp8 per-token: V-scale reference (probabilities carry v_scale / vref)
+  int emax[C::NBLK];  // MXFP4: V e8m0 reference per 32-dim block (-1: none yet)
+};
+
+// The running max is only raised when a slice's max exceeds it by more than 2^kLazyLog2
+// (probabilities stay <= 256, inside the f16 / bf16 range); the V-scale references move
+// only by more than 8x.  Slices that raise nothing skip the accumulator rescale.
+constexpr float kLazyLog2 = 8.f;
+constexpr float kLazyVref = 8.f;
+constexpr int kLazyExp = 3;
+
+// f16 bits of 2^x for an integer x <= 15 (0 below 2^-24).
+__device__ __forceinline__ uint32_t f16_exp2i(int x) {
+  if (x >= -14) return (uint32_t)(x + 15) << 10;
+  if (x >= -24) return 1u << (x + 24);
+  return 0u;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Both halves of a 32-bit word, each two e4m3 values, to two f16x2 words.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// m16n8k16 f16 MMA with a zero accumulator input.
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// One slice of one warp: QK^T, online softmax, PV over the slice's tokens.  MASKED is
+// the boundary path (tokens >= vw are unowned); full slices run no masking instruction.
+template <class C, bool MASKED>
+__device__ __forceinline__ void stage_compute(
+    WarpAcc<C>& A, const uint8_t* kv, const uint8_t* sc, uint8_t* smem, int vw, int lane, int dw,
+    int tg, const uint32_t (&qa)[C::Q_IN_REGS ? C::MT : 1][C::Q_IN_REGS ? C::NKCH : 1][4],
+    const uint16_t* qs, const float (&crow)[C::MT][2], const uint32_t (&koff)[C::NGRP],
+    const uint32_t (&voff)[C::NCP], int cw, int& xbuf) {
+  constexpr bool tok_scale = C::TOK_SCALE;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t kbase = smem_u32(kv);
+  const uint32_t vbase = kbase + C::SLOT_V;
+  const float* ksc = reinterpret_cast<const float*>(sc);
+  const float* vsc = reinterpret_cast<const float*>(sc + 4 * C::TW);
+  const uint32_t* kex = reinterpret_cast<const uint32_t*>(sc);
+  const uint32_t* vex = reinterpret_cast<const uint32_t*>(sc + 4 * C::TW);
+  float* ktab = reinterpret_cast<float*>(smem + C::OFF_TAB + cw * C::TAB_BYTES);
+  uint16_t* vtab = reinterpret_cast<uint16_t*>(ktab + C::NBLK * C::TW);
+
+  // ---------------- V-scale references (lazy) and MXFP4 factor tables ----------------
+  float beta[C::NBLK];
+#pragma unroll
+  for (int b = 0; b < C::NBLK; ++b) beta[b] = 1.f;
+  bool rescale_v = false;
+  float vinv = 1.f;
+  if constexpr (tok_scale) {
+    float mx = 0.f;
+#pragma unroll
+    for (int k = lane; k < C::TW; k += 32)
+      if (!MASKED || k < vw) mx = fmaxf(mx, fabsf(vsc[k]));
+#pragma unroll
+    for (int sh = 16; sh; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+    if (mx > A.vref * kLazyVref) {  // warp-uniform
+      beta[0] = A.vref / mx;
+      A.vref = mx;
+      rescale_v = true;
+    }
+    vinv = A.vref > 0.f ? 1.f / A.vref : 0.f;
+  }
+  if constexpr (C::KIND == KIND_FP4) {
+    const bool own = !MASKED || lane < vw;  // one lane per slice token
+    const uint32_t kw = kex[lane], vwd = vex[lane];
+    int cm[C::NBLK];
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b) {
+      const uint32_t e = (vwd >> (8 * b)) & 0xFF;
+      cm[b] = (int)__reduce_max_sync(0xffffffffu, own ? e : 0u);
+    }
+    bool need = false;
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b) need |= A.emax[b] < 0 || cm[b] > A.emax[b] + kLazyExp;
+    if (need) {
+#pragma unroll
+      for (int b = 0; b < C::NBLK; ++b) {
+        const int ne = max(A.emax[b], cm[b]);
+        beta[b] = A.emax[b] < 0 ? 0.f : exp2i(A.emax[b] - ne);
+        A.emax[b] = ne;
       }
-      issued |= 1u << stage;
-      last_par = (last_par & ~(1u << stage)) | (phase << stage);
-      if (++stage == C::NSTAGE) {
-        stage = 0;
-        phase ^= 1;
+      rescale_v = true;
+    }
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b) {
+      const uint32_t ek = (kw >> (8 * b)) & 0xFF;
+      const int ev = (int)((vwd >> (8 * b)) & 0xFF);
+      ktab[b * C::TW + lane] = own ? e8m0_to_f32(ek) : 0.f;
+      vtab[b * C::TW + lane] = own ? (uint16_t)f16_exp2i(ev - A.emax[b]) : (uint16_t)0;
+    }
+    __syncwarp();
+  }
+
+  // ---------------- S = Q K^T over this warp's dims ----------------
+  float sacc[C::MT][C::NT][4];
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sacc[mt][nt][j] = 0.f;
+#pragma unroll
+  for (int gi = 0; gi < C::NGRP; ++gi) {
+    uint32_t kr[C::NT][4];
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) ldsm_x4(kbase + koff[gi] + nt * 8 * C::SUB, kr[nt]);
+    if constexpr (C::KIND == KIND_BF16) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          uint32_t a[4];
+          if constexpr (C::Q_IN_REGS) {
+#pragma unroll
+            for (int z = 0; z < 4; ++z) a[z] = qa[mt][2 * gi + h][z];
+          } else {
+            load_qa<C>(qs, mt, 2 * gi + h, dw, g, t, a);
+          }
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) mma_bf16(sacc[mt][nt], a, kr[nt][2 * h], kr[nt][2 * h + 1]);
+        }
+    } else if constexpr (C::KIND == KIND_FP8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          uint32_t a[4];
+          if constexpr (C::Q_IN_REGS) {
+#pragma unroll
+            for (int z = 0; z < 4; ++z) a[z] = qa[mt][4 * gi + q][z];
+          } else {
+            load_qa<C>(qs, mt, 4 * gi + q, dw, g, t, a);
+          }
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2(kr[nt][q], b0, b1);
+            mma_f16(sacc[mt][nt], a, b0, b1);
+          }
+        }
+    } else {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float tmp[C::MT][C::NT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          uint32_t f[4];
+          e2m1x8_to_f16x2(kr[nt][b], f);
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) mma_f16_zc(tmp[mt][nt], qa[mt][2 * b], f[0], f[1]);
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) mma_f16(tmp[mt][nt], qa[mt][2 * b + 1], f[2], f[3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          const float2 kf = *reinterpret_cast<const float2*>(ktab + b * C::TW + 8 * nt + 2 * t);
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            sacc[mt][nt][0] = fmaf(tmp[mt][nt][0], kf.x, sacc[mt][nt][0]);
+            sacc[mt][nt][1] = fmaf(tmp[mt][nt][1], kf.y, sacc[mt][nt][1]);
+            sacc[mt][nt][2] = fmaf(tmp[mt][nt][2], kf.x, sacc[mt][nt][2]);
+            sacc[mt][nt][3] = fmaf(tmp[mt][nt][3], kf.y, sacc[mt][nt][3]);
+          }
+        }
       }
     }
   }
-  // Never leave while a copy into this CTA's shared memory may still be in flight.
-  for (int i = 0; i < C::NSTAGE; ++i)
-    if (issued & (1u << i)) (void)mbar_wait_bounded(&full[i], (last_par >> i) & 1, 200000000ull);
+  // ---------------- combine the two head-dim halves ----------------
+  if constexpr (C::NDW == 2) {
+    float* xb = reinterpret_cast<float*>(smem + C::OFF_X);
+    float* mine = xb + ((tg * 2 + xbuf) * 2 + dw) * C::XW;
+    const float* other = xb + ((tg * 2 + xbuf) * 2 + (dw ^ 1)) * C::XW;
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mine[((mt * C::NT + nt) * 4 + j) * 32 + lane] = sacc[mt][nt][j];
+    named_bar(1 + tg, 64);
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float x = other[((mt * C::NT + nt) * 4 + j) * 32 + lane];
+          sacc[mt][nt][j] = dw == 0 ? sacc[mt][nt][j] + x : x + sacc[mt][nt][j];
+        }
+    xbuf ^= 1;
+  }
+  // ---------------- logits and boundary mask ----------------
+#pragma unroll
+  for (int nt = 0; nt < C::NT; ++nt) {
+    const int tk0 = 8 * nt + 2 * t;
+    float2 ks = make_float2(1.f, 1.f);
+    if constexpr (tok_scale) ks = *reinterpret_cast<const float2*>(ksc + tk0);
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float x = sacc[mt][nt][j] * crow[mt][j >> 1];
+        if constexpr (tok_scale) x *= (j & 1) ? ks.y : ks.x;
+        if (MASKED && tk0 + (j & 1) >= vw) x = -INFINITY;
+        sacc[mt][nt][j] = x;
+      }
+  }
+  // ---------------- online softmax with a lazily raised max ----------------
+  float mx[C::MT][2];
+  bool need = false;
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float v = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+        v = fmaxf(v, fmaxf(sacc[mt][nt][2 * hr], sacc[mt][nt][2 * hr + 1]));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+      mx[mt][hr] = v;
+      need |= v > A.m[mt][hr] + kLazyLog2;
+    }
+  need = __any_sync(0xffffffffu, need);
+  float alpha[C::MT][2];
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      alpha[mt][hr] = 1.f;
+      if (need) {
+        const float mn = fmaxf(A.m[mt][hr], mx[mt][hr]);
+        if (mn != A.m[mt][hr]) {
+          alpha[mt][hr] = fast_exp2(A.m[mt][hr] - mn);  // -inf -> 0
+          A.m[mt][hr] = mn;
+          A.l[mt][hr] *= alpha[mt][hr];
+        }
+      }
+      const float base = A.m[mt][hr] == -INFINITY ? 0.f : A.m[mt][hr];
+      float rs = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) {
+        const float p0 = fast_exp2(sacc[mt][nt][2 * hr] - base);
+        const float p1 = fast_exp2(sacc[mt][nt][2 * hr + 1] - base);
+        sacc[mt][nt][2 * hr] = p0;
+        sacc[mt][nt][2 * hr + 1] = p1;
+        rs += p0 + p1;
+      }
+      A.l[mt][hr] += rs;
+    }
+  if (need || rescale_v) {
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < C::NTD; ++n) {
+        const float bb = C::KIND == KIND_FP4 ? beta[n >> 2] : beta[0];
+        const float f0 = alpha[mt][0] * bb, f1 = alpha[mt][1] * bb;
+        A.o[mt][n][0] *= f0;
+        A.o[mt][n][1] *= f0;
+        A.o[mt][n][2] *= f1;
+        A.o[mt][n][3] *= f1;
+      }
+  }
+  // ---------------- O += P V ----------------
+#pragma unroll
+  for (int kc = 0; kc < C::NKC; ++kc) {
+    if (MASKED && 16 * kc >= vw) break;
+    const int tb = 16 * kc + 2 * t;  // tokens tb, tb+1 (low pair) and tb+8, tb+9 (high pair)
+    uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+    if (MASKED) {
+      mlo = (tb < vw ? 0x0000FFFFu : 0u) | (tb + 1 < vw ? 0xFFFF0000u : 0u);
+      mhi = (tb + 8 < vw ? 0x0000FFFFu : 0u) | (tb + 9 < vw ? 0xFFFF0000u : 0u);
+    }
+    uint32_t pa[C::MT][4];
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+      const float* pl = sacc[mt][2 * kc];
+      const float* ph = sacc[mt][2 * kc + 1];
+      if constexpr (C::KIND == KIND_BF16) {
+        pa[mt][0] = pack_bf16x2(pl[0], pl[1]);
+        pa[mt][1] = pack_bf16x2(pl[2], pl[3]);
+        pa[mt][2] = pack_bf16x2(ph[0], ph[1]);
+        pa[mt][3] = pack_bf16x2(ph[2], ph[3]);
+      } else if constexpr (tok_scale) {
+        const float2 a = *reinterpret_cast<const float2*>(vsc + tb);
+        const float2 c = *reinterpret_cast<const float2*>(vsc + tb + 8);
+        const float vf0 = (MASKED && tb >= vw) ? 0.f : a.x * vinv;
+        const float vf1 = (MASKED && tb + 1 >= vw) ? 0.f : a.y * vinv;
+        const float vf2 = (MASKED && tb + 8 >= vw) ? 0.f : c.x * vinv;
+        const float vf3 = (MASKED && tb + 9 >= vw) ? 0.f : c.y * vinv;
+        pa[mt][0] = pack_f16x2(pl[0] * vf0, pl[1] * vf1);
+        pa[mt][1] = pack_f16x2(pl[2] * vf0, pl[3] * vf1);
+        pa[mt][2] = pack_f16x2(ph[0] * vf2, ph[1] * vf3);
+        pa[mt][3] = pack_f16x2(ph[2] * vf2, ph[3] * vf3);
+      } else {
+        pa[mt][0] = pack_f16x2(pl[0], pl[1]);
+        pa[mt][1] = pack_f16x2(pl[2], pl[3]);
+        pa[mt][2] = pack_f16x2(ph[0], ph[1]);
+        pa[mt][3] = pack_f16x2(ph[2], ph[3]);
+      }
+    }
+#pragma unroll
+    for (int cp = 0; cp < C::NCP; ++cp) {
+      uint32_t v[4];
+      ldsm_x4_t(vbase + voff[cp] + 16 * kc * C::SUB, v);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * cp + c;  // 16-byte chunk of the warp's row slice
+        if constexpr (C::KIND == KIND_BF16) {
+          const uint32_t b0 = MASKED ? v[2 * c] & mlo : v[2 * c];
+          const uint32_t b1 = MASKED ? v[2 * c + 1] & mhi : v[2 * c + 1];
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) mma_bf16(A.o[mt][ch], pa[mt], b0, b1);
+        } else if constexpr (C::KIND == KIND_FP8) {
+          uint32_t bA0, bB0, bA1, bB1;
+          e4m3x4_to_f16x2(prmt(v[2 * c], v[2 * c], 0x3120), bA0, bB0);
+          e4m3x4_to_f16x2(prmt(v[2 * c + 1], v[2 * c + 1], 0x3120), bA1, bB1);
+          if (MASKED) {
+            bA0 &= mlo;
+            bB0 &= mlo;
+            bA1 &= mhi;
+            bB1 &= mhi;
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            mma_f16(A.o[mt][2 * ch], pa[mt], bA0, bA1);
+            mma_f16(A.o[mt][2 * ch + 1], pa[mt], bB0, bB1);
+          }
+        } else {
+          // V block `ch`: its e8m0 factors (relative to emax[ch]) go into P, in f16
+          const uint32_t vp0 = *reinterpret_cast<const uint32_t*>(vtab + ch * C::TW + tb);
+          const uint32_t vp1 = *reinterpret_cast<const uint32_t*>(vtab + ch * C::TW + tb + 8);
+          uint32_t pb[C::MT][4];
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            pb[mt][0] = hmul2(pa[mt][0], vp0);
+            pb[mt][1] = hmul2(pa[mt][1], vp0);
+            pb[mt][2] = hmul2(pa[mt][2], vp1);
+            pb[mt][3] = hmul2(pa[mt][3], vp1);
+          }
+          uint32_t fl[4], fh[4];
+          e2m1x8_to_f16x2(v[2 * c], fl);
+          e2m1x8_to_f16x2(v[2 * c + 1], fh);
+          uint32_t b0[4] = {prmt(fl[0], fl[2], 0x5410), prmt(fl[0], fl[2], 0x7632),
+                            prmt(fl[1], fl[3], 0x5410), prmt(fl[1], fl[3], 0x7632)};
+          uint32_t b1[4] = {prmt(fh[0], fh[2], 0x5410), prmt(fh[0], fh[2], 0x7632),
+                            prmt(fh[1], fh[3], 0x5410), prmt(fh[1], fh[3], 0x7632)};
+          if (MASKED) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              b0[i] &= mlo;
+              b1[i] &= mhi;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) mma_f16(A.o[mt][4 * ch + i], pb[mt], b0[i], b1[i]);
+        }
+      }
+    }
+  }
 }
 
 template <class C>
-__device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                        volatile int* abort_flag, int ntasks, int cw, int lane) {
+__device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                          uint8_t* smem, uint64_t* full, volatile int* abort_flag, int ntasks,
+                          int cw, int lane) {
   const int tg = cw / C::NDW, dw = cw % C::NDW;
   const int g = lane >> 2, t = lane & 3;
+  const int r0 = tg * C::TW;  // this warp's slice inside a CTA stage
   const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + C::OFF_Q);
   const float* cr = reinterpret_cast<const float*>(smem + C::OFF_CR);
   float* obuf = reinterpret_cast<float*>(smem + C::OFF_OB);
   float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
   float2* fin = reinterpret_cast<float2*>(smem + C::OFF_FIN);
-  const float k_scale_tensor =
-      (C::KIND == KIND_FP8 && p.scale_kind == SK_TENSOR) ? reinterpret_cast<const float*>(p.k_scale)[0] : 1.f;
-  const float v_scale_tensor =
-      (C::KIND == KIND_FP8 && p.scale_kind == SK_TENSOR) ? reinterpret_cast<const float*>(p.v_scale)[0] : 1.f;
-  const bool tok_scale = C::KIND == KIND_FP8 && p.scale_kind == SK_TOKEN;
-  int stage = 0;
-  uint32_t phase = 0;
+  uint8_t* ring = smem + C::OFF_RING + cw * C::NSTAGE * C::SLOT_KV;
+  uint8_t* scring = smem + C::OFF_SC + cw * C::NSTAGE * C::SLOT_SC;
+  uint64_t* bars = full + cw * C::NSTAGE;
+  const float k_scale_tensor = (C::KIND == KIND_FP8 && C::SKT == SK_TENSOR)
+                                   ? reinterpret_cast<const float*>(p.k_scale)[0] : 1.f;
+  const float v_scale_tensor = (C::KIND == KIND_FP8 && C::SKT == SK_TENSOR)
+                                   ? reinterpret_cast<const float*>(p.v_scale)[0] : 1.f;
+  const int page_shift = __ffs(p.S) - 1;  // page sizes are powers of two
+  const int box_shift = p.S < C::TW ? page_shift : __ffs(C::TW) - 1;
+  const int page_mask = p.S - 1;
+  if (lane == 0) {
+    tma_prefetch_desc(tmk);
+    tma_prefetch_desc(tmv);
+  }
+  // Per-lane byte offsets of the ldmatrix rows inside a slot (the swizzle phase of a row
+  // depends only on its index modulo 8, i.e. on the lane).
+  uint32_t koff[C::NGRP], voff[C::NCP];
+  {
+    const int j = lane & 7, q = lane >> 3;
+#pragma unroll
+    for (int gi = 0; gi < C::NGRP; ++gi) {
+      const int off = gi * 64 + q * 16;
+      const int u = off / C::SUB, cin = (off % C::SUB) >> 4;
+      koff[gi] = u * (C::TW * C::SUB) + j * C::SUB + ((cin ^ swz<C>(j)) << 4);
+    }
+#pragma unroll
+    for (int cp = 0; cp < C::NCP; ++cp) {
+      const int off = (2 * cp + (q >> 1)) * 16;
+      const int u = off / C::SUB, cin = (off % C::SUB) >> 4;
+      const int row = 8 * (q & 1) + j;
+      voff[cp] = u * (C::TW * C::SUB) + row * C::SUB + ((cin ^ swz<C>(row)) << 4);
+    }
+  }
+
+  // prologue: fill the ring
+  SliceIt ld;
+  ld.task = blockIdx.x;
+  ld.done = ld.task >= ntasks;
+  ld.blk = 0;
+  if (!ld.done) it_load_task(ld, p);
+  it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
+  uint32_t issued = 0, consumed = 0;
+  int lslot = 0;  // ring slot of the next load
+  while (!ld.done && issued < (uint32_t)C::NSTAGE) {
+    issue_slice<C>(p, tmk, tmv, ring + lslot * C::SLOT_KV, scring + lslot * C::SLOT_SC,
+                   &bars[lslot], ld, r0, dw, lane, box_shift, page_mask);
+    ++issued;
+    lslot = lslot + 1 == C::NSTAGE ? 0 : lslot + 1;
+    ld.c0 += C::TC;
+    it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
+  }
+  int cslot = 0;      // ring slot of the next compute
+  uint32_t cpar = 0;  // its phase parity
   int xbuf = 0;
 
   for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
@@ -316,347 +770,51 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
       crow[mt][1] = cr[16 * mt + g + 8];
     }
 
-    float o[C::MT][C::NTD][4];
-    float m_run[C::MT][2], l_run[C::MT][2];
+    WarpAcc<C> A;
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
       for (int n = 0; n < C::NTD; ++n)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[mt][n][j] = 0.f;
-      m_run[mt][0] = m_run[mt][1] = -INFINITY;
-      l_run[mt][0] = l_run[mt][1] = 0.f;
+        for (int j = 0; j < 4; ++j) A.o[mt][n][j] = 0.f;
+      A.m[mt][0] = A.m[mt][1] = -INFINITY;
+      A.l[mt][0] = A.l[mt][1] = 0.f;
     }
-    float vref = 0.f;                 // fp8 per-token: running max |v_scale|
-    int emax[C::NBLK];                // MXFP4: running max V e8m0 exponent per block
+    A.vref = 0.f;
 #pragma unroll
-    for (int b = 0; b < C::NBLK; ++b) emax[b] = -1;
+    for (int b = 0; b < C::NBLK; ++b) A.emax[b] = -1;
 
-    for (int c0 = t0; c0 < t1; c0 += C::TC) {
+    for (int c0 = t0; c0 + r0 < t1; c0 += C::TC) {
       if (!*abort_flag) {
-        if (!mbar_wait_bounded(&full[stage], phase)) {
+        if (!mbar_wait_bounded(&bars[cslot], cpar)) {
           *abort_flag = 1;
           if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
         }
       }
-      const uint8_t* st = smem + stage * C::STAGE_BYTES;
-      const uint8_t* kst = st;
-      const uint8_t* vst = st + C::KV_STAGE;
-      const float* ksc = reinterpret_cast<const float*>(st + 2 * C::KV_STAGE);
-      const float* vsc = reinterpret_cast<const float*>(st + 2 * C::KV_STAGE + C::SC_STAGE);
-      const uint32_t* kex = reinterpret_cast<const uint32_t*>(st + 2 * C::KV_STAGE);
-      const uint32_t* vex = reinterpret_cast<const uint32_t*>(st + 2 * C::KV_STAGE + C::SC_STAGE);
-      const int r0 = tg * C::TW;
-      const int vw = L - (c0 + r0);  // owned tokens in this warp's slice (may be <= 0)
-      if (vw > 0) {
-        const bool masked = vw < C::TW;
-        // ---------------- S = Q K^T over this warp's dims ----------------
-        float sacc[C::MT][C::NT][4];
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sacc[mt][nt][j] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
-          float kf[C::NBLK][2];
-          if constexpr (C::KIND == KIND_FP4) {
-            const uint32_t w0 = kex[r0 + 8 * nt + 2 * t], w1 = kex[r0 + 8 * nt + 2 * t + 1];
-#pragma unroll
-            for (int b = 0; b < C::NBLK; ++b) {
-              kf[b][0] = e8m0_to_f32((w0 >> (8 * b)) & 0xFF);
-              kf[b][1] = e8m0_to_f32((w1 >> (8 * b)) & 0xFF);
-            }
-          }
-#pragma unroll
-          for (int gi = 0; gi < C::NGRP; ++gi) {
-            const int rr = r0 + 8 * nt + (lane & 7);
-            const int off = dw * C::WBYTES + gi * 64 + (lane >> 3) * 16;
-            uint32_t kr[4];
-            ldsm_x4(chunk_addr<C>(kst, rr, off), kr);
-            if constexpr (C::KIND == KIND_BF16) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                  uint32_t a[4];
-                  if constexpr (C::Q_IN_REGS) {
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) a[z] = qa[mt][2 * gi + h][z];
-                  } else {
-                    load_qa<C>(qs, mt, 2 * gi + h, dw, g, t, a);
-                  }
-                  mma_bf16(sacc[mt][nt], a, kr[2 * h], kr[2 * h + 1]);
-                }
-            } else if constexpr (C::KIND == KIND_FP8) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t b0 = e4m3x2_to_f16x2(kr[q] & 0xFFFF);
-                const uint32_t b1 = e4m3x2_to_f16x2(kr[q] >> 16);
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                  uint32_t a[4];
-                  if constexpr (C::Q_IN_REGS) {
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) a[z] = qa[mt][4 * gi + q][z];
-                  } else {
-                    load_qa<C>(qs, mt, 4 * gi + q, dw, g, t, a);
-                  }
-                  mma_f16(sacc[mt][nt], a, b0, b1);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                uint32_t f[4];
-                e2m1x8_to_f16x2(kr[b], f);
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                  float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-                  uint32_t a0[4], a1[4];
-                  if constexpr (C::Q_IN_REGS) {
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) {
-                      a0[z] = qa[mt][2 * b][z];
-                      a1[z] = qa[mt][2 * b + 1][z];
-                    }
-                  } else {
-                    load_qa<C>(qs, mt, 2 * b, dw, g, t, a0);
-                    load_qa<C>(qs, mt, 2 * b + 1, dw, g, t, a1);
-                  }
-                  mma_f16(tmp, a0, f[0], f[1]);
-                  mma_f16(tmp, a1, f[2], f[3]);
-                  sacc[mt][nt][0] = fmaf(tmp[0], kf[b][0], sacc[mt][nt][0]);
-                  sacc[mt][nt][1] = fmaf(tmp[1], kf[b][1], sacc[mt][nt][1]);
-                  sacc[mt][nt][2] = fmaf(tmp[2], kf[b][0], sacc[mt][nt][2]);
-                  sacc[mt][nt][3] = fmaf(tmp[3], kf[b][1], sacc[mt][nt][3]);
-                }
-              }
-            }
-          }
-        }
-        // ---------------- combine the two head-dim halves ----------------
-        if constexpr (C::NDW == 2) {
-          float* xb = reinterpret_cast<float*>(smem + C::OFF_X);
-          float* mine = xb + ((tg * 2 + xbuf) * 2 + dw) * C::XW;
-          const float* other = xb + ((tg * 2 + xbuf) * 2 + (dw ^ 1)) * C::XW;
-#pragma unroll
-          for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) mine[((mt * C::NT + nt) * 4 + j) * 32 + lane] = sacc[mt][nt][j];
-          named_bar(1 + tg, 64);
-#pragma unroll
-          for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float x = other[((mt * C::NT + nt) * 4 + j) * 32 + lane];
-                sacc[mt][nt][j] = dw == 0 ? sacc[mt][nt][j] + x : x + sacc[mt][nt][j];
-              }
-          xbuf ^= 1;
-        }
-        // ---------------- logits, boundary mask ----------------
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
-          const int tk0 = 8 * nt + 2 * t;
-          float ks0 = 1.f, ks1 = 1.f;
-          if (tok_scale) {
-            const float2 kk = *reinterpret_cast<const float2*>(ksc + r0 + tk0);
-            ks0 = kk.x;
-            ks1 = kk.y;
-          }
-#pragma unroll
-          for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float x = sacc[mt][nt][j] * crow[mt][j >> 1];
-              if (tok_scale) x *= (j & 1) ? ks1 : ks0;
-              if (masked && tk0 + (j & 1) >= vw) x = -INFINITY;
-              sacc[mt][nt][j] = x;
-            }
-        }
-        // ---------------- online softmax ----------------
-        float alpha[C::MT][2];
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt)
-              mx = fmaxf(mx, fmaxf(sacc[mt][nt][2 * hr], sacc[mt][nt][2 * hr + 1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mnew = fmaxf(m_run[mt][hr], mx);
-            const float base = mnew == -INFINITY ? 0.f : mnew;
-            alpha[mt][hr] = fast_exp2(m_run[mt][hr] - base);
-            m_run[mt][hr] = mnew;
-            float rs = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) {
-              const float p0 = fast_exp2(sacc[mt][nt][2 * hr] - base);
-              const float p1 = fast_exp2(sacc[mt][nt][2 * hr + 1] - base);
-              sacc[mt][nt][2 * hr] = p0;
-              sacc[mt][nt][2 * hr + 1] = p1;
-              rs += p0 + p1;
-            }
-            l_run[mt][hr] = l_run[mt][hr] * alpha[mt][hr] + rs;
-          }
-        // ---------------- V scale references and accumulator rescale ----------------
-        float beta[C::NBLK];
-        float vinv = 1.f;
-#pragma unroll
-        for (int b = 0; b < C::NBLK; ++b) beta[b] = 1.f;
-        if (tok_scale) {
-          float mx = 0.f;
-          for (int k = lane; k < vw && k < C::TW; k += 32) mx = fmaxf(mx, fabsf(vsc[r0 + k]));
-#pragma unroll
-          for (int sh = 16; sh; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-          const float nref = fmaxf(vref, mx);
-          beta[0] = nref > 0.f ? vref / nref : 0.f;
-          vinv = nref > 0.f ? 1.f / nref : 0.f;
-          vref = nref;
-        }
-        if constexpr (C::KIND == KIND_FP4) {
-          uint32_t mx[C::NBLK];
-#pragma unroll
-          for (int b = 0; b < C::NBLK; ++b) mx[b] = 0;
-          for (int k = lane; k < vw && k < C::TW; k += 32) {
-            const uint32_t w = vex[r0 + k];
-#pragma unroll
-            for (int b = 0; b < C::NBLK; ++b) mx[b] = max(mx[b], (w >> (8 * b)) & 0xFF);
-          }
-#pragma unroll
-          for (int b = 0; b < C::NBLK; ++b) {
-            const int cm = (int)__reduce_max_sync(0xffffffffu, mx[b]);
-            const int ne = max(emax[b], cm);
-            beta[b] = emax[b] < 0 ? 0.f : exp2i(emax[b] - ne);
-            emax[b] = ne;
-          }
-        }
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-          for (int n = 0; n < C::NTD; ++n) {
-            const float bb = C::KIND == KIND_FP4 ? beta[n >> 2] : beta[0];
-            const float f0 = alpha[mt][0] * bb, f1 = alpha[mt][1] * bb;
-            o[mt][n][0] *= f0;
-            o[mt][n][1] *= f0;
-            o[mt][n][2] *= f1;
-            o[mt][n][3] *= f1;
-          }
-        // ---------------- O += P V ----------------
-#pragma unroll
-        for (int kc = 0; kc < C::NKC; ++kc) {
-          if (masked && 16 * kc >= vw) break;
-          const int tb = 16 * kc + 2 * t;  // tokens tb, tb+1 (lo pair) and tb+8, tb+9 (hi pair)
-          uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-          if (masked) {
-            mlo = (tb < vw ? 0x0000FFFFu : 0u) | (tb + 1 < vw ? 0xFFFF0000u : 0u);
-            mhi = (tb + 8 < vw ? 0x0000FFFFu : 0u) | (tb + 9 < vw ? 0xFFFF0000u : 0u);
-          }
-          // per-token V factors (0 for unowned tokens, selected, never multiplied)
-          float vf[C::NBLK][4];
-#pragma unroll
-          for (int b = 0; b < C::NBLK; ++b)
-#pragma unroll
-            for (int z = 0; z < 4; ++z) vf[b][z] = 1.f;
-          if (tok_scale) {
-            const float2 a = *reinterpret_cast<const float2*>(vsc + r0 + tb);
-            const float2 c = *reinterpret_cast<const float2*>(vsc + r0 + tb + 8);
-            vf[0][0] = a.x * vinv;
-            vf[0][1] = a.y * vinv;
-            vf[0][2] = c.x * vinv;
-            vf[0][3] = c.y * vinv;
-          }
-          if constexpr (C::KIND == KIND_FP4) {
-            const uint32_t w[4] = {vex[r0 + tb], vex[r0 + tb + 1], vex[r0 + tb + 8], vex[r0 + tb + 9]};
-#pragma unroll
-            for (int b = 0; b < C::NBLK; ++b)
-#pragma unroll
-              for (int z = 0; z < 4; ++z) vf[b][z] = exp2i((int)((w[z] >> (8 * b)) & 0xFF) - emax[b]);
-          }
-          if (masked && (tok_scale || C::KIND == KIND_FP4)) {
-#pragma unroll
-            for (int b = 0; b < C::NBLK; ++b) {
-              if (tb >= vw) vf[b][0] = 0.f;
-              if (tb + 1 >= vw) vf[b][1] = 0.f;
-              if (tb + 8 >= vw) vf[b][2] = 0.f;
-              if (tb + 9 >= vw) vf[b][3] = 0.f;
-            }
-          }
-          // P A-fragments, one set per V block factor
-          uint32_t pa[C::NBLK][C::MT][4];
-#pragma unroll
-          for (int b = 0; b < C::NBLK; ++b)
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-              const float* pl = sacc[mt][2 * kc];
-              const float* ph = sacc[mt][2 * kc + 1];
-              if constexpr (C::KIND == KIND_BF16) {
-                pa[b][mt][0] = pack_bf16x2(pl[0], pl[1]);
-                pa[b][mt][1] = pack_bf16x2(pl[2], pl[3]);
-                pa[b][mt][2] = pack_bf16x2(ph[0], ph[1]);
-                pa[b][mt][3] = pack_bf16x2(ph[2], ph[3]);
-              } else {
-                pa[b][mt][0] = pack_f16x2(pl[0] * vf[b][0], pl[1] * vf[b][1]);
-                pa[b][mt][1] = pack_f16x2(pl[2] * vf[b][0], pl[3] * vf[b][1]);
-                pa[b][mt][2] = pack_f16x2(ph[0] * vf[b][2], ph[1] * vf[b][3]);
-                pa[b][mt][3] = pack_f16x2(ph[2] * vf[b][2], ph[3] * vf[b][3]);
-              }
-            }
-          // V fragments, two 16-byte chunks per ldmatrix.x4.trans
-#pragma unroll
-          for (int cp = 0; cp < C::WBYTES / 32; ++cp) {
-            const int q = lane >> 3;
-            const int rr = r0 + 16 * kc + 8 * (q & 1) + (lane & 7);
-            const int off = dw * C::WBYTES + (2 * cp + (q >> 1)) * 16;
-            uint32_t v[4];
-            ldsm_x4_t(chunk_addr<C>(vst, rr, off), v);
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int ch = 2 * cp + c;  // chunk index within the warp's row slice
-              if constexpr (C::KIND == KIND_BF16) {
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) mma_bf16(o[mt][ch], pa[0][mt], v[2 * c] & mlo, v[2 * c + 1] & mhi);
-              } else if constexpr (C::KIND == KIND_FP8) {
-                const uint32_t wl = prmt(v[2 * c], v[2 * c], 0x3120);
-                const uint32_t wh = prmt(v[2 * c + 1], v[2 * c + 1], 0x3120);
-                const uint32_t bA0 = e4m3x2_to_f16x2(wl & 0xFFFF) & mlo;
-                const uint32_t bB0 = e4m3x2_to_f16x2(wl >> 16) & mlo;
-                const uint32_t bA1 = e4m3x2_to_f16x2(wh & 0xFFFF) & mhi;
-                const uint32_t bB1 = e4m3x2_to_f16x2(wh >> 16) & mhi;
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                  mma_f16(o[mt][2 * ch], pa[0][mt], bA0, bA1);
-                  mma_f16(o[mt][2 * ch + 1], pa[0][mt], bB0, bB1);
-                }
-              } else {
-                uint32_t fl[4], fh[4];
-                e2m1x8_to_f16x2(v[2 * c], fl);
-                e2m1x8_to_f16x2(v[2 * c + 1], fh);
-                const uint32_t b0[4] = {prmt(fl[0], fl[2], 0x5410) & mlo, prmt(fl[0], fl[2], 0x7632) & mlo,
-                                        prmt(fl[1], fl[3], 0x5410) & mlo, prmt(fl[1], fl[3], 0x7632) & mlo};
-                const uint32_t b1[4] = {prmt(fh[0], fh[2], 0x5410) & mhi, prmt(fh[0], fh[2], 0x7632) & mhi,
-                                        prmt(fh[1], fh[3], 0x5410) & mhi, prmt(fh[1], fh[3], 0x7632) & mhi};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                  for (int mt = 0; mt < C::MT; ++mt) mma_f16(o[mt][4 * ch + i], pa[ch][mt], b0[i], b1[i]);
-              }
-            }
-          }
-        }
+      const uint8_t* kv = ring + cslot * C::SLOT_KV;
+      const uint8_t* sc = scring + cslot * C::SLOT_SC;
+      const int vw = L - (c0 + r0);  // owned tokens in the slice (> 0 here)
+      if (vw >= C::TW) {
+        stage_compute<C, false>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
+                                xbuf);
+      } else {
+        stage_compute<C, true>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
+                               xbuf);
+      }
+      const int done_slot = cslot;
+      ++consumed;
+      if (++cslot == C::NSTAGE) {
+        cslot = 0;
+        cpar ^= 1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == C::NSTAGE) {
-        stage = 0;
-        phase ^= 1;
+      if (!ld.done) {  // refill the slot just read with the slice NSTAGE ahead
+        issue_slice<C>(p, tmk, tmv, ring + done_slot * C::SLOT_KV, scring + done_slot * C::SLOT_SC,
+                       &bars[done_slot], ld, r0, dw, lane, box_shift, page_mask);
+        ++issued;
+        lslot = lslot + 1 == C::NSTAGE ? 0 : lslot + 1;
+        ld.c0 += C::TC;
+        it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
       }
     }
 
@@ -665,11 +823,11 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
     for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        float l = l_run[mt][hr];
+        float l = A.l[mt][hr];
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        l_run[mt][hr] = l;
-        if (dw == 0 && t == 0) ml[tg * C::RPAD + 16 * mt + g + 8 * hr] = make_float2(m_run[mt][hr], l);
+        A.l[mt][hr] = l;
+        if (dw == 0 && t == 0) ml[tg * C::RPAD + 16 * mt + g + 8 * hr] = make_float2(A.m[mt][hr], l);
       }
     named_bar(BAR_CONSUMERS, C::NCW * 32);
     float fac[C::MT][2];
@@ -682,7 +840,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
 #pragma unroll
         for (int i = 0; i < C::NTG; ++i) M = fmaxf(M, ml[i * C::RPAD + row].x);
         const float base = M == -INFINITY ? 0.f : M;
-        fac[mt][hr] = fast_exp2(m_run[mt][hr] - base);
+        fac[mt][hr] = fast_exp2(A.m[mt][hr] - base);
         if (tg == 0 && dw == 0 && t == 0) {
           float Lt = 0.f;
 #pragma unroll
@@ -697,9 +855,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
 #pragma unroll
     for (int b = 0; b < C::NBLK; ++b) {
       if constexpr (C::KIND == KIND_FP4) {
-        bfac[b] = emax[b] < 0 ? 0.f : (emax[b] == 0 ? __int_as_float(0x00400000) : __int_as_float(emax[b] << 23));
+        bfac[b] = A.emax[b] < 0 ? 0.f
+                                : (A.emax[b] == 0 ? __int_as_float(0x00400000) : __int_as_float(A.emax[b] << 23));
       } else {
-        bfac[b] = tok_scale ? vref : v_scale_tensor;
+        bfac[b] = C::TOK_SCALE ? A.vref : v_scale_tensor;
       }
     }
 #pragma unroll 1
@@ -714,7 +873,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
               const int row = 16 * mt + g + 8 * (j >> 1);
               const int d = o_dim<C>(n, j, dw, t);
               const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
-              const float val = o[mt][n][j] * fac[mt][j >> 1] * bb;
+              const float val = A.o[mt][n][j] * fac[mt][j >> 1] * bb;
               float* dst = obuf + row * C::D + d;
               *dst = (i == 0) ? val : (*dst + val);
             }
@@ -739,37 +898,37 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, uint64_t* full, u
       }
     }
   }
+  // Never leave while a copy into this CTA's shared memory may still be in flight (only
+  // possible after a timed-out wait).
+  for (; consumed < issued; ++consumed) {
+    (void)mbar_wait_bounded(&bars[cslot], cpar, 200000000ull);
+    if (++cslot == C::NSTAGE) {
+      cslot = 0;
+      cpar ^= 1;
+    }
+  }
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::NTHREADS, 1)
+__global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     pa_tile_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + C::NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NSTAGE; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], C::NCW);
-    }
+    for (int i = 0; i < C::NCW * C::NSTAGE; ++i) mbar_init(&full[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
   const int ntasks = *p.ntasks;
-  if (warp == C::NCW) {
-    producer<C>(p, &tmk, &tmv, smem, full, empty, abort_flag, ntasks, lane);
-  } else {
-    consumer<C>(p, smem, full, empty, abort_flag, ntasks, warp, lane);
-  }
+  warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, ntasks, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
-// Launch helper: persistent grid of min(capacity, SMs) CTAs, one CTA per SM.
+// Launch helper: persistent grid of min(task capacity, MINB x SMs) CTAs.
 template <class C>
 int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid_cap,
                 int num_sms, void* stream) {
@@ -779,7 +938,8 @@ int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap&
     if (e != cudaSuccess) return (int)e;
     attr_done = true;
   }
-  int grid = num_sms < grid_cap ? num_sms : grid_cap;
+  int grid = num_sms * C::MINB;
+  if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   pa_tile_kernel<C><<<grid, C::NTHREADS, C::SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(p, tk, tv);
   return (int)cudaGetLastError();
