@@ -688,7 +688,6 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   const float* cr = reinterpret_cast<const float*>(smem + C::OFF_CR);
   float* obuf = reinterpret_cast<float*>(smem + C::OFF_OB);
   float2* ml = reinterpret_cast<float2*>(smem + C::OFF_ML);
-  float2* fin = reinterpret_cast<float2*>(smem + C::OFF_FIN);
   uint8_t* ring = smem + C::OFF_RING + cw * C::NSTAGE * C::SLOT_KV;
   uint8_t* scring = smem + C::OFF_SC + cw * C::NSTAGE * C::SLOT_SC;
   uint64_t* bars = full + cw * C::NSTAGE;
@@ -830,7 +829,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         if (dw == 0 && t == 0) ml[tg * C::RPAD + 16 * mt + g + 8 * hr] = make_float2(A.m[mt][hr], l);
       }
     named_bar(BAR_CONSUMERS, C::NCW * 32);
-    float fac[C::MT][2];
+    float fac[C::MT][2], Mrow[C::MT][2], Lrow[C::MT][2];
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
@@ -841,15 +840,14 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         for (int i = 0; i < C::NTG; ++i) M = fmaxf(M, ml[i * C::RPAD + row].x);
         const float base = M == -INFINITY ? 0.f : M;
         fac[mt][hr] = fast_exp2(A.m[mt][hr] - base);
-        if (tg == 0 && dw == 0 && t == 0) {
-          float Lt = 0.f;
+        float Lt = 0.f;
 #pragma unroll
-          for (int i = 0; i < C::NTG; ++i) {
-            const float2 e = ml[i * C::RPAD + row];
-            Lt += e.y * fast_exp2(e.x - base);
-          }
-          fin[row] = make_float2(M, Lt);
+        for (int i = 0; i < C::NTG; ++i) {
+          const float2 e = ml[i * C::RPAD + row];
+          Lt += e.y * fast_exp2(e.x - base);
         }
+        Mrow[mt][hr] = M;
+        Lrow[mt][hr] = Lt;
       }
     float bfac[C::NBLK];
 #pragma unroll
@@ -861,40 +859,68 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         bfac[b] = C::TOK_SCALE ? A.vref : v_scale_tensor;
       }
     }
+    // Groups 0 .. NTG-2 add their scaled accumulators into a buffer kept in fragment order
+    // (each lane owns float4 columns: no bank conflicts), one group at a time; the last
+    // group adds its own and stores.
+    float4* ob4 = reinterpret_cast<float4*>(obuf) + dw * (C::MT * C::NTD * 32) + lane;
 #pragma unroll 1
-    for (int i = 0; i < C::NTG; ++i) {
+    for (int i = 0; i + 1 < C::NTG; ++i) {
       if (tg == i) {
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
-          for (int n = 0; n < C::NTD; ++n)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int row = 16 * mt + g + 8 * (j >> 1);
-              const int d = o_dim<C>(n, j, dw, t);
-              const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
-              const float val = A.o[mt][n][j] * fac[mt][j >> 1] * bb;
-              float* dst = obuf + row * C::D + d;
-              *dst = (i == 0) ? val : (*dst + val);
+          for (int n = 0; n < C::NTD; ++n) {
+            const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
+            const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
+            float4 v = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0, A.o[mt][n][2] * f1,
+                                   A.o[mt][n][3] * f1);
+            float4* dst = ob4 + (mt * C::NTD + n) * 32;
+            if (i > 0) {
+              const float4 w = *dst;
+              v = make_float4(w.x + v.x, w.y + v.y, w.z + v.z, w.w + v.w);
             }
+            *dst = v;
+          }
       }
       named_bar(BAR_CONSUMERS, C::NCW * 32);
     }
-    // final store: coalesced over head_dim
-    const int ctid = cw * 32 + lane;
-    for (int idx = ctid; idx < p.R * C::D; idx += C::NCW * 32) {
-      const int row = idx / C::D, d = idx % C::D;
-      const float2 mf = fin[row];
-      const float val = mf.y > 0.f ? obuf[idx] / mf.y : 0.f;
-      const int i = row / p.G, h = hkv * p.G + row % p.G;
-      const int64_t orow = (int64_t)s * p.qlen + i;
-      if (nparts <= 1) {
-        p.out[orow * p.o_st + (int64_t)h * p.o_sh + d] = __float2bfloat16_rn(val);
-      } else {
-        const int64_t slot = (int64_t)p.part_base[s] + (int64_t)hkv * nparts + part;
-        const int64_t pr = slot * p.R + row;
-        p.part_o[pr * C::D + d] = val;
-        if (d == 0) reinterpret_cast<float2*>(p.part_ml)[pr] = mf;
+    if (tg == C::NTG - 1) {
+      const int64_t slot = nparts > 1 ? (int64_t)p.part_base[s] + (int64_t)hkv * nparts + part : 0;
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+        float inv[2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          inv[hr] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
+          const int row = 16 * mt + g + 8 * hr;
+          if (nparts > 1 && dw == 0 && t == 0 && row < p.R)
+            reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] = make_float2(Mrow[mt][hr], Lrow[mt][hr]);
+        }
+#pragma unroll
+        for (int n = 0; n < C::NTD; ++n) {
+          const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
+          const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
+          float4 v = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0, A.o[mt][n][2] * f1,
+                                 A.o[mt][n][3] * f1);
+          if (C::NTG > 1) {
+            const float4 w = ob4[(mt * C::NTD + n) * 32];
+            v = make_float4(w.x + v.x, w.y + v.y, w.z + v.z, w.w + v.w);
+          }
+          const float vals[4] = {v.x * inv[0], v.y * inv[0], v.z * inv[1], v.w * inv[1]};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int row = 16 * mt + g + 8 * (j >> 1);
+            if (row >= p.R) continue;
+            const int d = o_dim<C>(n, j, dw, t);
+            if (nparts <= 1) {
+              const int i = row / p.G, h = hkv * p.G + row % p.G;
+              const int64_t orow = (int64_t)s * p.qlen + i;
+              p.out[orow * p.o_st + (int64_t)h * p.o_sh + d] = __float2bfloat16_rn(vals[j]);
+            } else {
+              p.part_o[(slot * p.R + row) * C::D + d] = vals[j];
+            }
+          }
+        }
       }
     }
   }
