@@ -294,6 +294,7 @@ struct WarpAcc {
   float m[C::MT][2];  // running max (log2 units); probabilities are exp2(s - m) <= 2^kLazyLog2
   float l[C::MT][2];  // thread-partial running sum
   float vref;         // fp8 per-token: V-scale reference (probabilities carry v_scale / vref)
+  float vinv;         // 1 / vref (0 while no reference)
   int emax[C::NBLK];  // MXFP4: V e8m0 reference per 32-dim block (-1: none yet)
 };
 
@@ -363,18 +364,17 @@ __device__ __forceinline__ void stage_compute(
   bool rescale_v = false;
   float vinv = 1.f;
   if constexpr (tok_scale) {
-    float mx = 0.f;
-#pragma unroll
-    for (int k = lane; k < C::TW; k += 32)
-      if (!MASKED || k < vw) mx = fmaxf(mx, fabsf(vsc[k]));
-#pragma unroll
-    for (int sh = 16; sh; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+    static_assert(C::TW <= 32, "one lane per slice token");
+    // |v_scale| of owned tokens; non-negative floats order like their bit patterns
+    const float vs = (lane < C::TW && (!MASKED || lane < vw)) ? fabsf(vsc[lane]) : 0.f;
+    const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs)));
     if (mx > A.vref * kLazyVref) {  // warp-uniform
       beta[0] = A.vref / mx;
       A.vref = mx;
+      A.vinv = 1.f / mx;
       rescale_v = true;
     }
-    vinv = A.vref > 0.f ? 1.f / A.vref : 0.f;
+    vinv = A.vinv;
   }
   if constexpr (C::KIND == KIND_FP4) {
     const bool own = !MASKED || lane < vw;  // one lane per slice token
@@ -409,12 +409,19 @@ __device__ __forceinline__ void stage_compute(
 
   // ---------------- S = Q K^T over this warp's dims ----------------
   float sacc[C::MT][C::NT][4];
+  // fp8 with one m-tile: odd k-chunks accumulate separately (two independent MMA chains
+  // per n-tile); the split is summed once before the softmax
+  constexpr bool kSplit = C::KIND == KIND_FP8 && C::MT == 1;
+  float sacc2[kSplit ? C::MT : 1][kSplit ? C::NT : 1][4];
 #pragma unroll
   for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sacc[mt][nt][j] = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        sacc[mt][nt][j] = 0.f;
+        if constexpr (kSplit) sacc2[mt][nt][j] = 0.f;
+      }
 #pragma unroll
   for (int gi = 0; gi < C::NGRP; ++gi) {
     uint32_t kr[C::NT][4];
@@ -451,7 +458,10 @@ __device__ __forceinline__ void stage_compute(
           for (int nt = 0; nt < C::NT; ++nt) {
             uint32_t b0, b1;
             e4m3x4_to_f16x2(kr[nt][q], b0, b1);
-            mma_f16(sacc[mt][nt], a, b0, b1);
+            if (kSplit && (q & 1))
+              mma_f16(sacc2[kSplit ? mt : 0][kSplit ? nt : 0], a, b0, b1);
+            else
+              mma_f16(sacc[mt][nt], a, b0, b1);
           }
         }
     } else {
@@ -480,6 +490,12 @@ __device__ __forceinline__ void stage_compute(
         }
       }
     }
+  }
+  if constexpr (kSplit) {
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sacc[0][nt][j] += sacc2[0][nt][j];
   }
   // ---------------- combine the two head-dim halves ----------------
   if constexpr (C::NDW == 2) {
@@ -527,10 +543,14 @@ __device__ __forceinline__ void stage_compute(
   for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      float v = -INFINITY;
+      float vt[C::NT];
 #pragma unroll
-      for (int nt = 0; nt < C::NT; ++nt)
-        v = fmaxf(v, fmaxf(sacc[mt][nt][2 * hr], sacc[mt][nt][2 * hr + 1]));
+      for (int nt = 0; nt < C::NT; ++nt) vt[nt] = fmaxf(sacc[mt][nt][2 * hr], sacc[mt][nt][2 * hr + 1]);
+#pragma unroll
+      for (int w = 1; w < C::NT; w <<= 1)
+#pragma unroll
+        for (int nt = 0; nt + w < C::NT; nt += 2 * w) vt[nt] = fmaxf(vt[nt], vt[nt + w]);
+      float v = vt[0];
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
       mx[mt][hr] = v;
@@ -552,16 +572,20 @@ __device__ __forceinline__ void stage_compute(
         }
       }
       const float base = A.m[mt][hr] == -INFINITY ? 0.f : A.m[mt][hr];
-      float rs = 0.f;
+      float rt[C::NT];
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) {
         const float p0 = fast_exp2(sacc[mt][nt][2 * hr] - base);
         const float p1 = fast_exp2(sacc[mt][nt][2 * hr + 1] - base);
         sacc[mt][nt][2 * hr] = p0;
         sacc[mt][nt][2 * hr + 1] = p1;
-        rs += p0 + p1;
+        rt[nt] = p0 + p1;
       }
-      A.l[mt][hr] += rs;
+#pragma unroll
+      for (int w = 1; w < C::NT; w <<= 1)
+#pragma unroll
+        for (int nt = 0; nt + w < C::NT; nt += 2 * w) rt[nt] += rt[nt + w];
+      A.l[mt][hr] += rt[0];
     }
   if (need || rescale_v) {
 #pragma unroll
@@ -780,6 +804,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       A.l[mt][0] = A.l[mt][1] = 0.f;
     }
     A.vref = 0.f;
+    A.vinv = 0.f;
 #pragma unroll
     for (int b = 0; b < C::NBLK; ++b) A.emax[b] = -1;
 
