@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from paged_attention_decode_02_gb300 import ops, synth  # noqa: E402
+from paged_attention_decode_02_gb300 import ops, replicas, synth  # noqa: E402
 
 METRIC = "pa_decode µs/call and achieved KV GB/s (fraction of GB300 HBM peak)"
 WORKLOAD = ("long-context decode: MXFP4 and fp8-per-token KV, batch 16, 1 KV head, GQA 16, "
@@ -206,13 +206,10 @@ def run_ours(a):
     total_ms = start.elapsed_time(end)
     tile_ms = [[evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(a.steps)]
                for k in range(len(variants))]
-    if ws_n > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replicas.max_over_ranks(total_ms, dev)
     ms_step = total_ms / a.steps
     step_bytes = sum(v["bytes"] for v in variants)
-    value = step_bytes / (ms_step * 1e-3) / 1e9 * ws_n
+    value = replicas.job_throughput(step_bytes, ms_step, ws_n)
 
     # end to end through the C ABI with host buffers
     host = []
@@ -247,8 +244,8 @@ def run_ours(a):
             e2e_step()
         t1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = t0.elapsed_time(t1) / a.steps
-        e2e_val = step_bytes / (e2e_ms * 1e-3) / 1e9 * ws_n
+        e2e_ms = replicas.max_over_ranks(t0.elapsed_time(t1) / a.steps, dev)
+        e2e_val = replicas.job_throughput(step_bytes, e2e_ms, ws_n)
         e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -314,8 +311,8 @@ def _oracle_problem(v, seqs):
 def cpu_baseline(variants, nseq=None):
     """The oracle as it stands, on the host cores, over a bounded sample of the workload."""
     from oracle import pa_oracle as orc
-    threads = orc.max_threads()
-    nseq = nseq or max(1, min(16, threads))
+    nseq = nseq or max(1, min(16, orc.max_threads()))
+    threads = min(orc.max_threads(), nseq)
     total_bytes, total_s, lens_used = 0, 0.0, 0
     for v in variants:
         seqs = list(range(nseq))
@@ -345,7 +342,8 @@ def run_reference(a):
         case = synth.config5(kv)
         p = synth.make(case)
         variants.append({"case": case, "p": p, "lens": p["context_lens"].tolist()})
-    nseq = 2
+    threads = orc.max_threads()
+    nseq = max(1, min(16, threads))  # one (sequence, KV head) unit per host thread
     probs = [_oracle_problem(v, list(range(nseq))) for v in variants]
     sample_bytes = sum(sum(v["lens"][:nseq]) * synth.kv_bytes_per_token(v["case"]) for v in variants)
     for _ in range(a.warmup):
@@ -357,7 +355,7 @@ def run_reference(a):
             pr.decode()
     el = (time.perf_counter() - t) / a.steps
     val = sample_bytes / el / 1e9
-    threads = orc.max_threads()
+    threads = min(threads, nseq)
     line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
             "n_gpus": ws_n, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(el * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
