@@ -196,10 +196,15 @@ def run_ours(a):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
+        # whole steps, nothing between the launches
         start.record(stream)
         for i in range(a.steps):
-            step(evs[i])
+            step()
         end.record(stream)
+        torch.cuda.synchronize()
+        # the same steps again with events around each tile kernel (its roofline)
+        for i in range(a.steps):
+            step(evs[i])
         torch.cuda.synchronize()
     if ws_n > 1:
         torch.distributed.barrier()
@@ -271,14 +276,15 @@ def run_ours(a):
                    "global_batch": 16 * ws_n, "seq_len": "120000-131072",
                    "parallelism": f"replicas x{ws_n}",
                    "l2": "no flush: each call streams more than the 129 MB L2",
-                   "mma": "mma.sync m16n8k16 f16 x f16 -> f32"},
+                   "mma": "mma.sync m16n8k16 f16 x f16 -> f32",
+                   "merge": "separate pa_decode_reduce launch"},
         "per_variant": per,
         "roofline": {"bound": "hbm", "kernel": f"pa_tile_kernel ({dom['case'].name})",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic_from_profile()},
         "e2e": e2e,
-        "gpu_launches": 3 * len(variants) * a.steps,
+        "gpu_launches": 3 * len(variants) * a.steps,  # plan, tile, reduce per variant
         "clocks": clk.summary(),
     }
     if a.batch is not None or a.variant != "both":

@@ -105,10 +105,12 @@ typedef struct pa_decode_args {
   int32_t q_scale_per_row;    /* e4m3 query: 0 = q_scale[1], 1 = q_scale[B*qlen*Hq] */
   float softmax_scale;        /* <= 0 selects 1/sqrt(head_dim) */
   /* work split */
-  int32_t max_partitions;     /* >= 1 caps partitions per sequence; 1 = direct output, no
-                                 reduce; <= 0 picks a default from batch and the SM count */
+  int32_t max_partitions;     /* >= 1 caps partitions per sequence (at most 128); 1 = direct
+                                 output, no reduce; <= 0 picks 128 */
   int32_t task_budget;        /* target number of tasks; <= 0 picks a default */
-  int32_t reserved0;
+  int32_t merge_in_decode;    /* 1: pa_decode merges the partitions of split sequences itself
+                                 (the last task of a sequence to finish does it) and
+                                 pa_decode_reduce launches nothing; 0: pa_decode_reduce merges */
   /* tensors (device pointers) */
   const void* query;          /* [B*qlen, Hq, D] bf16 or e4m3 */
   int64_t q_stride_token;     /* elements between consecutive (s, i) rows */
@@ -159,7 +161,8 @@ pa_status pa_decode(const pa_decode_args* args, void* workspace, size_t workspac
 
 /* Merges the partials of every sequence with two or more partitions, in a fixed
  * partition order: M = max_p m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
- * A no-op launch-free return when max_partitions is 1.  ("[FlyDSL] pa_decode: MXFP4
+ * A no-op launch-free return when max_partitions is 1 or merge_in_decode is set (the
+ * same merge, in the same order, then runs at the end of pa_decode).  ("[FlyDSL] pa_decode: MXFP4
  * K/V ...", Self-Review: the partition reducer.) */
 pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
                            size_t workspace_bytes, void* stream);

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   __shared__ int sh32b[32];
   const int tid = threadIdx.x;
   const int cap = pp.W * pp.S;
+  pdl_wait_prior();          // the previous kernel may still read this workspace
+  pdl_launch_dependents();  // the tile kernel may launch now; it waits for this grid
   if (tid == 0) *pp.status = 0;
   __syncthreads();
   int clamped = 0;
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     if (s < pp.B) {
       pp.nparts[s] = P;
       pp.part_base[s] = carry_slots + off_s;
+      for (int h = 0; h < pp.Hkv; ++h) pp.counters[s * pp.Hkv + h] = 0;
       for (int h = 0; h < pp.Hkv; ++h)
         for (int q = 0; q < P; ++q) {
           PlanTask tk;
@@ -116,8 +119,11 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
 // One warp per output row.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  __shared__ float wsh[8][128];  // normalised partition weights of each warp's row
+  pdl_wait_prior();  // the tile kernel's partials are complete and visible from here on
+  pdl_launch_dependents();  // a following plan may launch; it waits before writing
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long row = (long long)blockIdx.x * 8 + wid;
   const long long rows = (long long)rp.B * rp.qlen * rp.Hq;
   if (row >= rows) return;
   const int s = (int)(row / ((long long)rp.qlen * rp.Hq));
@@ -128,7 +134,8 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   const int r = i * rp.G + h % rp.G;
   const long long base = (long long)rp.part_base[s] + (long long)hkv * P;
   const float2* ml = reinterpret_cast<const float2*>(rp.part_ml);
-  // M and the total weight: lane-strided partials, then a fixed shuffle tree
+  float* w = wsh[wid];
+  // M and the weights: lanes over partitions, then a fixed shuffle tree
   float M = -INFINITY;
   for (int q = lane; q < P; q += 32) M = fmaxf(M, ml[(base + q) * rp.R + r].x);
 #pragma unroll
@@ -137,28 +144,44 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   float W = 0.f;
   for (int q = lane; q < P; q += 32) {
     const float2 e = ml[(base + q) * rp.R + r];
-    W += e.y * fast_exp2(e.x - mb);
+    w[q] = e.y * fast_exp2(e.x - mb);
+    W += w[q];
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
   const float inv = W > 0.f ? 1.f / W : 0.f;
+  __syncwarp();
+  for (int q = lane; q < P; q += 32) w[q] *= inv;
+  __syncwarp();
   __nv_bfloat16* dst = rp.out + (long long)(s * rp.qlen + i) * rp.o_st + (long long)h * rp.o_sh;
   // each lane owns 4 consecutive dims per 128; partitions are added in a fixed order
   for (int d0 = 4 * lane; d0 < rp.D; d0 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < P; ++q) {
-      const float2 e = ml[(base + q) * rp.R + r];
-      const float w = e.y * fast_exp2(e.x - mb);
-      const float4 v = *reinterpret_cast<const float4*>(rp.part_o + ((base + q) * rp.R + r) * rp.D + d0);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    int q = 0;
+    for (; q + 4 <= P; q += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = *reinterpret_cast<const float4*>(rp.part_o + ((base + q + u) * rp.R + r) * rp.D + d0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x += w[q + u] * v[u].x;
+        acc.y += w[q + u] * v[u].y;
+        acc.z += w[q + u] * v[u].z;
+        acc.w += w[q + u] * v[u].w;
+      }
     }
-    dst[d0] = __float2bfloat16_rn(acc.x * inv);
-    dst[d0 + 1] = __float2bfloat16_rn(acc.y * inv);
-    dst[d0 + 2] = __float2bfloat16_rn(acc.z * inv);
-    dst[d0 + 3] = __float2bfloat16_rn(acc.w * inv);
+    for (; q < P; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(rp.part_o + ((base + q) * rp.R + r) * rp.D + d0);
+      acc.x += w[q] * v.x;
+      acc.y += w[q] * v.y;
+      acc.z += w[q] * v.z;
+      acc.w += w[q] * v.w;
+    }
+    dst[d0] = __float2bfloat16_rn(acc.x);
+    dst[d0 + 1] = __float2bfloat16_rn(acc.y);
+    dst[d0 + 2] = __float2bfloat16_rn(acc.z);
+    dst[d0 + 3] = __float2bfloat16_rn(acc.w);
   }
 }
 
@@ -196,6 +219,7 @@ using pa::WsLayout;
 
 constexpr int kMaxRows = 32;         // G * qlen served by the tile kernels
 constexpr int kDefaultMaxParts = 128;
+constexpr int kMaxParts = 128;  // the in-decode merge keeps [rows, partitions] weights in smem
 
 int device_sms(int* out) {
   int dev = 0;
@@ -242,6 +266,7 @@ pa_status validate(const pa_decode_args* a) {
   if (a->kv_dtype < 0 || a->kv_dtype > 2 || a->kv_scale < 0 || a->kv_scale > 3) return PA_ERR_INVALID_ARG;
   if (!combo) return PA_ERR_UNSUPPORTED;
   if (a->q_dtype != PA_Q_BF16 && a->q_dtype != PA_Q_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (a->merge_in_decode != 0 && a->merge_in_decode != 1) return PA_ERR_INVALID_ARG;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
@@ -290,7 +315,7 @@ pa_status split_params(const pa_decode_args* a, int* budget, int* maxp) {
   }
   *budget = b;
   *maxp = a->max_partitions > 0 ? a->max_partitions : kDefaultMaxParts;
-  if (*maxp > 32767) *maxp = 32767;
+  if (*maxp > kMaxParts) *maxp = kMaxParts;
   return PA_OK;
 }
 
@@ -315,6 +340,8 @@ pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
   off = align_up(off + 4 * (size_t)B, 256);
   L->part_base = off;
   off = align_up(off + 4 * (size_t)B, 256);
+  L->counters = off;
+  off = align_up(off + 4 * (size_t)B * a->num_kv_heads, 256);
   L->tasks = off;
   off = align_up(off + sizeof(pa::PlanTask) * (size_t)L->capacity, 256);
   L->part_ml = off;
@@ -413,8 +440,20 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   pp.ntasks = reinterpret_cast<int*>(w + L.ntasks);
   pp.nparts = reinterpret_cast<int*>(w + L.nparts);
   pp.part_base = reinterpret_cast<int*>(w + L.part_base);
+  pp.counters = reinterpret_cast<int*>(w + L.counters);
   pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
-  pa::pa_plan_kernel<<<1, 1024, 0, reinterpret_cast<cudaStream_t>(stream)>>>(pp);
+  int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
+  threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pa::pa_plan_kernel, pp) != cudaSuccess) return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -474,6 +513,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.tasks = reinterpret_cast<const pa::PlanTask*>(w + L.tasks);
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_o = reinterpret_cast<float*>(w + L.part_o);
+  p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
   int rc;
   if (kind == pa::KIND_BF16)
     rc = pa::launch_tile_bf16(p, tk, tv, L.capacity, sms, stream);
@@ -489,7 +529,7 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
   if (st != PA_OK) return st;
   WsLayout L;
   if ((st = check_ws(a, ws, bytes, &L)) != PA_OK) return st;
-  if (a->batch == 0 || L.max_partitions < 2) return PA_OK;
+  if (a->batch == 0 || L.max_partitions < 2 || a->merge_in_decode) return PA_OK;
   uint8_t* w = static_cast<uint8_t*>(ws);
   pa::ReduceParams rp;
   rp.B = a->batch;
@@ -507,7 +547,16 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
   rp.o_sh = a->out_stride_head;
   const long long rows = (long long)a->batch * a->qlen * a->num_q_heads;
   const unsigned grid = (unsigned)((rows + 7) / 8);
-  pa::pa_reduce_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(rp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pa::pa_reduce_kernel, rp) != cudaSuccess) return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

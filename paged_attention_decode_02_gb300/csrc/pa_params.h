@@ -24,6 +24,7 @@ struct WsLayout {
   size_t ntasks;
   size_t nparts;     // int32 [B]: partitions of each sequence
   size_t part_base;  // int32 [B]: first partial slot of each split sequence
+  size_t counters;   // int32 [B*Hkv]: finished tasks per split (sequence, KV head)
   size_t tasks;      // PlanTask [capacity]
   size_t part_ml;    // float2 [slots, R]: (max in log2 units, sum)
   size_t part_o;     // float [slots, R, D]: normalised partial outputs
@@ -57,6 +58,7 @@ struct DecodeParams {
   const PlanTask* tasks;
   float* part_ml;
   float* part_o;
+  int* counters;  // non-null: merge split sequences at the end of the tile kernel
 };
 
 struct PlanParams {
@@ -68,6 +70,7 @@ struct PlanParams {
   int* ntasks;
   int* nparts;
   int* part_base;
+  int* counters;
   PlanTask* tasks;
 };
 

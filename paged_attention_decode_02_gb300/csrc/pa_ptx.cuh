@@ -88,6 +88,16 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+// Lets the next kernel in the stream (launched with programmatic serialisation) start
+// its prologue; it must still wait before touching this kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the preceding kernel in the stream has completed and its writes are visible
+// (a no-op when this kernel was launched without programmatic serialisation).
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- named barriers -------------------------------------------------------------
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -948,6 +948,77 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         }
       }
     }
+    // ---------------- fused partition merge (optional) ----------------
+    // The task that finishes a split (sequence, KV head) last merges all its partitions,
+    // in partition order, with the reduce kernel's formula (counters zeroed by the plan).
+    if (p.counters != nullptr && nparts > 1) {
+      volatile int* mflag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG) + 1;
+      __threadfence();  // this task's partials are visible before it is counted
+      named_bar(BAR_CONSUMERS, C::NCW * 32);
+      if (threadIdx.x == 0) *mflag = atomicAdd(p.counters + (int64_t)s * p.Hkv + hkv, 1) == nparts - 1;
+      named_bar(BAR_CONSUMERS, C::NCW * 32);
+      if (*mflag) {
+        __threadfence();
+        const int64_t base = (int64_t)p.part_base[s] + (int64_t)hkv * nparts;
+        const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
+        float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= D)
+        // one warp per row: lanes over partitions, shuffle-tree max and sum
+        for (int r = cw; r < p.R; r += C::NCW) {
+          float M = -INFINITY;
+          for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&pml[(base + q) * p.R + r]).x);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          const float mb = M == -INFINITY ? 0.f : M;
+          float W = 0.f;
+          for (int q = lane; q < nparts; q += 32) {
+            const float2 e = __ldcg(&pml[(base + q) * p.R + r]);
+            const float w = e.y * fast_exp2(e.x - mb);
+            wts[r * nparts + q] = w;
+            W += w;
+          }
+#pragma unroll
+          for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+          const float inv = W > 0.f ? 1.f / W : 0.f;
+          __syncwarp();
+          for (int q = lane; q < nparts; q += 32) wts[r * nparts + q] *= inv;
+        }
+        named_bar(BAR_CONSUMERS, C::NCW * 32);
+        // float4 columns, partitions in order; loads are independent of the sum
+        const float4* po4 = reinterpret_cast<const float4*>(p.part_o);
+        for (int idx = threadIdx.x; idx < p.R * (C::D / 4); idx += C::NTHREADS) {
+          const int r = idx / (C::D / 4), d4 = idx % (C::D / 4);
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          int q = 0;
+          for (; q + 4 <= nparts; q += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldcg(&po4[((base + q + u) * p.R + r) * (C::D / 4) + d4]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float w = wts[r * nparts + q + u];
+              acc.x += w * v[u].x;
+              acc.y += w * v[u].y;
+              acc.z += w * v[u].z;
+              acc.w += w * v[u].w;
+            }
+          }
+          for (; q < nparts; ++q) {
+            const float4 v = __ldcg(&po4[((base + q) * p.R + r) * (C::D / 4) + d4]);
+            const float w = wts[r * nparts + q];
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+          }
+          const int i = r / p.G, h = hkv * p.G + r % p.G;
+          __nv_bfloat16* dst = p.out + ((int64_t)s * p.qlen + i) * p.o_st + (int64_t)h * p.o_sh + 4 * d4;
+          dst[0] = __float2bfloat16_rn(acc.x);
+          dst[1] = __float2bfloat16_rn(acc.y);
+          dst[2] = __float2bfloat16_rn(acc.z);
+          dst[3] = __float2bfloat16_rn(acc.w);
+        }
+      }
+    }
   }
   // Never leave while a copy into this CTA's shared memory may still be in flight (only
   // possible after a timed-out wait).
@@ -975,6 +1046,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_launch_dependents();  // the reduce kernel may launch; it waits for this grid's results
+  pdl_wait_prior();         // the plan's task list is complete and visible from here on
   const int ntasks = *p.ntasks;
   warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, ntasks, threadIdx.x >> 5, threadIdx.x & 31);
 }
@@ -992,7 +1065,20 @@ int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap&
   int grid = num_sms * C::MINB;
   if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
-  pa_tile_kernel<C><<<grid, C::NTHREADS, C::SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(p, tk, tv);
+  // Programmatic serialisation: this grid launches while the plan kernel runs and waits
+  // for it (griddepcontrol.wait) before reading the task list.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pa_tile_kernel<C>, p, tk, tv);
+  if (e != cudaSuccess) return (int)e;
   return (int)cudaGetLastError();
 }
 

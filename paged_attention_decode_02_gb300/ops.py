@@ -40,7 +40,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("kv_scale", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
         ("q_scale_per_row", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
         ("max_partitions", ctypes.c_int32), ("task_budget", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("merge_in_decode", ctypes.c_int32),
         ("query", ctypes.c_void_p), ("q_stride_token", ctypes.c_int64),
         ("q_stride_head", ctypes.c_int64), ("q_scale", ctypes.c_void_p),
         ("key_cache", ctypes.c_void_p), ("value_cache", ctypes.c_void_p),
@@ -118,7 +118,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               block_tables: torch.Tensor, context_lens: torch.Tensor, out: torch.Tensor, *,
               key_scale: Optional[torch.Tensor] = None, value_scale: Optional[torch.Tensor] = None,
               q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
-              max_partitions: int = 0, task_budget: int = 0) -> PaDecodeArgs:
+              max_partitions: int = 0, task_budget: int = 0,
+              merge_in_decode: bool = False) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -160,6 +161,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     a.q_scale_per_row = int(q_scale is not None and q_scale.numel() > 1)
     a.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)
     a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
+    a.merge_in_decode = int(bool(merge_in_decode))
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
@@ -253,7 +255,8 @@ def pa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
 
 
 def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions: int = 0,
-           task_budget: int = 0, workspace: Optional[torch.Tensor] = None):
+           task_budget: int = 0, workspace: Optional[torch.Tensor] = None,
+           merge_in_decode: bool = False):
     """plan + decode + reduce on a synthetic-workload dict (device tensors)."""
     case = problem["case"]
     q = problem["query"]
@@ -265,7 +268,7 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      problem["context_lens"], out, key_scale=problem["key_scale"],
                      value_scale=problem["value_scale"], q_scale=problem["q_scale"],
                      softmax_scale=case.scale_qk(), max_partitions=max_partitions,
-                     task_budget=task_budget)
+                     task_budget=task_budget, merge_in_decode=merge_in_decode)
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -74,6 +74,7 @@ REFUSED = [
                           kv_stride_token=64, kv_stride_head=64 * 128, kv_stride_block=64 * 128),
      ops.PA_ERR_UNSUPPORTED),
     ("unknown kv dtype", dict(kv_dtype=7), ops.PA_ERR_INVALID_ARG),
+    ("merge flag not 0/1", dict(merge_in_decode=2), ops.PA_ERR_INVALID_ARG),
     ("null query", dict(query=None), ops.PA_ERR_INVALID_ARG),
     ("null scales", dict(key_scale=None), ops.PA_ERR_INVALID_ARG),
     ("e4m3 query without scale", dict(q_dtype=ops.PA_Q_FP8_E4M3), ops.PA_ERR_INVALID_ARG),

@@ -48,11 +48,12 @@ SMALL = [
 
 
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"{c.name}-s{c.seed}")
-@pytest.mark.parametrize("max_partitions", [0, 1], ids=["split", "direct"])
-def test_small_cases_match_oracle(case, max_partitions):
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_small_cases_match_oracle(case, mode):
     p = synth.make(case)
     ref = util.oracle_decode(p)
-    got = run_gpu(p, max_partitions=max_partitions, task_budget=64)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=64,
+                  merge_in_decode=mode == "fused")
     util.assert_parity(got, ref, case.kv, case.name)
 
 
@@ -72,6 +73,7 @@ def test_ragged_edges(lens):
 
 @pytest.mark.parametrize("kv", [synth.KV_MXFP4, synth.KV_FP8], ids=["5a_mxfp4", "5b_fp8_token"])
 def test_long_context_full_size_sampled(kv):
+    # the launch configuration bench.py times: default split, separate reduce
     case = synth.config5(kv)
     p = synth.make(case)
     got = run_gpu(p)
@@ -79,6 +81,15 @@ def test_long_context_full_size_sampled(kv):
     ref = util.oracle_decode(p, seqs=seqs)
     util.assert_parity(got[seqs], ref, case.kv, case.name)
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("kv", [synth.KV_MXFP4, synth.KV_FP8], ids=["5a_mxfp4", "5b_fp8_token"])
+def test_long_context_fused_merge_sampled(kv):
+    case = synth.config5(kv, batch=6, seed=2200)
+    p = synth.make(case)
+    got = run_gpu(p, merge_in_decode=True)
+    seqs = [0, 5]
+    util.assert_parity(got[seqs], util.oracle_decode(p, seqs=seqs), case.kv, case.name)
 
 
 def test_mxfp4_batch_4096_sampled():

@@ -57,14 +57,16 @@ def _cases():
 
 
 @pytest.mark.parametrize("case", _cases(), ids=lambda c: c.name)
-@pytest.mark.parametrize("max_partitions", [0, 1], ids=["split", "direct"])
-def test_unowned_fill_is_bit_identical(case, max_partitions):
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_unowned_fill_is_bit_identical(case, mode):
+    kw = dict(max_partitions=1 if mode == "direct" else 0, task_budget=16,
+              merge_in_decode=mode == "fused")
     p = synth.make(case)
-    base = gpu_bits(synth.refill(p, synth.FILL_ZERO), max_partitions=max_partitions, task_budget=16)
+    base = gpu_bits(synth.refill(p, synth.FILL_ZERO), **kw)
     assert np.isfinite(_f32(base)).all()
     fills = (synth.FILL_NAN, synth.FILL_INF, synth.FILL_RANDOM)
     for fill in fills:
-        got = gpu_bits(synth.refill(p, fill), max_partitions=max_partitions, task_budget=16)
+        got = gpu_bits(synth.refill(p, fill), **kw)
         assert np.isfinite(_f32(got)).all(), fill
         assert np.array_equal(got, base), fill
 
