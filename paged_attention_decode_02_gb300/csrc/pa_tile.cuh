@@ -305,13 +305,6 @@ constexpr float kLazyLog2 = 8.f;
 constexpr float kLazyVref = 8.f;
 constexpr int kLazyExp = 3;
 
-// f16 bits of 2^x for an integer x <= 15 (0 below 2^-24).
-__device__ __forceinline__ uint32_t f16_exp2i(int x) {
-  if (x >= -14) return (uint32_t)(x + 15) << 10;
-  if (x >= -24) return 1u << (x + 24);
-  return 0u;
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -397,12 +390,15 @@ __device__ __forceinline__ void stage_compute(
       }
       rescale_v = true;
     }
+    // K: 2^(e-127) as fp32; V: 2^(e-emax) as f16 (factors below 2^-14 flush to zero: such
+    // a block is at least 2^14 times smaller than the largest one seen for that block)
+    const uint32_t kown = own ? 0xFFFFFFFFu : 0u;
 #pragma unroll
     for (int b = 0; b < C::NBLK; ++b) {
       const uint32_t ek = (kw >> (8 * b)) & 0xFF;
       const int ev = (int)((vwd >> (8 * b)) & 0xFF);
-      ktab[b * C::TW + lane] = own ? e8m0_to_f32(ek) : 0.f;
-      vtab[b * C::TW + lane] = own ? (uint16_t)f16_exp2i(ev - A.emax[b]) : (uint16_t)0;
+      ktab[b * C::TW + lane] = __uint_as_float((ek << 23) & kown);
+      vtab[b * C::TW + lane] = (uint16_t)(((uint32_t)max(ev - A.emax[b] + 15, 0) << 10) & kown);
     }
     __syncwarp();
   }
