@@ -62,13 +62,19 @@ TOL_MAX_ABS = 3e-2
 # 2^-7 |x| (the round-to-nearest error alone reaches 2^-9 |x|).  The absolute bound is
 # applied beyond that quantum, since MXFP4 outputs reach |48| at the workloads' e8m0
 # range, where a single bf16 rounding is 0.125.
-BF16_QUANTUM = 2.0 ** -8
+def bf16_ulp(x) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significant bits): 2^(floor(log2 |x|) - 7)."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.exp2(e - 7), 0.0)
 
 
 def excess_abs(got, ref) -> float:
+    """max(|got - ref| - ulp_bf16(ref)): the output is bf16, so a result computed with any
+    error at all may round to the neighbour of the correctly rounded value."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    d = np.abs(got - ref) - BF16_QUANTUM * np.abs(ref)
+    d = np.abs(got - ref) - bf16_ulp(ref)
     return float(d.max()) if d.size else 0.0
 
 
@@ -78,6 +84,6 @@ def assert_parity(got, ref, kv: str, what: str = ""):
     e = excess_abs(got, ref)
     assert np.isfinite(np.asarray(got, np.float64)).all(), f"{what}: non-finite output"
     assert r <= TOL_REL_L2[kv], f"{what}: rel-L2 {r:.3e} > {TOL_REL_L2[kv]:.1e}"
-    assert e <= TOL_MAX_ABS, (f"{what}: max-abs beyond the bf16 quantum {e:.3e} > "
+    assert e <= TOL_MAX_ABS, (f"{what}: max-abs beyond one bf16 ulp {e:.3e} > "
                               f"{TOL_MAX_ABS:.1e} (raw max-abs {m:.3e})")
     return r, m
