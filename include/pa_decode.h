@@ -105,11 +105,11 @@ typedef struct pa_decode_args {
   int32_t q_scale_per_row;    /* e4m3 query: 0 = q_scale[1], 1 = q_scale[B*qlen*Hq] */
   float softmax_scale;        /* <= 0 selects 1/sqrt(head_dim) */
   /* work split */
-  int32_t max_partitions;     /* >= 1 caps partitions per sequence (at most 128); 1 = direct
-                                 output, no reduce; <= 0 picks 128 */
-  int32_t task_budget;        /* target number of tasks; <= 0 picks a default */
-  int32_t merge_in_decode;    /* 1: pa_decode merges the partitions of split sequences itself
-                                 (the last task of a sequence to finish does it) and
+  int32_t max_partitions;     /* >= 1 caps partitions per (sequence, KV head) (at most 128);
+                                 1 = direct output, no reduce; <= 0 picks 128 */
+  int32_t task_budget;        /* work chunks = tile-kernel CTAs; <= 0 picks the SM count */
+  int32_t merge_in_decode;    /* 1: pa_decode merges the partitions of split units itself
+                                 (the last task of a unit to finish does it) and
                                  pa_decode_reduce launches nothing; 0: pa_decode_reduce merges */
   /* tensors (device pointers) */
   const void* query;          /* [B*qlen, Hq, D] bf16 or e4m3 */
@@ -145,21 +145,24 @@ size_t pa_decode_workspace_size(const pa_decode_args* args);
 pa_status pa_decode_validate(const pa_decode_args* args);
 
 /* Builds the tile/partition work list on the device from context_lens: ceil(L/256)
- * tiles per sequence, split into at most max_partitions near-equal tasks per
- * (sequence, KV head) so that the total is close to task_budget.  Clears the device
- * status word.  One launch, 1 CTA.  ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit
- * messages: planned tasks, direct output with one partition, plan-free split.) */
+ * tiles per (sequence, KV head) unit; all units' tiles, laid end to end, are cut into
+ * task_budget chunks of equal length (one per tile-kernel CTA), longer when needed so
+ * that no unit touches more than max_partitions chunks.  A unit crossing chunk
+ * boundaries becomes one partition per chunk it touches; with max_partitions 1 each
+ * unit is one task, run by the chunk it starts in.  Clears the device status word.  One
+ * launch, 1 CTA.  ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit messages: planned tasks,
+ * direct output with one partition, tasks from a CU budget.) */
 pa_status pa_decode_plan(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                          void* stream);
 
-/* Runs the tile kernel over the planned tasks: block-table page gather (TMA), QK,
- * online softmax, boundary-tile masking, PV.  Sequences with one partition get their
- * output rows written here (context 0 gives zeros); others get partials in the
- * workspace.  ("[FlyDSL] pa_decode: zero V rows past the context before PV", Fix.) */
+/* Runs the tile kernel over the planned tasks, task_budget CTAs, each on its chunk:
+ * block-table page gather (TMA), QK, online softmax, boundary-tile masking, PV.  Units
+ * with one partition get their output rows written here (context 0 gives zeros);
+ * others get partials in the workspace.  ("[FlyDSL] pa_decode: zero V rows past the context before PV", Fix.) */
 pa_status pa_decode(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                     void* stream);
 
-/* Merges the partials of every sequence with two or more partitions, in a fixed
+/* Merges the partials of every unit with two or more partitions, in a fixed
  * partition order: M = max_p m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
  * A no-op launch-free return when max_partitions is 1 or merge_in_decode is set (the
  * same merge, in the same order, then runs at the end of pa_decode).  ("[FlyDSL] pa_decode: MXFP4

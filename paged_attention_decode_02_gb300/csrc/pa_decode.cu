@@ -3,18 +3,25 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "pa_configs.cuh"
+#include "pa_tc.cuh"
 #include "../../include/pa_decode.h"
 
 namespace pa {
 
 // ------------------------------------------------------------------------------------
-// Plan: ceil(L/256) tiles per sequence ("[FlyDSL] pa_decode: zero V rows past the context
-// before PV", Root cause), split into partitions proportional to the sequence's share of
-// all tiles so that the task count stays within the budget ("[FlyDSL] pa_decode: MXFP4
-// K/V ...", plan-free commit: tasks from a 2 x CU budget; max_partitions caps the split).
+// Plan: ceil(L/256) tiles per (sequence, KV head) unit ("[FlyDSL] pa_decode: zero V rows
+// past the context before PV", Root cause).  The units' tiles, laid end to end, are cut
+// into `budget` chunks of equal length, one per tile-kernel CTA; a unit crossing a chunk
+// boundary becomes several partitions whose partials are merged afterwards ("[FlyDSL]
+// pa_decode: MXFP4 K/V ...", commit messages: planned tasks, direct output with one
+// partition, tasks from a CU budget; max_partitions caps the split).  Equal chunks keep
+// every CTA busy for the same number of tiles whatever the mix of context lengths.
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ int clamp_len(int L, int cap, int* clamped) {
   if (L < 0) return 0;
@@ -52,69 +59,132 @@ __device__ T block_exclusive_scan(T v, T* total, T* sh) {  // sh: >= 32 elements
   return before;
 }
 
+// How a unit of n tiles starting at global tile U splits: one partition per chunk it
+// touches (one in all when it is empty or splitting is off).
+struct ChunkGrid {
+  long long C;        // tiles per chunk
+  long long nchunks;  // chunks that hold tiles (>= 1)
+  int maxp;
+};
+
+__device__ __forceinline__ int unit_parts(const ChunkGrid& cg, long long U, int n) {
+  if (n == 0 || cg.maxp < 2) return 1;
+  return (int)((U + n - 1) / cg.C - U / cg.C + 1);
+}
+
+// Tiles [begin, end) of partition q of the unit, and its chunk.
+__device__ __forceinline__ void unit_part(const ChunkGrid& cg, long long U, int n, int q, int* begin,
+                                          int* end, int* chunk) {
+  if (n == 0 || cg.maxp < 2) {
+    const long long c = U / cg.C;
+    *begin = 0;
+    *end = n;
+    *chunk = (int)(c < cg.nchunks - 1 ? c : cg.nchunks - 1);
+    return;
+  }
+  const long long c = U / cg.C + q;
+  const long long g0 = c * cg.C > U ? c * cg.C : U;
+  const long long g1 = (c + 1) * cg.C < U + n ? (c + 1) * cg.C : U + n;
+  *begin = (int)(g0 - U);
+  *end = (int)(g1 - U);
+  *chunk = (int)c;
+}
+
 __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   __shared__ long long sh64[32];
   __shared__ int sh32[32];
   __shared__ int sh32b[32];
+  __shared__ int shmax;
   const int tid = threadIdx.x;
   const int cap = pp.W * pp.S;
   pdl_wait_prior();          // the previous kernel may still read this workspace
   pdl_launch_dependents();  // the tile kernel may launch now; it waits for this grid
-  if (tid == 0) *pp.status = 0;
+  if (tid == 0) {
+    *pp.status = 0;
+    shmax = 0;
+  }
   __syncthreads();
-  int clamped = 0;
+  int clamped = 0, lmax = 0;
   long long local = 0;
-  for (int s = tid; s < pp.B; s += blockDim.x)
-    local += (clamp_len(pp.ctx[s], cap, &clamped) + kTileTokens - 1) / kTileTokens;
-  long long total_tiles;
-  (void)block_exclusive_scan<long long>(local, &total_tiles, sh64);
-  total_tiles *= pp.Hkv;
+  for (int s = tid; s < pp.B; s += blockDim.x) {
+    const int n = (clamp_len(pp.ctx[s], cap, &clamped) + kTileTokens - 1) / kTileTokens;
+    local += n;
+    lmax = n > lmax ? n : lmax;
+  }
+  if (lmax > 0) atomicMax(&shmax, lmax);
   if (clamped) atomicOr(pp.status, ST_CLAMPED);
+  long long seq_tiles;
+  (void)block_exclusive_scan<long long>(local, &seq_tiles, sh64);  // also orders shmax
+  const long long T = seq_tiles * pp.Hkv;
+  ChunkGrid cg;
+  cg.maxp = pp.max_partitions;
+  cg.C = (T + pp.budget - 1) / pp.budget;
+  if (cg.C < 1) cg.C = 1;
+  if (cg.maxp >= 2) {  // no unit may touch more than max_partitions chunks
+    const long long cmin = (long long)(shmax - 1) / (cg.maxp - 1) + 1;
+    if (cg.C < cmin) cg.C = cmin;
+  }
+  cg.nchunks = T > 0 ? (T + cg.C - 1) / cg.C : 1;
 
+  long long carry_tiles = 0;
   int carry_tasks = 0, carry_slots = 0;
   for (int base = 0; base < pp.B; base += blockDim.x) {
     const int s = base + tid;
-    int P = 0, tiles = 0;
-    if (s < pp.B) {
-      int dummy = 0;
-      tiles = (clamp_len(pp.ctx[s], cap, &dummy) + kTileTokens - 1) / kTileTokens;
-      if (tiles == 0) {
-        P = 1;
-      } else {
-        long long share = total_tiles > 0 ? (long long)tiles * pp.budget / total_tiles : 1;
-        if (share < 1) share = 1;
-        if (share > pp.max_partitions) share = pp.max_partitions;
-        if (share > tiles) share = tiles;
-        P = (int)share;
+    int dummy = 0;
+    const int n = s < pp.B ? (clamp_len(pp.ctx[s], cap, &dummy) + kTileTokens - 1) / kTileTokens : 0;
+    long long round_tiles;
+    const long long before = block_exclusive_scan<long long>((long long)n, &round_tiles, sh64);
+    const long long U0 = (carry_tiles + before) * pp.Hkv;  // global first tile of unit (s, 0)
+    int ntask = 0, nslot = 0;
+    if (s < pp.B)
+      for (int h = 0; h < pp.Hkv; ++h) {
+        const int P = unit_parts(cg, U0 + (long long)h * n, n);
+        ntask += P;
+        nslot += P >= 2 ? P : 0;
       }
-    }
-    const int ntask = s < pp.B ? P * pp.Hkv : 0;
-    const int nslot = (s < pp.B && P >= 2) ? P * pp.Hkv : 0;
     int tot_t, tot_s;
     const int off_t = block_exclusive_scan<int>(ntask, &tot_t, sh32);
     const int off_s = block_exclusive_scan<int>(nslot, &tot_s, sh32b);
     if (s < pp.B) {
-      pp.nparts[s] = P;
-      pp.part_base[s] = carry_slots + off_s;
-      for (int h = 0; h < pp.Hkv; ++h) pp.counters[s * pp.Hkv + h] = 0;
-      for (int h = 0; h < pp.Hkv; ++h)
-        for (int q = 0; q < P; ++q) {
+      int t = carry_tasks + off_t, slot = carry_slots + off_s;
+      for (int h = 0; h < pp.Hkv; ++h) {
+        const long long U = U0 + (long long)h * n;
+        const int P = unit_parts(cg, U, n);
+        const int u = s * pp.Hkv + h;
+        pp.nparts[u] = P;
+        pp.part_base[u] = P >= 2 ? slot : 0;
+        pp.counters[u] = 0;
+        if (P >= 2) slot += P;
+        for (int q = 0; q < P; ++q, ++t) {
           PlanTask tk;
+          int chunk;
           tk.seq = s;
           tk.hkv_part = h | (q << 16);
-          tk.tile_begin = (int)((long long)q * tiles / P);
-          tk.tile_end = (int)((long long)(q + 1) * tiles / P);
-          pp.tasks[carry_tasks + off_t + h * P + q] = tk;
+          unit_part(cg, U, n, q, &tk.tile_begin, &tk.tile_end, &chunk);
+          pp.tasks[t] = tk;
+          pp.task_chunk[t] = chunk;
         }
+      }
     }
+    carry_tiles += round_tiles;
     carry_tasks += tot_t;
     carry_slots += tot_s;
   }
   if (tid == 0) *pp.ntasks = carry_tasks;
+  __syncthreads();  // this block's task_chunk writes are visible to all its threads
+  // Tasks are in unit order, hence in non-decreasing chunk order: chunk c runs tasks
+  // [chunk_first[c], chunk_first[c + 1]).  Chunks past the last task hold none.
+  for (int t = tid; t < carry_tasks; t += blockDim.x) {
+    const int c = pp.task_chunk[t];
+    const int prev = t == 0 ? -1 : pp.task_chunk[t - 1];
+    for (int k = prev + 1; k <= c; ++k) pp.chunk_first[k] = t;
+  }
+  const int last = carry_tasks > 0 ? pp.task_chunk[carry_tasks - 1] + 1 : 0;
+  for (int c = last + tid; c <= pp.budget; c += blockDim.x) pp.chunk_first[c] = carry_tasks;
 }
 
 // ------------------------------------------------------------------------------------
-// Reduce: merge the partitions of each split sequence in a fixed order
+// Reduce: merge the partitions of each split (sequence, KV head) unit in a fixed order
 // ("[FlyDSL] pa_decode: MXFP4 K/V ...", Self-Review: the partition reducer).
 // One warp per output row.
 // ------------------------------------------------------------------------------------
@@ -127,12 +197,13 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   const long long rows = (long long)rp.B * rp.qlen * rp.Hq;
   if (row >= rows) return;
   const int s = (int)(row / ((long long)rp.qlen * rp.Hq));
-  const int P = rp.nparts[s];
-  if (P < 2) return;
   const int rem = (int)(row % ((long long)rp.qlen * rp.Hq));
   const int i = rem / rp.Hq, h = rem % rp.Hq, hkv = h / rp.G;
+  const int u = s * rp.Hkv + hkv;
+  const int P = rp.nparts[u];
+  if (P < 2) return;
   const int r = i * rp.G + h % rp.G;
-  const long long base = (long long)rp.part_base[s] + (long long)hkv * P;
+  const long long base = rp.part_base[u];
   const float2* ml = reinterpret_cast<const float2*>(rp.part_ml);
   float* w = wsh[wid];
   // M and the weights: lanes over partitions, then a fixed shuffle tree
@@ -321,6 +392,16 @@ pa_status split_params(const pa_decode_args* a, int* budget, int* maxp) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
+// and pages of at least 8 tokens, with the separate reduce.  It runs when
+// PA_DECODE_KERNEL=tc is set in the environment (read at each call); otherwise every
+// shape runs the mma.sync kernel, the faster of the two on the long-context workloads.
+bool tc_kernel_applies(const pa_decode_args* a, int rows) {
+  const char* e = getenv("PA_DECODE_KERNEL");
+  const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
+  return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode;
+}
+
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
   int budget = 0, maxp = 0;
   pa_status st = split_params(a, &budget, &maxp);
@@ -330,20 +411,27 @@ pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
   const int B = a->batch;
   L->budget = budget;
   L->max_partitions = maxp;
+  // tasks <= units + chunks - 1; a split unit holds >= 1 of the chunks - 1 interior chunk
+  // boundaries and has one partition more than it holds, so split partitions <= 2 * budget
   L->capacity = B * a->num_kv_heads + budget;
-  L->slots = maxp >= 2 ? budget : 0;
+  L->slots = maxp >= 2 ? 2 * budget : 0;
   size_t off = 0;
   L->status = off;
   L->ntasks = off + 4;
   off = 256;
+  const size_t units = (size_t)B * a->num_kv_heads;
   L->nparts = off;
-  off = align_up(off + 4 * (size_t)B, 256);
+  off = align_up(off + 4 * units, 256);
   L->part_base = off;
-  off = align_up(off + 4 * (size_t)B, 256);
+  off = align_up(off + 4 * units, 256);
   L->counters = off;
-  off = align_up(off + 4 * (size_t)B * a->num_kv_heads, 256);
+  off = align_up(off + 4 * units, 256);
   L->tasks = off;
   off = align_up(off + sizeof(pa::PlanTask) * (size_t)L->capacity, 256);
+  L->task_chunk = off;
+  off = align_up(off + 4 * (size_t)L->capacity, 256);
+  L->chunk_first = off;
+  off = align_up(off + 4 * ((size_t)budget + 1), 256);
   L->part_ml = off;
   off = align_up(off + 8 * (size_t)L->slots * R, 256);
   L->part_o = off;
@@ -442,6 +530,8 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   pp.part_base = reinterpret_cast<int*>(w + L.part_base);
   pp.counters = reinterpret_cast<int*>(w + L.counters);
   pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
+  pp.task_chunk = reinterpret_cast<int*>(w + L.task_chunk);
+  pp.chunk_first = reinterpret_cast<int*>(w + L.chunk_first);
   int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
   cudaLaunchConfig_t cfg = {};
@@ -463,13 +553,17 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   WsLayout L;
   if ((st = check_ws(a, ws, bytes, &L)) != PA_OK) return st;
   if (a->batch == 0) return PA_OK;
-  int sms = 0;
-  if (device_sms(&sms)) return PA_ERR_CUDA;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   const int kind = a->kv_dtype == PA_KV_BF16 ? pa::KIND_BF16 : (a->kv_dtype == PA_KV_FP8_E4M3 ? pa::KIND_FP8 : pa::KIND_FP4);
+  const bool use_tc = tc_kernel_applies(a, R);
   int tc = 0, sub = 0;
-  pa::tile_geometry(kind, a->head_dim, R, &tc, &sub);
+  if (use_tc) {
+    tc = 128;
+    sub = kind == pa::KIND_FP4 ? 64 : 128;
+  } else {
+    pa::tile_geometry(kind, a->head_dim, R, &tc, &sub);
+  }
   const int box = a->page_size < tc ? a->page_size : tc;
   CUtensorMap tk, tv;
   if ((st = cache_map(a, a->key_cache, sub, box, &tk)) != PA_OK) return st;
@@ -511,16 +605,24 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.nparts = reinterpret_cast<const int*>(w + L.nparts);
   p.part_base = reinterpret_cast<const int*>(w + L.part_base);
   p.tasks = reinterpret_cast<const pa::PlanTask*>(w + L.tasks);
+  p.chunk_first = reinterpret_cast<const int*>(w + L.chunk_first);
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_o = reinterpret_cast<float*>(w + L.part_o);
   p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
   int rc;
-  if (kind == pa::KIND_BF16)
-    rc = pa::launch_tile_bf16(p, tk, tv, L.capacity, sms, stream);
+  if (use_tc) {
+    if (kind == pa::KIND_BF16)
+      rc = pa::launch_tc_bf16(p, tk, tv, L.budget, stream);
+    else if (kind == pa::KIND_FP8)
+      rc = pa::launch_tc_fp8(p, tk, tv, L.budget, stream);
+    else
+      rc = pa::launch_tc_mxfp4(p, tk, tv, L.budget, stream);
+  } else if (kind == pa::KIND_BF16)
+    rc = pa::launch_tile_bf16(p, tk, tv, L.budget, stream);
   else if (kind == pa::KIND_FP8)
-    rc = pa::launch_tile_fp8(p, tk, tv, L.capacity, sms, stream);
+    rc = pa::launch_tile_fp8(p, tk, tv, L.budget, stream);
   else
-    rc = pa::launch_tile_mxfp4(p, tk, tv, L.capacity, sms, stream);
+    rc = pa::launch_tile_mxfp4(p, tk, tv, L.budget, stream);
   return rc == 0 ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -535,6 +637,7 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
   rp.B = a->batch;
   rp.qlen = a->qlen;
   rp.Hq = a->num_q_heads;
+  rp.Hkv = a->num_kv_heads;
   rp.G = a->num_q_heads / a->num_kv_heads;
   rp.R = rp.G * a->qlen;
   rp.D = a->head_dim;

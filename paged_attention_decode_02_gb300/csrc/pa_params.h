@@ -10,7 +10,7 @@ namespace pa {
 
 constexpr int kTileTokens = 256;  // the plan's work unit: ceil(L / 256) tiles per sequence
 
-// One task = a run of consecutive 256-token tiles of one (sequence, KV head).
+// One task = a run of consecutive 256-token tiles of one (sequence, KV head) unit.
 struct PlanTask {
   int32_t seq;
   int32_t hkv_part;  // hkv | (partition << 16)
@@ -22,16 +22,18 @@ struct PlanTask {
 struct WsLayout {
   size_t status;   // int32 device status word (PA_DEVICE_*), then ntasks
   size_t ntasks;
-  size_t nparts;     // int32 [B]: partitions of each sequence
-  size_t part_base;  // int32 [B]: first partial slot of each split sequence
-  size_t counters;   // int32 [B*Hkv]: finished tasks per split (sequence, KV head)
-  size_t tasks;      // PlanTask [capacity]
+  size_t nparts;       // int32 [B*Hkv]: partitions of each (sequence, KV head) unit
+  size_t part_base;    // int32 [B*Hkv]: first partial slot of each split unit
+  size_t counters;     // int32 [B*Hkv]: finished tasks per split unit
+  size_t tasks;        // PlanTask [capacity], in unit order (and so in chunk order)
+  size_t task_chunk;   // int32 [capacity]: the chunk (CTA) each task belongs to
+  size_t chunk_first;  // int32 [budget + 1]: first task of each chunk; [budget] = ntasks
   size_t part_ml;    // float2 [slots, R]: (max in log2 units, sum)
   size_t part_o;     // float [slots, R, D]: normalised partial outputs
   size_t total;
   int32_t capacity;  // task capacity = B*Hkv + budget
-  int32_t slots;     // partial slots = budget (split sequences only)
-  int32_t budget;
+  int32_t slots;     // partial slots = 2 * budget (split units only)
+  int32_t budget;    // chunks = tile-kernel CTAs
   int32_t max_partitions;
 };
 
@@ -53,9 +55,10 @@ struct DecodeParams {
   // workspace views
   int* status;
   const int* ntasks;
-  const int* nparts;
-  const int* part_base;
+  const int* nparts;       // per unit
+  const int* part_base;    // per unit
   const PlanTask* tasks;
+  const int* chunk_first;  // CTA b runs tasks [chunk_first[b], chunk_first[b + 1])
   float* part_ml;
   float* part_o;
   int* counters;  // non-null: merge split sequences at the end of the tile kernel
@@ -72,10 +75,12 @@ struct PlanParams {
   int* part_base;
   int* counters;
   PlanTask* tasks;
+  int* task_chunk;
+  int* chunk_first;
 };
 
 struct ReduceParams {
-  int B, qlen, Hq, G, R, D;
+  int B, qlen, Hq, Hkv, G, R, D;
   const int* nparts;
   const int* part_base;
   const float* part_ml;
@@ -84,14 +89,23 @@ struct ReduceParams {
   int64_t o_st, o_sh;
 };
 
-// Kernel launchers, one per KV format (defined in the per-format translation units).
-// Each returns a cudaError_t value (0 = success).
+// Kernel launchers, one per KV format (defined in the per-format translation units):
+// `grid` CTAs, one per plan chunk.  Each returns a cudaError_t value (0 = success).
 int launch_tile_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                     int grid_cap, int num_sms, void* stream);
+                     int grid, void* stream);
 int launch_tile_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                    int grid_cap, int num_sms, void* stream);
+                    int grid, void* stream);
 int launch_tile_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                      int grid_cap, int num_sms, void* stream);
+                      int grid, void* stream);
+
+// Tensor-core (tcgen05) kernel launchers, head_dim 128, up to 32 query rows per KV
+// head; the K / V tensor maps have boxes of min(page size, 128) rows.
+int launch_tc_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                   int grid, void* stream);
+int launch_tc_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                  int grid, void* stream);
+int launch_tc_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                    int grid, void* stream);
 
 // Tokens per warp slice and swizzle span (bytes) of the tile kernel chosen for a
 // format / head_dim / query-row count; the TMA box is min(S, slice tokens) rows high.

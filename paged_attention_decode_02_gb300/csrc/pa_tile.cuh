@@ -1,18 +1,18 @@
 // pa_tile.cuh -- the sm_103a paged-attention decode tile kernel.
 //
-// One persistent CTA walks planned tasks (runs of 256-token tiles of one sequence
-// and KV head).  Every warp owns a token slice of each CTA stage and runs its own
-// pipeline: it gathers its slice's pages through the block table with TMA (K and V
-// land 128- or 64-byte swizzled; per-token or e8m0 scales arrive by 1-D bulk copy)
-// into a private ring of mbarrier-guarded slots, NSTAGE slices ahead of the one it
-// computes, so no warp ever waits for another inside a task.  Softmax state and the
-// output accumulators are warp-private; QK^T and PV run on mma.sync (m16n8k16, fp32
-// accumulate) with fp8 / fp4 operands widened to f16 in registers.  Only a slice
-// holding tokens at or past the context length runs the masked path: scores there
-// become -inf, and V values and per-token scales become 0 by select, so unowned rows
-// never reach the output whatever bytes they hold ("[FlyDSL] pa_decode: zero V rows
-// past the context before PV", Fix).  At the end of a task the warps merge their
-// (max, sum, output) in a fixed order and store either the final bf16 row (sequences
+// Each CTA walks the tasks of its plan chunk (runs of 256-token tiles of one sequence
+// and KV head; a chunk is an equal share of all tiles).  Every warp owns a token slice
+// of each CTA stage and runs its own pipeline: it gathers its slice's pages through the
+// block table with TMA (K and V land 128- or 64-byte swizzled; per-token or e8m0 scales
+// arrive by 1-D bulk copy) into a private ring of mbarrier-guarded slots, NSTAGE slices
+// ahead of the one it computes, so no warp ever waits for another inside a task.
+// Softmax state and the output accumulators are warp-private; QK^T and PV run on
+// mma.sync (m16n8k16, fp32 accumulate) with fp8 / fp4 operands widened to f16 in
+// registers.  Only a slice holding tokens at or past the context length runs the masked
+// path: scores there become -inf, and V values and per-token scales become 0 by select,
+// so unowned rows never reach the output whatever bytes they hold ("[FlyDSL] pa_decode:
+// zero V rows past the context before PV", Fix).  At the end of a task the warps merge
+// their (max, sum, output) in a fixed order and store either the final bf16 row (units
 // with one partition) or a partial for the reduce kernel ("[FlyDSL] pa_decode: MXFP4
 // K/V ...", direct output commit).
 #pragma once
@@ -210,7 +210,8 @@ __device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int
   }
 }
 
-// Where a warp's loads stand: the next (task, slice) it will load.  The warp walks the
+// Where a warp's loads stand: the next (task, slice) it will load (tasks of this CTA's
+// chunk, in order).  The warp walks the
 // same sequence of slices for loading and for computing, the loads NSTAGE ahead.  The
 // block-table entries of the next slice are fetched one slice early (blk, one per box,
 // held by lanes 0..nbox-1) so that no refill waits on a dependent global load.
@@ -235,11 +236,10 @@ __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p)
 // Advance to the first slice at or after the current one that holds tokens, and start
 // the block-table loads of its boxes.
 template <class C>
-__device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, int ntasks, int r0,
+__device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, int t_end, int r0,
                                           int lane, int box_shift, int page_shift) {
   while (!it.done && it.c0 + r0 >= it.t1) {
-    it.task += gridDim.x;
-    if (it.task >= ntasks) {
+    if (++it.task >= t_end) {
       it.done = true;
       return;
     }
@@ -699,8 +699,8 @@ __device__ __forceinline__ void stage_compute(
 
 template <class C>
 __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                          uint8_t* smem, uint64_t* full, volatile int* abort_flag, int ntasks,
-                          int cw, int lane) {
+                          uint8_t* smem, uint64_t* full, volatile int* abort_flag, int t_begin,
+                          int t_end, int cw, int lane) {
   const int tg = cw / C::NDW, dw = cw % C::NDW;
   const int g = lane >> 2, t = lane & 3;
   const int r0 = tg * C::TW;  // this warp's slice inside a CTA stage
@@ -744,11 +744,11 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
 
   // prologue: fill the ring
   SliceIt ld;
-  ld.task = blockIdx.x;
-  ld.done = ld.task >= ntasks;
+  ld.task = t_begin;
+  ld.done = ld.task >= t_end;
   ld.blk = 0;
   if (!ld.done) it_load_task(ld, p);
-  it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
+  it_settle<C>(ld, p, t_end, r0, lane, box_shift, page_shift);
   uint32_t issued = 0, consumed = 0;
   int lslot = 0;  // ring slot of the next load
   while (!ld.done && issued < (uint32_t)C::NSTAGE) {
@@ -757,20 +757,21 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     ++issued;
     lslot = lslot + 1 == C::NSTAGE ? 0 : lslot + 1;
     ld.c0 += C::TC;
-    it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
+    it_settle<C>(ld, p, t_end, r0, lane, box_shift, page_shift);
   }
   int cslot = 0;      // ring slot of the next compute
   uint32_t cpar = 0;  // its phase parity
   int xbuf = 0;
 
-  for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
+  for (int task = t_begin; task < t_end; ++task) {
     const PlanTask tk = p.tasks[task];
     const int s = tk.seq, hkv = tk.hkv_part & 0xFFFF, part = tk.hkv_part >> 16;
     const int L = clamped_context(p, s);
     const int t0 = tk.tile_begin * kTileTokens;
     int t1 = tk.tile_end * kTileTokens;
     t1 = t1 < L ? t1 : L;
-    const int nparts = p.nparts[s];
+    const int unit = s * p.Hkv + hkv;
+    const int nparts = p.nparts[unit];
 
     load_q<C>(p, smem, s, hkv, cw, lane, k_scale_tensor);
     named_bar(BAR_CONSUMERS, C::NCW * 32);
@@ -834,7 +835,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         ++issued;
         lslot = lslot + 1 == C::NSTAGE ? 0 : lslot + 1;
         ld.c0 += C::TC;
-        it_settle<C>(ld, p, ntasks, r0, lane, box_shift, page_shift);
+        it_settle<C>(ld, p, t_end, r0, lane, box_shift, page_shift);
       }
     }
 
@@ -906,7 +907,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       named_bar(BAR_CONSUMERS, C::NCW * 32);
     }
     if (tg == C::NTG - 1) {
-      const int64_t slot = nparts > 1 ? (int64_t)p.part_base[s] + (int64_t)hkv * nparts + part : 0;
+      const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
         float inv[2];
@@ -951,11 +952,11 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       volatile int* mflag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG) + 1;
       __threadfence();  // this task's partials are visible before it is counted
       named_bar(BAR_CONSUMERS, C::NCW * 32);
-      if (threadIdx.x == 0) *mflag = atomicAdd(p.counters + (int64_t)s * p.Hkv + hkv, 1) == nparts - 1;
+      if (threadIdx.x == 0) *mflag = atomicAdd(p.counters + unit, 1) == nparts - 1;
       named_bar(BAR_CONSUMERS, C::NCW * 32);
       if (*mflag) {
         __threadfence();
-        const int64_t base = (int64_t)p.part_base[s] + (int64_t)hkv * nparts;
+        const int64_t base = p.part_base[unit];
         const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
         float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= D)
         // one warp per row: lanes over partitions, shuffle-tree max and sum
@@ -1044,22 +1045,21 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
   __syncthreads();
   pdl_launch_dependents();  // the reduce kernel may launch; it waits for this grid's results
   pdl_wait_prior();         // the plan's task list is complete and visible from here on
-  const int ntasks = *p.ntasks;
-  warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, ntasks, threadIdx.x >> 5, threadIdx.x & 31);
+  const int t_begin = p.chunk_first[blockIdx.x], t_end = p.chunk_first[blockIdx.x + 1];
+  warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, t_begin, t_end, threadIdx.x >> 5,
+               threadIdx.x & 31);
 }
 
-// Launch helper: persistent grid of min(task capacity, MINB x SMs) CTAs.
+// Launch helper: one CTA per plan chunk.
 template <class C>
-int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid_cap,
-                int num_sms, void* stream) {
+int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                void* stream) {
   static bool attr_done = false;  // per process; the attribute is per function
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(pa_tile_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return (int)e;
     attr_done = true;
   }
-  int grid = num_sms * C::MINB;
-  if (grid > grid_cap) grid = grid_cap;
   if (grid < 1) grid = 1;
   // Programmatic serialisation: this grid launches while the plan kernel runs and waits
   // for it (griddepcontrol.wait) before reading the task list.

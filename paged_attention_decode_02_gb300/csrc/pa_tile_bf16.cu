@@ -4,12 +4,12 @@
 namespace pa {
 
 int launch_tile_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                     int grid_cap, int num_sms, void* stream) {
+                     int grid, void* stream) {
   if (p.D == 128)
-    return p.R <= 16 ? launch_tile<CfgBf16D128M1>(p, tk, tv, grid_cap, num_sms, stream)
-                     : launch_tile<CfgBf16D128M2>(p, tk, tv, grid_cap, num_sms, stream);
-  return p.R <= 16 ? launch_tile<CfgBf16D256M1>(p, tk, tv, grid_cap, num_sms, stream)
-                   : launch_tile<CfgBf16D256M2>(p, tk, tv, grid_cap, num_sms, stream);
+    return p.R <= 16 ? launch_tile<CfgBf16D128M1>(p, tk, tv, grid, stream)
+                     : launch_tile<CfgBf16D128M2>(p, tk, tv, grid, stream);
+  return p.R <= 16 ? launch_tile<CfgBf16D256M1>(p, tk, tv, grid, stream)
+                   : launch_tile<CfgBf16D256M2>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pa

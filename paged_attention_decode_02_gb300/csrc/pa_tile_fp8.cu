@@ -5,18 +5,18 @@ namespace pa {
 
 template <int SKT>
 static int launch_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                      int grid_cap, int num_sms, void* stream) {
+                      int grid, void* stream) {
   if (p.D == 128)
-    return p.R <= 16 ? launch_tile<CfgFp8D128M1<SKT>>(p, tk, tv, grid_cap, num_sms, stream)
-                     : launch_tile<CfgFp8D128M2<SKT>>(p, tk, tv, grid_cap, num_sms, stream);
-  return p.R <= 16 ? launch_tile<CfgFp8D256M1<SKT>>(p, tk, tv, grid_cap, num_sms, stream)
-                   : launch_tile<CfgFp8D256M2<SKT>>(p, tk, tv, grid_cap, num_sms, stream);
+    return p.R <= 16 ? launch_tile<CfgFp8D128M1<SKT>>(p, tk, tv, grid, stream)
+                     : launch_tile<CfgFp8D128M2<SKT>>(p, tk, tv, grid, stream);
+  return p.R <= 16 ? launch_tile<CfgFp8D256M1<SKT>>(p, tk, tv, grid, stream)
+                   : launch_tile<CfgFp8D256M2<SKT>>(p, tk, tv, grid, stream);
 }
 
 int launch_tile_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                    int grid_cap, int num_sms, void* stream) {
-  return p.scale_kind == SK_TOKEN ? launch_fp8<SK_TOKEN>(p, tk, tv, grid_cap, num_sms, stream)
-                                  : launch_fp8<SK_TENSOR>(p, tk, tv, grid_cap, num_sms, stream);
+                    int grid, void* stream) {
+  return p.scale_kind == SK_TOKEN ? launch_fp8<SK_TOKEN>(p, tk, tv, grid, stream)
+                                  : launch_fp8<SK_TENSOR>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pa

@@ -4,8 +4,8 @@
 namespace pa {
 
 int launch_tile_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
-                      int grid_cap, int num_sms, void* stream) {
-  return launch_tile<CfgFp4D128M1>(p, tk, tv, grid_cap, num_sms, stream);
+                      int grid, void* stream) {
+  return launch_tile<CfgFp4D128M1>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pa

@@ -51,6 +51,10 @@ class Case:
     e8m0_range: tuple = (120, 130)
     pad_columns: int = 2
     extra_blocks: int = 0
+    # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and
+    # V rows, fp8 per-token scales, MXFP4 e8m0 exponents (rounded) -- so that later tokens
+    # keep raising the running max and the V references
+    ramp: float = 0.0
 
     @property
     def gqa(self) -> int:
@@ -168,6 +172,16 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
             tail = L - (n - 1) * S
             owned[int(blks[-1]), :tail] = True
     own4 = owned[:, None, :].expand(NB, Hkv, S)
+    frac = torch.zeros((NB, S), dtype=torch.float32)  # position / length of owned rows
+    if case.ramp > 0:
+        pos = 0
+        for s in range(B):
+            n, L = pages[s], int(lens[s])
+            if n:
+                blks = bt[s, :n].long()
+                p_ = torch.arange(n * S, dtype=torch.float32).reshape(n, S) / max(L, 1)
+                frac[blks] = p_
+                pos += n
 
     # query
     Hq, qlen = case.num_q_heads, case.qlen
@@ -207,6 +221,21 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
                                   dtype=torch.int32).to(torch.uint8)
         value_scale = torch.randint(lo, hi + 1, (NB, Hkv, S, D // 32), generator=g,
                                     dtype=torch.int32).to(torch.uint8)
+
+    if case.ramp > 0:
+        f = (case.ramp * frac)[:, None, :].expand(NB, Hkv, S)  # log2 growth per row
+        if case.kv == KV_BF16:
+            g2 = torch.exp2(f)[..., None]
+            kc = (kc.float() * g2).to(torch.bfloat16)
+            vc = (vc.float() * g2).to(torch.bfloat16)
+            caches = [kc.view(torch.int16), vc.view(torch.int16)]
+        elif case.kv == KV_FP8 and case.scale == SCALE_TOKEN:
+            key_scale = key_scale * torch.exp2(f)
+            value_scale = value_scale * torch.exp2(f)
+        elif case.kv == KV_MXFP4:
+            add = torch.round(f).to(torch.int32)[..., None]
+            key_scale = (key_scale.to(torch.int32) + add).clamp(0, 254).to(torch.uint8)
+            value_scale = (value_scale.to(torch.int32) + add).clamp(0, 254).to(torch.uint8)
 
     # fill every row that no sequence owns
     unowned = ~own4

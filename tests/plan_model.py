@@ -1,0 +1,94 @@
+"""The work split that pa_decode_plan builds, restated on the host for tests.
+
+Units are (sequence, KV head) pairs in sequence-major order, each with ceil(L/256)
+tiles.  All units' tiles, laid end to end, are cut into `budget` chunks of C tiles
+(C = ceil(total / budget), raised when needed so that no unit touches more than
+max_partitions chunks); a unit becomes one partition per chunk it touches.  With
+max_partitions 1, or an empty unit, the unit is one task in the chunk it starts in.
+
+The workspace layout mirrors the library's (256-byte aligned regions): status word and
+task count, then nparts, part_base, counters (int32 per unit), tasks (4 x int32 per
+task, `capacity` of them), task_chunk (int32 per task), chunk_first (int32, budget + 1).
+"""
+import math
+
+import numpy as np
+
+TILE = 256
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def plan(context_lens, hkv, budget, max_partitions, cap_tokens):
+    tiles = [(min(max(int(L), 0), cap_tokens) + TILE - 1) // TILE for L in context_lens]
+    total = sum(tiles) * hkv
+    maxt = max(tiles, default=0)
+    C = max(1, -(-total // budget))
+    if max_partitions >= 2 and maxt > 0:
+        C = max(C, (maxt - 1) // (max_partitions - 1) + 1)
+    nchunks = -(-total // C) if total > 0 else 1
+    tasks, chunks, nparts, part_base = [], [], [], []
+    U, slot = 0, 0
+    for s, n in enumerate(tiles):
+        for h in range(hkv):
+            if n == 0 or max_partitions < 2:
+                pieces = [(0, n, min(U // C, nchunks - 1))]
+            else:
+                pieces = [(max(U, c * C) - U, min(U + n, (c + 1) * C) - U, c)
+                          for c in range(U // C, (U + n - 1) // C + 1)]
+            nparts.append(len(pieces))
+            part_base.append(slot if len(pieces) >= 2 else 0)
+            if len(pieces) >= 2:
+                slot += len(pieces)
+            for q, (b, e, c) in enumerate(pieces):
+                tasks.append((s, h | (q << 16), b, e))
+                chunks.append(c)
+            U += n
+    first = [len(tasks)] * (budget + 1)
+    prev = -1
+    for t, c in enumerate(chunks):
+        for k in range(prev + 1, c + 1):
+            first[k] = t
+        prev = c
+    return {"tiles": tiles, "C": C, "nchunks": nchunks, "tasks": tasks, "chunks": chunks,
+            "nparts": nparts, "part_base": part_base, "chunk_first": first, "slots": slot}
+
+
+def capacity(batch, hkv, budget):
+    return batch * hkv + budget
+
+
+def read_workspace(ws: np.ndarray, batch, hkv, budget):
+    """Decode the plan regions of a workspace (uint8 array, host copy)."""
+    units = batch * hkv
+    cap = capacity(batch, hkv, budget)
+    i32 = lambda off, n: ws[off:off + 4 * n].view(np.int32).copy()
+    off = 256
+    nparts = i32(off, units)
+    off = _align(off + 4 * units)
+    part_base = i32(off, units)
+    off = _align(off + 4 * units)
+    off = _align(off + 4 * units)  # counters
+    ntasks = int(i32(4, 1)[0])
+    tasks = i32(off, 4 * cap).reshape(cap, 4)[:ntasks]
+    off = _align(off + 16 * cap)
+    chunks = i32(off, cap)[:ntasks]
+    off = _align(off + 4 * cap)
+    first = i32(off, budget + 1)
+    return {"ntasks": ntasks, "tasks": [tuple(int(x) for x in t) for t in tasks],
+            "chunks": chunks.tolist(), "nparts": nparts.tolist(),
+            "part_base": part_base.tolist(), "chunk_first": first.tolist()}
+
+
+def chunk_tiles(model):
+    """Tiles each chunk runs."""
+    out = np.zeros(len(model["chunk_first"]) - 1, dtype=np.int64)
+    for (s, hp, b, e), c in zip(model["tasks"], model["chunks"]):
+        out[c] += e - b
+    return out
+
+
+def ceil_div(a, b):
+    return math.ceil(a / b)

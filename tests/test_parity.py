@@ -57,6 +57,45 @@ def test_small_cases_match_oracle(case, mode):
     util.assert_parity(got, ref, case.kv, case.name)
 
 
+RAMP = [
+    synth.replace(synth.config1(context_lens=[3000, 700], seed=2301), ramp=14.0),
+    synth.replace(synth.config5(synth.KV_FP8, batch=3, context_lens=(3000, 9000), seed=2302), ramp=14.0),
+    synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2303), ramp=14.0),
+    synth.replace(synth.config4(batch=6, seed=2304), ramp=10.0),
+]
+
+
+@pytest.mark.parametrize("case", RAMP, ids=lambda c: f"{c.name}-ramp")
+@pytest.mark.parametrize("mode", ["split", "direct"])
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_rising_magnitudes_match_oracle(case, mode, kernel, monkeypatch):
+    # scores and V scales keep growing along each sequence: the running max and the V
+    # references rise again and again, and every rise rescales the accumulated output
+    monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
+    p = synth.make(case)
+    ref = util.oracle_decode(p)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16)
+    util.assert_parity(got, ref, case.kv, f"{case.name} {kernel}")
+
+
+TC_CASES = [c for c in SMALL if c.head_dim == 128] + [
+    synth.config3(qlen=1, batch=4, head_dim=128, context_lens=(200, 1500), seed=2401),
+    synth.config3(qlen=2, batch=3, head_dim=128, context_lens=(200, 900), seed=2402),
+    synth.config2("b", batch=5, head_dim=128, seed=2403),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"{c.name}-q{c.qlen}-s{c.seed}")
+@pytest.mark.parametrize("mode", ["split", "direct"])
+def test_tensor_core_kernel_matches_oracle(case, mode, monkeypatch):
+    # the tcgen05 kernel (PA_DECODE_KERNEL=tc) on every head_dim-128 shape: bf16, fp8 per
+    # tensor and per token, MXFP4; 8 to 32 query rows per KV head; pages of 16 to 128
+    monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+    p = synth.make(case)
+    util.assert_parity(run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=64),
+                       util.oracle_decode(p), case.kv, case.name + " tcgen05")
+
+
 @pytest.mark.parametrize("lens", [[0, 0], [1, 2], [255, 256, 257], [511, 512, 513, 767]])
 def test_ragged_edges(lens):
     case = synth.Case("edges", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=len(lens),

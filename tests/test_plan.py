@@ -1,0 +1,108 @@
+"""The work split: the arithmetic of the chunked plan on the host (CPU), and the device
+plan kernel against it task for task (GPU).
+
+The plan's job ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit messages: planned tasks,
+tasks from a CU budget, direct output with one partition): every tile of every
+(sequence, KV head) unit runs exactly once, in order, each CTA gets an equal share of
+tiles, no unit has more than max_partitions partitions, and the task and partial-slot
+counts stay within the workspace the host sized.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import plan_model as pm
+
+MIXES = [
+    ("long16", [int(x) for x in np.random.default_rng(5).integers(120000, 131073, 16)], 1),
+    ("ragged", [0, 1, 255, 256, 257, 4000, 0, 70000, 3, 131072], 2),
+    ("uniform4096", [2048] * 4096, 1),
+    ("one", [500000], 1),
+    ("empty", [0, 0, 0], 4),
+    ("mixed", [int(x) for x in np.random.default_rng(9).integers(1, 9000, 37)], 2),
+]
+BUDGETS = [1, 7, 152, 304]
+MAXP = [1, 2, 3, 128]
+
+
+@pytest.mark.parametrize("name,lens,hkv", MIXES, ids=[m[0] for m in MIXES])
+@pytest.mark.parametrize("budget", BUDGETS)
+@pytest.mark.parametrize("maxp", MAXP)
+def test_plan_arithmetic(name, lens, hkv, budget, maxp):
+    cap = 1 << 20
+    m = pm.plan(lens, hkv, budget, maxp, cap)
+    tiles = m["tiles"]
+    # every tile of every unit exactly once, partitions in order and contiguous
+    by_unit = {}
+    for (s, hp, b, e) in m["tasks"]:
+        by_unit.setdefault((s, hp & 0xFFFF), []).append((hp >> 16, b, e))
+    assert len(by_unit) == len(lens) * hkv
+    for (s, h), parts in by_unit.items():
+        assert [q for q, _, _ in parts] == list(range(len(parts)))
+        assert parts[0][1] == 0 and parts[-1][2] == tiles[s]
+        for (_, _, e0), (_, b1, _) in zip(parts, parts[1:]):
+            assert e0 == b1
+        assert all(e > b for _, b, e in parts) or tiles[s] == 0
+        assert len(parts) <= max(1, maxp)
+        assert m["nparts"][s * hkv + h] == len(parts)
+    # sizes the host reserved
+    assert len(m["tasks"]) <= pm.capacity(len(lens), hkv, budget)
+    assert maxp < 2 or m["slots"] <= 2 * budget
+    # chunks: non-decreasing over the task list, each CTA's range is its chunk
+    assert all(a <= b for a, b in zip(m["chunks"], m["chunks"][1:]))
+    first = m["chunk_first"]
+    assert first[-1] == len(m["tasks"]) and all(a <= b for a, b in zip(first, first[1:]))
+    for c in range(budget):
+        assert all(m["chunks"][t] == c for t in range(first[c], first[c + 1]))
+    # balance: with splitting on, no chunk runs more than C tiles and all but the last
+    # non-empty chunk run exactly C
+    if maxp >= 2:
+        per = pm.chunk_tiles(m)
+        assert per.max(initial=0) <= m["C"]
+        assert m["nchunks"] <= budget
+        full = per[: m["nchunks"] - 1]
+        assert np.all(full == m["C"])
+        if sum(tiles) > 0:
+            assert m["C"] == max(pm.ceil_div(sum(tiles) * hkv, budget),
+                                 (max(tiles) - 1) // (maxp - 1) + 1)
+
+
+def test_plan_balance_long_context():
+    # 16 long sequences over 152 CTAs: the busiest CTA runs at most one tile more than
+    # the mean (the proportional split it replaces left ~10% of the GPU idle)
+    lens = MIXES[0][1]
+    m = pm.plan(lens, 1, 152, 128, 1 << 20)
+    per = pm.chunk_tiles(m)
+    assert per.max() - per.sum() / 152 <= 1.0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,lens,hkv", MIXES, ids=[m[0] for m in MIXES])
+@pytest.mark.parametrize("budget,maxp", [(152, 128), (7, 3), (304, 1), (1, 2)])
+def test_device_plan_matches_model(name, lens, hkv, budget, maxp):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_attention_decode_02_gb300 import build, ops
+    build.build()
+    ops.load_library()
+    B = len(lens)
+    S, W, D = 128, max(1, (max(lens) + 127) // 128), 128
+    dev = "cuda"
+    q = torch.zeros(B, 1, 8 * hkv, D, dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros(2, hkv, S, D, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(B, W, dtype=torch.int32, device=dev)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    args = ops.make_args(q, kc, kc, bt, ctx, out, max_partitions=maxp, task_budget=budget)
+    ws = ops.alloc_workspace(args)
+    ops.pa_decode_plan(args, ws)
+    torch.cuda.synchronize()
+    got = pm.read_workspace(ws.cpu().numpy(), B, hkv, budget)
+    m = pm.plan(lens, hkv, budget, maxp, W * S)
+    assert got["ntasks"] == len(m["tasks"])
+    assert got["tasks"] == m["tasks"]
+    assert got["chunks"] == m["chunks"]
+    assert got["chunk_first"] == m["chunk_first"]
+    assert got["nparts"] == m["nparts"]
+    split = [i for i, p in enumerate(m["nparts"]) if p >= 2]
+    assert [got["part_base"][i] for i in split] == [m["part_base"][i] for i in split]

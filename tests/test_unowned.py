@@ -57,8 +57,12 @@ def _cases():
 
 
 @pytest.mark.parametrize("case", _cases(), ids=lambda c: c.name)
-@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
-def test_unowned_fill_is_bit_identical(case, mode):
+@pytest.mark.parametrize("mode", ["split", "direct", "fused", "split-tc", "direct-tc"])
+def test_unowned_fill_is_bit_identical(case, mode, monkeypatch):
+    # "-tc": the tcgen05 kernel (head_dim 128 shapes; others fall back to mma.sync)
+    if mode.endswith("-tc"):
+        monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+        mode = mode[:-3]
     kw = dict(max_partitions=1 if mode == "direct" else 0, task_budget=16,
               merge_in_decode=mode == "fused")
     p = synth.make(case)
