@@ -8,10 +8,12 @@
 //   warp 1      owns the tensor memory, converts each task's query rows into the MMA's
 //               B operand, and issues every tcgen05.mma:  S^T = K Q^T (tokens on the
 //               M dimension) and O^T += V^T P^T (head dims on the M dimension);
-//   warps 2-17  the consumer group.  Four threads own each token of S (each a quarter of
-//               the query rows) for the softmax, and every thread widens a share of the
-//               tile's V (and MXFP4 K) to f16 in double-buffered shared memory, so the
-//               tensor cores run tile k's PV and tile k+1's QK while tile k+1 is widened.
+//   warps 2-9   the softmax group: two threads own each token of S (each half the query
+//               rows); they keep the running max and sums, rescale O in TMEM when the
+//               max rises, and write P;
+//   warps 10-17 the widening group: V (and MXFP4 K) to f16 in double-buffered shared
+//               memory, running ahead of the softmax group, so that tile k+1 is widened
+//               while tile k's softmax runs and the tensor cores run its PV.
 // Scores of tokens at or past the context length become -inf and their V rows are
 // written as zeros (or zeroed in place for bf16), so unowned rows never reach the output
 // ("[FlyDSL] pa_decode: zero V rows past the context before PV", Fix).  fp8 K feeds the
@@ -33,10 +35,11 @@ template <int KIND_, int SKT_, int RPAD_, int NS_>
 struct TcCfg {
   static constexpr int KIND = KIND_, SKT = SKT_, RPAD = RPAD_, NS = NS_;
   static constexpr int D = 128, TT = 128;
-  static constexpr int NCW = 16;                 // consumer warps: four per TMEM lane quarter
+  static constexpr int NSW = 8;                  // softmax warps: two per TMEM lane quarter
+  static constexpr int NWW = 8;                  // widening warps
+  static constexpr int NCW = NSW + NWW;
   static constexpr int NTHREADS = 64 + 32 * NCW;
-  static constexpr int NQ = NCW / 4;             // consumer threads per token
-  static constexpr int RH = RPAD / NQ;           // query rows per consumer thread
+  static constexpr int RH = RPAD / 2;            // query rows per softmax thread
   static constexpr bool TOK = SKT == SK_TOKEN;
   static constexpr bool SCALES = SKT == SK_TOKEN || SKT == SK_E8M0;
   static constexpr bool QK_F8 = KIND == KIND_FP8;  // e4m3 K as stored, query split hi + lo
@@ -56,26 +59,32 @@ struct TcCfg {
   static constexpr int KF_BYTES = KDQ ? TT * 256 : 0;
   static constexpr int BUF_BYTES = P_BYTES + VF_BYTES + KF_BYTES;  // one of two tile buffers
   static constexpr int RED_W = 2 * RH + 10;                         // exchange words per warp
+  static constexpr int VINFO_W = 8;  // per tile buffer: MXFP4 V exponent drops [4], references [4]
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_Q = OFF_RING + NS * SLOT;
   static constexpr int OFF_BUF = OFF_Q + NQB * Q_BYTES;
   static constexpr int OFF_QC = OFF_BUF + 2 * BUF_BYTES;
   static constexpr int OFF_RED = OFF_QC + NQB * RPAD * 4;
-  static constexpr int OFF_BAR = (OFF_RED + NCW * RED_W * 4 + 7) / 8 * 8;
+  static constexpr int OFF_VINFO = OFF_RED + NCW * RED_W * 4;
+  static constexpr int OFF_BAR = (OFF_VINFO + 2 * VINFO_W * 4 + 7) / 8 * 8;
   static constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = NS, B_S_FULL = 2 * NS;
-  static constexpr int B_KF_FULL = B_S_FULL + SBUF, B_PV_READY = B_KF_FULL + 2;
-  static constexpr int B_PV_DONE = B_PV_READY + 2, B_GS = B_PV_DONE + 2;
-  static constexpr int B_MMA_DONE = B_GS + 1, NBAR = B_MMA_DONE + 1;
+  static constexpr int B_KF_FULL = B_S_FULL + SBUF, B_VINFO = B_KF_FULL + 2;
+  static constexpr int B_PV_READY = B_VINFO + 2, B_PV_DONE = B_PV_READY + 2;
+  static constexpr int B_SYNC_S = B_PV_DONE + 2, B_SYNC_W = B_SYNC_S + 1;
+  static constexpr int B_MMA_DONE = B_SYNC_W + 1, NBAR = B_MMA_DONE + 1;
   static constexpr int RAW_EMPTY_COUNT = NCW + (KIND == KIND_FP4 ? 0 : 1);
-  // arrival count of barrier i: TMA / MMA-commit signals 1, consumer signals one per warp,
-  // a raw stage one per consumer warp (+ 1 commit when the tensor cores read the stage)
+  // arrival count of barrier i: TMA / MMA-commit signals 1, a group signals one per warp
+  // (widening group NWW, softmax group NSW, both NCW), a raw stage one per consumer warp
+  // (+ 1 commit when the tensor cores read the stage)
   static constexpr uint32_t bar_count(int i) {
     return i < B_RAW_EMPTY  ? 1u
            : i < B_S_FULL   ? (uint32_t)RAW_EMPTY_COUNT
            : i < B_KF_FULL  ? 1u
+           : i < B_PV_READY ? (uint32_t)NWW
            : i < B_PV_DONE  ? (uint32_t)NCW
-           : i < B_GS       ? 1u
-           : i < B_MMA_DONE ? (uint32_t)NCW
+           : i < B_SYNC_S   ? 1u
+           : i < B_SYNC_W   ? (uint32_t)NSW
+           : i < B_MMA_DONE ? (uint32_t)NWW
                             : 1u;
   }
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -463,15 +472,16 @@ __device__ __forceinline__ bool grp_sync(uint64_t* bar, uint32_t& phase, volatil
 }
 
 // MXFP4 K or V tile (64-byte rows, 64-byte swizzle) to f16 [2 dim atoms][128][128 B]:
-// consumer thread `ci` (0..511) widens 32-value block (ci & 3) of token ci / 4,
+// widening thread `ci` (0..255) widens 32-value block (ci & 3) of tokens ci / 4 + 64 j,
 // times 2^(e - ref) (K: ref = the token's largest block exponent; V: the running
 // reference of block ci & 3).  Rows past the context become zeros.
 template <class C, bool ISK>
 __device__ __forceinline__ void tc_widen_fp4(const uint8_t* raw, const uint8_t* sc, uint8_t* dst, int ci,
                                              int c0, int L, int vref_b) {
   const int b = ci & 3;
-  {
-    const int tok = ci >> 2;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int tok = (ci >> 2) + 64 * j;
     const uint4 v = *reinterpret_cast<const uint4*>(raw + tok * 64 + ((b ^ ((tok >> 1) & 3)) << 4));
     const uint32_t sw = *reinterpret_cast<const uint32_t*>(sc + tok * 4);
     const int e = (int)((sw >> (8 * b)) & 0xFF);
@@ -502,14 +512,14 @@ __device__ __forceinline__ void tc_widen_fp4(const uint8_t* raw, const uint8_t* 
   }
 }
 
-// fp8 V tile (128-byte rows, 128-byte swizzle) to f16: consumer thread `ci` (0..511)
-// widens dims 16 (ci & 7) .. +15 of tokens ci / 8 + 64 j.
+// fp8 V tile (128-byte rows, 128-byte swizzle) to f16: widening thread `ci` (0..255)
+// widens dims 16 (ci & 7) .. +15 of tokens ci / 8 + 32 j.
 template <class C>
 __device__ __forceinline__ void tc_widen_fp8(const uint8_t* raw, uint8_t* dst, int ci, int c0, int L) {
   const int qd = ci & 7;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int tok = (ci >> 3) + 64 * j;
+  for (int j = 0; j < 4; ++j) {
+    const int tok = (ci >> 3) + 32 * j;
     const uint4 v = *reinterpret_cast<const uint4*>(raw + tok * 128 + ((qd ^ (tok & 7)) << 4));
     uint32_t h[8];
     e4m3x4_to_f16x2(v.x, h[0], h[1]);
@@ -525,15 +535,12 @@ __device__ __forceinline__ void tc_widen_fp8(const uint8_t* raw, uint8_t* dst, i
   }
 }
 
-// RH consecutive 32-bit TMEM columns of this thread's lane (RH = 4 or 8).
+// RH consecutive 32-bit TMEM columns of this thread's lane (RH = 8 or 16).
 template <class C>
 __device__ __forceinline__ void tc_ld_half(uint32_t taddr, float (&v)[C::RH]) {
   uint32_t r[16];
-  if constexpr (C::RH == 4) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr)
-                 : "memory");
+  if constexpr (C::RH == 16) {
+    tmem_ld16(taddr, r);
   } else {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
@@ -550,10 +557,8 @@ __device__ __forceinline__ void tc_st_half(uint32_t taddr, const float (&v)[C::R
   uint32_t r[16];
 #pragma unroll
   for (int j = 0; j < C::RH; ++j) r[j] = __float_as_uint(v[j]);
-  if constexpr (C::RH == 4) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
+  if constexpr (C::RH == 16) {
+    tmem_st16(taddr, r);
   } else {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -562,40 +567,39 @@ __device__ __forceinline__ void tc_st_half(uint32_t taddr, const float (&v)[C::R
   tmem_wait_st();
 }
 
-// Slots of a warp's row in the group exchange area (after RH row words).
-constexpr int RX_MFLAG = 0;  // raise flags after the scores
-constexpr int RX_VMAX = 1;   // |v scale| maximum (fp8 per-token)
-constexpr int RX_EMAX = 1;   // .. + 4: V exponent maxima per block (MXFP4)
-constexpr int RX_VFLAG = 5;  // V reference flags before the widening (MXFP4)
+// Exchange area: a row of RED_W words per consumer warp.  Softmax warps: [0, RH) row
+// maxima, [RH, 2 RH) row sums, then raise flags by tile parity [2] and the |v scale|
+// maximum.  Widening warps: V reference flags by tile parity [2], then exponent maxima [4].
+constexpr int XS_M = 0, XS_VMAX = 2;
+constexpr int XW_V = 0, XW_EMAX = 2;
 
+// Softmax group (warps 2-9): scores, lazy max, P, O rescale and the epilogue.
 template <class C>
-__device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volatile int* abort_flag,
-                            uint32_t tmem, int tb, int te, int wi, int lane) {
+__device__ void tc_softmax(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volatile int* abort_flag,
+                           uint32_t tmem, int tb, int te, int wi, int lane) {
   constexpr int R = C::RPAD, RH = C::RH, RW = C::RED_W;
   const int q = (wi + 2) & 3;    // TMEM lane quarter of this warp (warp wi + 2)
-  const int h = wi >> 2;         // which quarter of the query rows
+  const int h = wi >> 2;         // which half of the query rows
   const int tt = q * 32 + lane;  // token of S, dim of O
-  const int ci = wi * 32 + lane; // share of the widening (0 .. 511)
   const int r0 = h * RH;         // first query row of this thread
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
   int* redi = reinterpret_cast<int*>(red);
+  const int* vinfo = reinterpret_cast<const int*>(sm + C::OFF_VINFO);
   const float* qcs = reinterpret_cast<const float*>(sm + C::OFF_QC);
   const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
   const uint32_t tO = tl + (uint32_t)(C::COL_O + r0);
-  uint64_t* gbar = &bars[C::B_GS];
+  uint64_t* sbar = &bars[C::B_SYNC_S];
   const float vs_tensor = (C::KIND == KIND_FP8 && C::SKT == SK_TENSOR) ? reinterpret_cast<const float*>(p.v_scale)[0]
                                                                        : 1.f;
-  // exchange area of warp w: [0, RH) row maxima, [RH, 2 RH) row sums, then flags
   auto xr = [&](int w, int j) -> float& { return red[w * RW + j]; };
   auto xl = [&](int w, int j) -> float& { return red[w * RW + RH + j]; };
   auto xi = [&](int w, int slot) -> int& { return redi[w * RW + 2 * RH + slot]; };
-  constexpr int XM = 0, XV = 2, XVMAX = 4, XEMAX = 5;  // m flags[2], V flags[2], |vs| max, e max[4]
-  uint32_t gph = 0;
+  uint32_t sph = 0;
   int ord = -1, k = 0;
   bool ok = true;
   float m[RH], lp[RH], cq[RH];
   float vref = 0.f;
-  int vrefb[4] = {-1000, -1000, -1000, -1000};
+  int vrefq = 127;  // MXFP4: running V reference of this thread's dims' block (q)
 
   for (int task = tb; task < te && ok; ++task) {
     const TcTask T = tc_task(p, task);
@@ -621,8 +625,6 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
       const int kk = k + i, slot = kk % C::NS, buf = kk & 1;
       const uint8_t* raw = sm + C::OFF_RING + slot * C::SLOT;
       uint8_t* P = sm + C::OFF_BUF + buf * C::BUF_BYTES;
-      uint8_t* VF = P + C::P_BYTES;
-      uint8_t* KF = VF + C::VF_BYTES;
       const int c0 = T.t0 + i * C::TT;
       const bool own = c0 + tt < T.L;
       const bool first = i == 0;
@@ -633,16 +635,12 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
           lp[j] = 0.f;
         }
         vref = 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) vrefb[b] = -1000;
       }
       if (!tc_wait(&bars[C::B_RAW_FULL + slot], (kk / C::NS) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
-      // this token's scales, read before the stage is released
-      float kt = 1.f, vs = 0.f;
-      uint32_t vexp = 0;
+      float kt = 1.f, vs = 0.f;  // this token's scales, read before the stage is released
       if constexpr (C::TOK) {
         kt = reinterpret_cast<const float*>(raw + 2 * C::RAW_T)[tt];
         vs = own ? reinterpret_cast<const float*>(raw + 2 * C::RAW_T + C::RAW_SC)[tt] : 0.f;
@@ -652,77 +650,9 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
         const int e01 = max((int)(sw & 0xFF), (int)((sw >> 8) & 0xFF));
         const int e23 = max((int)((sw >> 16) & 0xFF), (int)(sw >> 24));
         kt = exp2i(max(e01, e23) - 127);
-        vexp = own ? reinterpret_cast<const uint32_t*>(raw + 2 * C::RAW_T + C::RAW_SC)[tt] : 0u;
       }
-      // this parity's buffers are free once the tile two back is through PV (and QK)
-      if (kk >= 2 && !tc_wait(&bars[C::B_PV_DONE + buf], ((kk - 2) >> 1) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if constexpr (C::KDQ) {
-        tc_widen_fp4<C, true>(raw, raw + 2 * C::RAW_T, KF, ci, c0, T.L, 0);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C::B_KF_FULL + buf]);
-      }
-      // ---- MXFP4: V references (lazy, per 32-dim block) before V is widened ----
-      int dexp = 0;  // exponent drop of this thread's dims' block (q), MXFP4
-      if constexpr (C::KIND == KIND_FP4) {
-        int ev[4];
-        bool need_v = false;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          ev[b] = (int)((vexp >> (8 * b)) & 0xFF);
-          need_v |= own && ev[b] > vrefb[b] + kLazyExp;
-        }
-        const int vfl = __any_sync(0xffffffffu, need_v) ? 1 : 0;
-        if (lane == 0) xi(wi, XV + buf) = vfl;
-        if (!grp_sync(gbar, gph, abort_flag, p.status, lane)) {
-          ok = false;
-          break;
-        }
-        int Fv = 0;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) Fv |= xi(w, XV + buf);
-        if (Fv) {
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int mv = (int)__reduce_max_sync(0xffffffffu, own ? (unsigned)ev[b] : 0u);
-            if (lane == 0) xi(wi, XEMAX + b) = mv;
-          }
-          if (!grp_sync(gbar, gph, abort_flag, p.status, lane)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            int tv = 0;
-#pragma unroll
-            for (int w = 0; w < C::NCW; ++w) tv = max(tv, xi(w, XEMAX + b));
-            if (tv > vrefb[b] + kLazyExp) {
-              if (b == q) dexp = vrefb[b] - tv;
-              vrefb[b] = tv;
-            }
-          }
-        }
-      }
-      // ---- widened V ----
-      if constexpr (C::KIND == KIND_FP8) {
-        tc_widen_fp8<C>(raw + C::RAW_T, VF, ci, c0, T.L);
-      } else if constexpr (C::KIND == KIND_FP4) {
-        const int bb = ci & 3;
-        const int vb = bb == 0 ? vrefb[0] : (bb == 1 ? vrefb[1] : (bb == 2 ? vrefb[2] : vrefb[3]));
-        tc_widen_fp4<C, false>(raw + C::RAW_T, raw + 2 * C::RAW_T + C::RAW_SC, VF, ci, c0, T.L, vb);
-      } else {
-        if (!own) {  // bf16 V feeds the MMA as stored: zero this quarter of an unowned row in place
-          uint8_t* vr = const_cast<uint8_t*>(raw) + C::RAW_T + (h >> 1) * (C::TT * 128) + tt * 128 + (h & 1) * 64;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(vr + 16 * c) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      fence_proxy_async();  // widened / zeroed rows are read next by the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C::B_RAW_EMPTY + slot]);  // bf16: the PV commit too
+      if (lane == 0) mbar_arrive(&bars[C::B_RAW_EMPTY + slot]);
       // ---- scores of this thread's token and rows ----
       const int sb = kk % C::SBUF;
       if (!tc_wait(&bars[C::B_S_FULL + sb], (kk / C::SBUF) & 1, abort_flag, p.status)) {
@@ -752,6 +682,19 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
         for (int j = 0; j < RH; ++j)
           if (!own || r0 + j >= p.R) x[j] = -INFINITY;
       }
+      // MXFP4: this tile's V reference moves, decided by the widening group
+      int dexpq = 0;
+      bool any_dexp = false;
+      if constexpr (C::KIND == KIND_FP4) {
+        if (!tc_wait(&bars[C::B_VINFO + buf], (kk >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const int* vi = vinfo + buf * C::VINFO_W;
+        any_dexp = (vi[0] | vi[1] | vi[2] | vi[3]) != 0;
+        dexpq = q == 0 ? vi[0] : (q == 1 ? vi[1] : (q == 2 ? vi[2] : vi[3]));
+        vrefq = q == 0 ? vi[4] : (q == 1 ? vi[5] : (q == 2 ? vi[6] : vi[7]));
+      }
       // ---- lazy raise of the running max (and fp8 per-token V reference), group-wide ----
       bool need_m = false;
 #pragma unroll
@@ -759,14 +702,14 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
       const float vsa = fabsf(vs);
       const bool need_v = C::TOK && vsa > vref * kLazyVref;
       const int fl = (__any_sync(0xffffffffu, need_m) ? 1 : 0) | (__any_sync(0xffffffffu, need_v) ? 2 : 0);
-      if (lane == 0) xi(wi, XM + buf) = fl;
-      if (!grp_sync(gbar, gph, abort_flag, p.status, lane)) {
+      if (lane == 0) xi(wi, XS_M + buf) = fl;
+      if (!grp_sync(sbar, sph, abort_flag, p.status, lane)) {
         ok = false;
         break;
       }
       int F = 0;
 #pragma unroll
-      for (int w = 0; w < C::NCW; ++w) F |= xi(w, XM + buf);
+      for (int w = 0; w < C::NSW; ++w) F |= xi(w, XS_M + buf);
       float alpha[RH];
 #pragma unroll
       for (int j = 0; j < RH; ++j) alpha[j] = 1.f;
@@ -784,10 +727,10 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
         if constexpr (C::TOK) {
           if (F & 2) {
             const uint32_t mv = __reduce_max_sync(0xffffffffu, __float_as_uint(vsa));
-            if (lane == 0) xi(wi, XVMAX) = (int)mv;
+            if (lane == 0) xi(wi, XS_VMAX) = (int)mv;
           }
         }
-        if (!grp_sync(gbar, gph, abort_flag, p.status, lane)) {
+        if (!grp_sync(sbar, sph, abort_flag, p.status, lane)) {
           ok = false;
           break;
         }
@@ -807,7 +750,7 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
           if (F & 2) {
             int a0 = 0;
 #pragma unroll
-            for (int w = 0; w < C::NCW; ++w) a0 = max(a0, xi(w, XVMAX));
+            for (int w = 0; w < C::NSW; ++w) a0 = max(a0, xi(w, XS_VMAX));
             const float tv = __int_as_float(a0);
             if (tv > vref * kLazyVref) {
               beta = vref > 0.f ? vref / tv : 0.f;
@@ -816,20 +759,24 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
           }
         }
       }
-      if (!first && (F != 0 || dexp != 0)) {  // rescale this thread's part of O (its dim, its rows)
+      if (!first && (F != 0 || any_dexp)) {  // rescale this thread's part of O (its dim, its rows)
         if (!tc_wait(&bars[C::B_PV_DONE + (buf ^ 1)], ((kk - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float bq = C::TOK ? beta : (C::KIND == KIND_FP4 ? exp2i(dexp) : 1.f);
+        const float bq = C::TOK ? beta : (C::KIND == KIND_FP4 ? exp2i(dexpq) : 1.f);
         float o[RH];
         tc_ld_half<C>(tO, o);
 #pragma unroll
         for (int j = 0; j < RH; ++j) o[j] *= alpha[j] * bq;
         tc_st_half<C>(tO, o);
       }
-      // ---- P ----
+      // ---- P (its buffer is free once the tile two back is through PV) ----
+      if (kk >= 2 && !tc_wait(&bars[C::B_PV_DONE + buf], ((kk - 2) >> 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
       {
         const float vf = C::TOK ? (vref > 0.f ? vs / vref : 0.f) : 1.f;
         uint8_t* pb = P + (tt >> 6) * (R * 128);
@@ -865,7 +812,7 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
       for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) xl(wi, j) = v;
     }
-    if (!grp_sync(gbar, gph, abort_flag, p.status, lane)) break;
+    if (!grp_sync(sbar, sph, abort_flag, p.status, lane)) break;
     float L[RH];
 #pragma unroll
     for (int j = 0; j < RH; ++j) L[j] = ((xl(4 * h, j) + xl(4 * h + 1, j)) + xl(4 * h + 2, j)) + xl(4 * h + 3, j);
@@ -877,10 +824,7 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
     float gam = 1.f;
     if constexpr (C::TOK) gam = vref;
     if constexpr (C::KIND == KIND_FP8 && C::SKT == SK_TENSOR) gam = vs_tensor;
-    if constexpr (C::KIND == KIND_FP4) {
-      const int vb = q == 0 ? vrefb[0] : (q == 1 ? vrefb[1] : (q == 2 ? vrefb[2] : vrefb[3]));
-      gam = exp2i(vb - 127);
-    }
+    if constexpr (C::KIND == KIND_FP4) gam = exp2i(vrefq - 127);
     if (nparts <= 1) {
 #pragma unroll
       for (int j = 0; j < RH; ++j) {
@@ -899,6 +843,126 @@ __device__ void tc_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
         const float inv = L[j] > 0.f ? gam / L[j] : 0.f;
         p.part_o[(slot * p.R + r) * C::D + tt] = o[j] * inv;
         if (tt == 0) reinterpret_cast<float2*>(p.part_ml)[slot * p.R + r] = make_float2(m[j], L[j]);
+      }
+    }
+    k += T.n;
+  }
+}
+
+// Widening group (warps 10-17): V (and MXFP4 K) of each tile to f16, bf16 unowned rows to
+// zero; MXFP4 per-block V references, published for the softmax group.
+template <class C>
+__device__ void tc_widener(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volatile int* abort_flag, int tb,
+                           int te, int wi, int lane) {
+  constexpr int RW = C::RED_W;
+  const int ci = wi * 32 + lane;  // share of the widening (0 .. 255)
+  int* redi = reinterpret_cast<int*>(sm + C::OFF_RED) + C::NSW * RW;  // rows of the widening warps
+  int* vinfo = reinterpret_cast<int*>(sm + C::OFF_VINFO);
+  uint64_t* wbar = &bars[C::B_SYNC_W];
+  auto xw = [&](int w, int slot) -> int& { return redi[w * RW + slot]; };
+  uint32_t wph = 0;
+  int k = 0;
+  bool ok = true;
+  int vrefb[4] = {-1000, -1000, -1000, -1000};
+  for (int task = tb; task < te && ok; ++task) {
+    const TcTask T = tc_task(p, task);
+    for (int i = 0; i < T.n; ++i) {
+      const int kk = k + i, slot = kk % C::NS, buf = kk & 1;
+      const uint8_t* raw = sm + C::OFF_RING + slot * C::SLOT;
+      uint8_t* VF = sm + C::OFF_BUF + buf * C::BUF_BYTES + C::P_BYTES;
+      uint8_t* KF = VF + C::VF_BYTES;
+      const int c0 = T.t0 + i * C::TT;
+      const bool first = i == 0;
+      if (first) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) vrefb[b] = -1000;
+      }
+      if (!tc_wait(&bars[C::B_RAW_FULL + slot], (kk / C::NS) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      // this parity's buffers are free once the tile two back is through PV (and QK)
+      if (kk >= 2 && !tc_wait(&bars[C::B_PV_DONE + buf], ((kk - 2) >> 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      if constexpr (C::KDQ) {
+        tc_widen_fp4<C, true>(raw, raw + 2 * C::RAW_T, KF, ci, c0, T.L, 0);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_KF_FULL + buf]);
+      }
+      if constexpr (C::KIND == KIND_FP4) {
+        // V references: raise block b when an owned exponent exceeds it by more than 2^3
+        const int b = ci & 3;
+        const uint8_t* vsc = raw + 2 * C::RAW_T + C::RAW_SC;
+        int emx = 0;
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int tok = (ci >> 2) + 64 * j;
+          const int e = c0 + tok < T.L ? (int)vsc[tok * 4 + b] : 0;
+          emx = max(emx, e);
+          need |= c0 + tok < T.L && e > vrefb[b] + kLazyExp;
+        }
+        const int vfl = __any_sync(0xffffffffu, need) ? 1 : 0;
+        if (lane == 0) xw(wi, XW_V + buf) = vfl;
+        if (!grp_sync(wbar, wph, abort_flag, p.status, lane)) {
+          ok = false;
+          break;
+        }
+        int Fv = 0;
+#pragma unroll
+        for (int w = 0; w < C::NWW; ++w) Fv |= xw(w, XW_V + buf);
+        int dexp[4] = {0, 0, 0, 0};
+        if (Fv) {
+          const int wm = (int)__reduce_max_sync(0x11111111u << (lane & 3), (unsigned)emx);  // lanes of block b
+          if (lane < 4) xw(wi, XW_EMAX + lane) = wm;
+          if (!grp_sync(wbar, wph, abort_flag, p.status, lane)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            int tv = 0;
+#pragma unroll
+            for (int w = 0; w < C::NWW; ++w) tv = max(tv, xw(w, XW_EMAX + bb));
+            if (tv > vrefb[bb] + kLazyExp) {
+              dexp[bb] = first ? 0 : vrefb[bb] - tv;
+              vrefb[bb] = tv;
+            }
+          }
+        }
+        if (wi == 0 && lane == 0) {
+          int* vi = vinfo + buf * C::VINFO_W;
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            vi[bb] = dexp[bb];
+            vi[4 + bb] = vrefb[bb];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_VINFO + buf]);
+      }
+      if constexpr (C::KIND == KIND_FP8) {
+        tc_widen_fp8<C>(raw + C::RAW_T, VF, ci, c0, T.L);
+      } else if constexpr (C::KIND == KIND_FP4) {
+        const int bb = ci & 3;
+        const int vb = bb == 0 ? vrefb[0] : (bb == 1 ? vrefb[1] : (bb == 2 ? vrefb[2] : vrefb[3]));
+        tc_widen_fp4<C, false>(raw + C::RAW_T, raw + 2 * C::RAW_T + C::RAW_SC, VF, ci, c0, T.L, vb);
+      } else {
+        const int tok = ci >> 1, u = ci & 1;  // bf16 V feeds the MMA as stored: zero unowned rows in place
+        if (c0 + tok >= T.L) {
+          uint8_t* vr = const_cast<uint8_t*>(raw) + C::RAW_T + u * (C::TT * 128) + tok * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vr + 16 * c) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async();  // widened / zeroed rows are read next by the tensor cores
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[C::B_PV_READY + buf]);
+        mbar_arrive(&bars[C::B_RAW_EMPTY + slot]);  // bf16: the PV commit releases it as well
       }
     }
     k += T.n;
@@ -933,8 +997,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     tc_producer<C>(p, &tmk, &tmv, sm, bars, abort_flag, tb, te, lane);
   } else if (warp == 1) {
     tc_mma<C>(p, sm, bars, abort_flag, tmem, tb, te, lane);
+  } else if (warp < 2 + C::NSW) {
+    tc_softmax<C>(p, sm, bars, abort_flag, tmem, tb, te, warp - 2, lane);
   } else {
-    tc_consumer<C>(p, sm, bars, abort_flag, tmem, tb, te, warp - 2, lane);
+    tc_widener<C>(p, sm, bars, abort_flag, tb, te, warp - 2 - C::NSW, lane);
   }
   tc_fence_before();
   __syncthreads();
