@@ -216,10 +216,11 @@ __device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int
 // block-table entries of the next slice are fetched one slice early (blk, one per box,
 // held by lanes 0..nbox-1) so that no refill waits on a dependent global load.
 struct SliceIt {
-  int task, c0, t1, s, hkv, L;
+  int task, c0, t0, t1, s, hkv, L;
   const int32_t* btrow;
   int blk;
   bool done;
+  int bx0, bcur, bnxt;  // blocks of this warp's boxes bx0 + lane and bx0 + 32 + lane in the task
 };
 
 __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p) {
@@ -228,13 +229,26 @@ __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p)
   it.hkv = tk.hkv_part & 0xFFFF;
   it.L = clamped_context(p, it.s);
   it.c0 = tk.tile_begin * kTileTokens;
+  it.t0 = it.c0;
   const int t1 = tk.tile_end * kTileTokens;
   it.t1 = t1 < it.L ? t1 : it.L;
   it.btrow = p.bt + (int64_t)it.s * p.bt_stride;
+  it.bx0 = -1;
 }
 
-// Advance to the first slice at or after the current one that holds tokens, and start
-// the block-table loads of its boxes.
+// Block of this warp's box ordinal `o` in the task (slice o / bps, box o % bps; 0 past
+// the context).
+template <class C>
+__device__ __forceinline__ int it_bt(const SliceIt& it, int o, int r0, int box_shift, int page_shift) {
+  const int bps_shift = (__ffs(C::TW) - 1) - box_shift;  // boxes per slice = 2^bps_shift
+  const int n = o >> bps_shift, b = o & ((1 << bps_shift) - 1);
+  const int tok = it.t0 + n * C::TC + r0 + (b << box_shift);
+  return tok < it.L ? it.btrow[tok >> page_shift] : 0;
+}
+
+// Advance to the first slice at or after the current one that holds tokens, and take
+// the blocks of its boxes from the warp's block-table window: entries for 32 boxes per
+// load, one per lane, the next 32 in flight while these are used.
 template <class C>
 __device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, int t_end, int r0,
                                           int lane, int box_shift, int page_shift) {
@@ -245,10 +259,23 @@ __device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, in
     }
     it_load_task(it, p);
   }
-  if (!it.done) {
-    const int tok = it.c0 + r0 + (lane << box_shift);
-    if (lane < (C::TW >> box_shift) && tok < it.L) it.blk = it.btrow[tok >> page_shift];
+  if (it.done) return;
+  if (it.bx0 < 0) {
+    it.bx0 = 0;
+    it.bcur = it_bt<C>(it, lane, r0, box_shift, page_shift);
+    it.bnxt = it_bt<C>(it, 32 + lane, r0, box_shift, page_shift);
   }
+  const int bps_shift = (__ffs(C::TW) - 1) - box_shift;
+  const int o0 = ((it.c0 - it.t0) / C::TC) << bps_shift;  // first box of this slice
+  if (o0 >= it.bx0 + 32) {  // boxes per slice divide 32: a slice never straddles windows
+    it.bx0 += 32;
+    it.bcur = it.bnxt;
+    it.bnxt = it_bt<C>(it, it.bx0 + 32 + lane, r0, box_shift, page_shift);
+  }
+  const int idx = o0 + lane - it.bx0;
+  const int from_cur = __shfl_sync(0xffffffffu, it.bcur, idx & 31);
+  const int from_nxt = __shfl_sync(0xffffffffu, it.bnxt, idx & 31);
+  it.blk = idx < 32 ? from_cur : from_nxt;
 }
 
 // Issue the TMA / bulk copies of one warp slice (tokens [a, min(a + TW, L)) of the
