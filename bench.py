@@ -14,6 +14,9 @@ e2e    = the same metric through the C ABI with host buffers: per step the query
          block tables and context lengths are copied from pinned host memory and
          the output is copied back, inside the timed region (the KV cache is the
          engine's resident state and stays in HBM).
+per_config = every workload of the method, timed one call at a time through the C ABI
+         (plan + tile + reduce, device buffers) with the 129 MB L2 flushed before each
+         call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak.
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -142,6 +145,47 @@ def kernel_source_hash():
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def per_config(device, peak, calls=10, warmup=3):
+    """µs/call and GB/s of every workload of the method, one call at a time, L2 flushed."""
+    cases = [synth.config1(), synth.config2("a"), synth.config2("b"), synth.config3(qlen=1),
+             synth.config3(qlen=4)] + [synth.config4(batch=b) for b in (8, 64, 512, 4096)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for case in cases:
+        p = synth.make(case, device=device)
+        q = p["query"]
+        if q.dtype == torch.uint8:
+            q = q.view(torch.float8_e4m3fn)
+        out = torch.empty(tuple(p["query"].shape), dtype=torch.bfloat16, device=device)
+        args = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"], p["context_lens"],
+                             out, key_scale=p["key_scale"], value_scale=p["value_scale"],
+                             q_scale=p["q_scale"], softmax_scale=case.scale_qk())
+        ws = ops.alloc_workspace(args, device)
+        for _ in range(warmup):
+            ops.pa_decode_run(args, ws, stream)
+        ts = []
+        for _ in range(calls):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ops.pa_decode_run(args, ws, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        assert ops.pa_decode_read_status(ws) == 0, case.name
+        nbytes = synth.algorithmic_bytes(case, p["context_lens"].cpu().tolist())
+        med = statistics.median(ts)
+        name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
+        res[name] = {"us_per_call": round(med * 1e3, 2), "algorithmic_bytes": nbytes,
+                     "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
+                     "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
+        del p, out, ws
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def make_variant(kv, device, batch=None):
@@ -276,7 +320,8 @@ def run_ours(a):
                    "global_batch": 16 * ws_n, "seq_len": "120000-131072",
                    "parallelism": f"replicas x{ws_n}",
                    "l2": "no flush: each call streams more than the 129 MB L2",
-                   "mma": "mma.sync m16n8k16 f16 x f16 -> f32",
+                   "mma": ("tcgen05.mma (TMEM accumulators)" if os.environ.get("PA_DECODE_KERNEL") == "tc"
+                           else "mma.sync m16n8k16 f16 x f16 -> f32"),
                    "merge": "separate pa_decode_reduce launch"},
         "per_variant": per,
         "roofline": {"bound": "hbm", "kernel": f"pa_tile_kernel ({dom['case'].name})",
@@ -289,6 +334,10 @@ def run_ours(a):
     }
     if a.batch is not None or a.variant != "both":
         line["config"]["note"] = "profiling subset, not the benchmark workload"
+    if os.environ.get("PA_DECODE_KERNEL") == "tc":
+        line["config"]["kernel"] = "tcgen05 (PA_DECODE_KERNEL=tc)"
+    if not a.no_per_config and a.batch is None and a.variant == "both":
+        line["per_config"] = per_config(dev, peak)
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(variants) if not a.no_cpu_baseline else None
         print(json.dumps(line), flush=True)
@@ -386,7 +435,13 @@ def main():
                     help="KV variants of the long-context workload in a step (profiling: one)")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch for profiling captures (default: the workload's 16)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload µs/call table")
+    ap.add_argument("--kernel", default=None, choices=["mma", "tc"],
+                    help="decode kernel: mma.sync (default) or the tcgen05 kernel")
     a = ap.parse_args()
+    if a.kernel is not None:
+        os.environ["PA_DECODE_KERNEL"] = a.kernel
     if a.warmup < 3 and a.impl == "ours":
         a.warmup = 3
     if a.impl == "reference":

@@ -60,34 +60,42 @@ __device__ T block_exclusive_scan(T v, T* total, T* sh) {  // sh: >= 32 elements
 }
 
 // How a unit of n tiles starting at global tile U splits: one partition per chunk it
-// touches (one in all when it is empty or splitting is off).
+// touches (one in all when it is empty or splitting is off).  Tile counts are 32-bit:
+// the plan serves fewer than 2^31 tiles (5.5e11 tokens) in one call.
 struct ChunkGrid {
-  long long C;        // tiles per chunk
-  long long nchunks;  // chunks that hold tiles (>= 1)
+  uint32_t C;        // tiles per chunk
+  uint32_t nchunks;  // chunks that hold tiles (>= 1)
   int maxp;
 };
 
-__device__ __forceinline__ int unit_parts(const ChunkGrid& cg, long long U, int n) {
+__device__ __forceinline__ int unit_parts(const ChunkGrid& cg, uint32_t U, int n) {
   if (n == 0 || cg.maxp < 2) return 1;
-  return (int)((U + n - 1) / cg.C - U / cg.C + 1);
+  return (int)((U + (uint32_t)n - 1) / cg.C - U / cg.C + 1);
 }
 
 // Tiles [begin, end) of partition q of the unit, and its chunk.
-__device__ __forceinline__ void unit_part(const ChunkGrid& cg, long long U, int n, int q, int* begin,
+__device__ __forceinline__ void unit_part(const ChunkGrid& cg, uint32_t U, int n, int q, int* begin,
                                           int* end, int* chunk) {
+  const uint32_t c0 = U / cg.C;
   if (n == 0 || cg.maxp < 2) {
-    const long long c = U / cg.C;
     *begin = 0;
     *end = n;
-    *chunk = (int)(c < cg.nchunks - 1 ? c : cg.nchunks - 1);
+    *chunk = (int)(c0 < cg.nchunks - 1 ? c0 : cg.nchunks - 1);
     return;
   }
-  const long long c = U / cg.C + q;
-  const long long g0 = c * cg.C > U ? c * cg.C : U;
-  const long long g1 = (c + 1) * cg.C < U + n ? (c + 1) * cg.C : U + n;
+  const uint32_t c = c0 + (uint32_t)q;
+  const uint32_t g0 = c * cg.C > U ? c * cg.C : U;
+  const uint32_t g1 = (c + 1) * cg.C < U + (uint32_t)n ? (c + 1) * cg.C : U + (uint32_t)n;
   *begin = (int)(g0 - U);
   *end = (int)(g1 - U);
   *chunk = (int)c;
+}
+
+// Chunk of the last task of a unit (its last partition).
+__device__ __forceinline__ int unit_last_chunk(const ChunkGrid& cg, uint32_t U, int n) {
+  int b, e, c;
+  unit_part(cg, U, n, unit_parts(cg, U, n) - 1, &b, &e, &c);
+  return c;
 }
 
 __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
@@ -95,6 +103,7 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   __shared__ int sh32[32];
   __shared__ int sh32b[32];
   __shared__ int shmax;
+  __shared__ int sh_last[1024];  // chunk of each thread's last task in the current round
   const int tid = threadIdx.x;
   const int cap = pp.W * pp.S;
   pdl_wait_prior();          // the previous kernel may still read this workspace
@@ -104,10 +113,11 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     shmax = 0;
   }
   __syncthreads();
-  int clamped = 0, lmax = 0;
+  int clamped = 0, lmax = 0, n_own = 0;  // n_own: tiles of sequence tid (one round of sequences)
   long long local = 0;
   for (int s = tid; s < pp.B; s += blockDim.x) {
     const int n = (clamp_len(pp.ctx[s], cap, &clamped) + kTileTokens - 1) / kTileTokens;
+    if (s == tid) n_own = n;
     local += n;
     lmax = n > lmax ? n : lmax;
   }
@@ -115,40 +125,53 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   if (clamped) atomicOr(pp.status, ST_CLAMPED);
   long long seq_tiles;
   (void)block_exclusive_scan<long long>(local, &seq_tiles, sh64);  // also orders shmax
-  const long long T = seq_tiles * pp.Hkv;
+  long long T64 = seq_tiles * pp.Hkv;
+  if (T64 > 0x7FFFFFFFll) {  // beyond the plan's range: flag it (the host bounds make this unreachable)
+    if (tid == 0) atomicOr(pp.status, ST_CLAMPED);
+    T64 = 0x7FFFFFFFll;
+  }
+  const uint32_t T = (uint32_t)T64;
   ChunkGrid cg;
   cg.maxp = pp.max_partitions;
-  cg.C = (T + pp.budget - 1) / pp.budget;
+  cg.C = (T + (uint32_t)pp.budget - 1) / (uint32_t)pp.budget;
   if (cg.C < 1) cg.C = 1;
   if (cg.maxp >= 2) {  // no unit may touch more than max_partitions chunks
-    const long long cmin = (long long)(shmax - 1) / (cg.maxp - 1) + 1;
+    const uint32_t cmin = (uint32_t)(shmax - 1) / (uint32_t)(cg.maxp - 1) + 1;
     if (cg.C < cmin) cg.C = cmin;
   }
   cg.nchunks = T > 0 ? (T + cg.C - 1) / cg.C : 1;
 
   long long carry_tiles = 0;
-  int carry_tasks = 0, carry_slots = 0;
+  int carry_tasks = 0, carry_slots = 0, carry_chunk = -1;  // chunk of the last task so far
   for (int base = 0; base < pp.B; base += blockDim.x) {
     const int s = base + tid;
-    int dummy = 0;
-    const int n = s < pp.B ? (clamp_len(pp.ctx[s], cap, &dummy) + kTileTokens - 1) / kTileTokens : 0;
+    int n = 0;
+    if (s < pp.B) {
+      int dummy = 0;
+      n = base == 0 ? n_own : (clamp_len(pp.ctx[s], cap, &dummy) + kTileTokens - 1) / kTileTokens;
+    }
     long long round_tiles;
     const long long before = block_exclusive_scan<long long>((long long)n, &round_tiles, sh64);
-    const long long U0 = (carry_tiles + before) * pp.Hkv;  // global first tile of unit (s, 0)
+    const uint32_t U0 = (uint32_t)((carry_tiles + before) * pp.Hkv);  // first tile of unit (s, 0)
     int ntask = 0, nslot = 0;
-    if (s < pp.B)
+    if (s < pp.B) {
       for (int h = 0; h < pp.Hkv; ++h) {
-        const int P = unit_parts(cg, U0 + (long long)h * n, n);
+        const int P = unit_parts(cg, U0 + (uint32_t)(h * n), n);
         ntask += P;
         nslot += P >= 2 ? P : 0;
       }
+      sh_last[tid] = unit_last_chunk(cg, U0 + (uint32_t)((pp.Hkv - 1) * n), n);
+    }
     int tot_t, tot_s;
-    const int off_t = block_exclusive_scan<int>(ntask, &tot_t, sh32);
+    const int off_t = block_exclusive_scan<int>(ntask, &tot_t, sh32);  // its syncs order sh_last
     const int off_s = block_exclusive_scan<int>(nslot, &tot_s, sh32b);
     if (s < pp.B) {
       int t = carry_tasks + off_t, slot = carry_slots + off_s;
+      // tasks are in unit order, hence in non-decreasing chunk order: chunk c runs tasks
+      // [chunk_first[c], chunk_first[c + 1]); every chunk that begins at a task is set here
+      int prev = tid > 0 ? sh_last[tid - 1] : carry_chunk;
       for (int h = 0; h < pp.Hkv; ++h) {
-        const long long U = U0 + (long long)h * n;
+        const uint32_t U = U0 + (uint32_t)(h * n);
         const int P = unit_parts(cg, U, n);
         const int u = s * pp.Hkv + h;
         pp.nparts[u] = P;
@@ -163,24 +186,21 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
           unit_part(cg, U, n, q, &tk.tile_begin, &tk.tile_end, &chunk);
           pp.tasks[t] = tk;
           pp.task_chunk[t] = chunk;
+          for (int k = prev + 1; k <= chunk; ++k) pp.chunk_first[k] = t;
+          prev = chunk;
         }
       }
     }
+    const int last_s = min(pp.B, base + (int)blockDim.x) - 1 - base;
+    carry_chunk = sh_last[last_s];
     carry_tiles += round_tiles;
     carry_tasks += tot_t;
     carry_slots += tot_s;
+    __syncthreads();  // sh_last is rewritten by the next round
   }
   if (tid == 0) *pp.ntasks = carry_tasks;
-  __syncthreads();  // this block's task_chunk writes are visible to all its threads
-  // Tasks are in unit order, hence in non-decreasing chunk order: chunk c runs tasks
-  // [chunk_first[c], chunk_first[c + 1]).  Chunks past the last task hold none.
-  for (int t = tid; t < carry_tasks; t += blockDim.x) {
-    const int c = pp.task_chunk[t];
-    const int prev = t == 0 ? -1 : pp.task_chunk[t - 1];
-    for (int k = prev + 1; k <= c; ++k) pp.chunk_first[k] = t;
-  }
-  const int last = carry_tasks > 0 ? pp.task_chunk[carry_tasks - 1] + 1 : 0;
-  for (int c = last + tid; c <= pp.budget; c += blockDim.x) pp.chunk_first[c] = carry_tasks;
+  // chunks past the last task hold none
+  for (int c = carry_chunk + 1 + tid; c <= pp.budget; c += blockDim.x) pp.chunk_first[c] = carry_tasks;
 }
 
 // ------------------------------------------------------------------------------------
