@@ -95,6 +95,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Brings the line holding `p` into L2 (no register result, never faults the warp).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Orders this thread's earlier generic-proxy accesses to shared memory before later
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async() {

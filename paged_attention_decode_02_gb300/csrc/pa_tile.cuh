@@ -65,7 +65,7 @@ struct TileCfg {
   static constexpr int X_BYTES = NDW == 2 ? NTG * 2 * 2 * XW * 4 : 0;
   static constexpr int OFF_OB = OFF_X + X_BYTES;
   static constexpr int OFF_ML = OFF_OB + RPAD * D * 4;
-  static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;
+  static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;  // 1 / sum per row
   static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 6 : 0;  // e8m0 factor tables
   static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
   static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
@@ -129,6 +129,32 @@ __device__ __forceinline__ int o_dim(int n, int j, int dw, int t) {
   } else {
     return 32 * (n >> 2) + 8 * t + (n & 3) + 4 * (j & 1);
   }
+}
+
+// Inverse of o_dim: the float index, in the fragment-ordered merge buffer, of output
+// row `row`, head dim `d` (buffer: per warp of a token group, per (m-tile, n-tile), 32
+// lanes x float4).
+template <class C>
+__device__ __forceinline__ int frag_pos(int row, int d) {
+  const int mt = row >> 4, g = row & 7, jh = (row >> 3) & 1;
+  const int dw = d / C::DW, dd = d - dw * C::DW;
+  int n, t, jl;
+  if constexpr (C::KIND == KIND_BF16) {  // dd = 8n + 2t + jl
+    n = dd >> 3;
+    t = (dd >> 1) & 3;
+    jl = dd & 1;
+  } else if constexpr (C::KIND == KIND_FP8) {  // dd = 16 (n >> 1) + 4t + (n & 1) + 2 jl
+    const int r = dd & 15;
+    n = 2 * (dd >> 4) + (r & 1);
+    t = r >> 2;
+    jl = (r >> 1) & 1;
+  } else {  // dd = 32 (n >> 2) + 8t + (n & 3) + 4 jl
+    const int r = dd & 31;
+    n = 4 * (dd >> 5) + (r & 3);
+    t = r >> 3;
+    jl = (r >> 2) & 1;
+  }
+  return ((dw * (C::MT * C::NTD) + mt * C::NTD + n) * 32 + 4 * g + t) * 4 + 2 * jh + jl;
 }
 
 // 2^(e - 127) for an e8m0 byte as fp32 (e = 0 flushes to 0; 255 gives +inf).
@@ -799,9 +825,20 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     t1 = t1 < L ? t1 : L;
     const int unit = s * p.Hkv + hkv;
     const int nparts = p.nparts[unit];
+    const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
 
     load_q<C>(p, smem, s, hkv, cw, lane, k_scale_tensor);
     named_bar(BAR_CONSUMERS, C::NCW * 32);
+    // Touch this task's output rows now, so that their address translation is not first
+    // needed by the stores at the end of the task, with the memory system under load.
+    if (cw == 0 && lane == 0) {
+      if (nparts > 1) {
+        prefetch_l2(p.part_o + slot * p.R * C::D);
+        prefetch_l2(p.part_ml + 2 * slot * p.R);
+      } else {
+        prefetch_l2(p.out + (int64_t)s * p.qlen * p.o_st + (int64_t)hkv * p.G * p.o_sh);
+      }
+    }
 
     uint32_t qa[C::Q_IN_REGS ? C::MT : 1][C::Q_IN_REGS ? C::NKCH : 1][4];
     if constexpr (C::Q_IN_REGS) {
@@ -908,12 +945,14 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         bfac[b] = C::TOK_SCALE ? A.vref : v_scale_tensor;
       }
     }
-    // Groups 0 .. NTG-2 add their scaled accumulators into a buffer kept in fragment order
-    // (each lane owns float4 columns: no bank conflicts), one group at a time; the last
-    // group adds its own and stores.
+    // The groups add their scaled accumulators, one group at a time, into a buffer kept in
+    // fragment order (each lane owns float4 columns: no bank conflicts); the last group
+    // also leaves 1 / sum per row.  Then all threads store the rows, 4 consecutive head
+    // dims each, with coalesced writes.
     float4* ob4 = reinterpret_cast<float4*>(obuf) + dw * (C::MT * C::NTD * 32) + lane;
+    float* fin = reinterpret_cast<float*>(smem + C::OFF_FIN);
 #pragma unroll 1
-    for (int i = 0; i + 1 < C::NTG; ++i) {
+    for (int i = 0; i < C::NTG; ++i) {
       if (tg == i) {
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt)
@@ -930,45 +969,36 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
             }
             *dst = v;
           }
+        if (i == C::NTG - 1 && dw == 0 && t == 0) {
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int row = 16 * mt + g + 8 * hr;
+              fin[row] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
+              if (nparts > 1 && row < p.R)
+                reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] =
+                    make_float2(Mrow[mt][hr], Lrow[mt][hr]);
+            }
+        }
       }
       named_bar(BAR_CONSUMERS, C::NCW * 32);
     }
-    if (tg == C::NTG - 1) {
-      const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
-#pragma unroll
-      for (int mt = 0; mt < C::MT; ++mt) {
-        float inv[2];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          inv[hr] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
-          const int row = 16 * mt + g + 8 * hr;
-          if (nparts > 1 && dw == 0 && t == 0 && row < p.R)
-            reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] = make_float2(Mrow[mt][hr], Lrow[mt][hr]);
-        }
-#pragma unroll
-        for (int n = 0; n < C::NTD; ++n) {
-          const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
-          const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
-          float4 v = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0, A.o[mt][n][2] * f1,
-                                 A.o[mt][n][3] * f1);
-          if (C::NTG > 1) {
-            const float4 w = ob4[(mt * C::NTD + n) * 32];
-            v = make_float4(w.x + v.x, w.y + v.y, w.z + v.z, w.w + v.w);
-          }
-          const float vals[4] = {v.x * inv[0], v.y * inv[0], v.z * inv[1], v.w * inv[1]};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int row = 16 * mt + g + 8 * (j >> 1);
-            if (row >= p.R) continue;
-            const int d = o_dim<C>(n, j, dw, t);
-            if (nparts <= 1) {
-              const int i = row / p.G, h = hkv * p.G + row % p.G;
-              const int64_t orow = (int64_t)s * p.qlen + i;
-              p.out[orow * p.o_st + (int64_t)h * p.o_sh + d] = __float2bfloat16_rn(vals[j]);
-            } else {
-              p.part_o[(slot * p.R + row) * C::D + d] = vals[j];
-            }
-          }
+    {
+      constexpr int Q4 = C::D / 4;
+      for (int c = cw * 32 + lane; c < p.R * Q4; c += C::NTHREADS) {
+        const int row = c / Q4, d0 = 4 * (c - row * Q4);
+        const float inv = fin[row];
+        const float v0 = obuf[frag_pos<C>(row, d0)] * inv, v1 = obuf[frag_pos<C>(row, d0 + 1)] * inv;
+        const float v2 = obuf[frag_pos<C>(row, d0 + 2)] * inv, v3 = obuf[frag_pos<C>(row, d0 + 3)] * inv;
+        if (nparts <= 1) {
+          const int i = row / p.G, h = hkv * p.G + row % p.G;
+          const int64_t orow = (int64_t)s * p.qlen + i;
+          *reinterpret_cast<uint2*>(p.out + orow * p.o_st + (int64_t)h * p.o_sh + d0) =
+              make_uint2(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3));
+        } else {
+          *reinterpret_cast<float4*>(p.part_o + (slot * p.R + row) * C::D + d0) =
+              make_float4(v0, v1, v2, v3);
         }
       }
     }

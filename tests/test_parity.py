@@ -96,6 +96,26 @@ def test_tensor_core_kernel_matches_oracle(case, mode, monkeypatch):
                        util.oracle_decode(p), case.kv, case.name + " tcgen05")
 
 
+_LENS30 = [int(x) for x in np.random.default_rng(2504).integers(1, 800, 30)]
+MANY_TASKS = [
+    synth.config4(batch=64, seed=2501),
+    synth.config3(qlen=1, batch=40, head_dim=128, context_lens=(200, 1500), seed=2502),
+    synth.config3(qlen=4, batch=24, context_lens=(100, 900), seed=2503),
+    synth.config1(batch=30, context_lens=_LENS30, seed=2504),
+]
+
+
+@pytest.mark.parametrize("case", MANY_TASKS, ids=lambda c: f"{c.name}-b{c.batch}")
+@pytest.mark.parametrize("mode", ["split", "direct"])
+def test_many_tasks_per_chunk(case, mode):
+    # three CTAs, each walking 16 to 30 tasks: past the tasks staged in shared memory at
+    # CTA start, so both the staged and the global-memory paths of a task switch run,
+    # with bf16 and e4m3 queries staged for the next task
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=3)
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name + " many tasks")
+
+
 @pytest.mark.parametrize("lens", [[0, 0], [1, 2], [255, 256, 257], [511, 512, 513, 767]])
 def test_ragged_edges(lens):
     case = synth.Case("edges", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=len(lens),
