@@ -16,12 +16,14 @@ namespace pa {
 
 // ------------------------------------------------------------------------------------
 // Plan: ceil(L/256) tiles per (sequence, KV head) unit ("[FlyDSL] pa_decode: zero V rows
-// past the context before PV", Root cause).  The units' tiles, laid end to end, are cut
+// past the context before PV", Root cause).  The units are laid end to end, each as a
+// gap of kUnitCostTiles (the fixed cost of starting and finishing a task: query load,
+// first-slice latency, masked tail, merge) followed by its tiles, and the line is cut
 // into `budget` chunks of equal length, one per tile-kernel CTA; a unit crossing a chunk
 // boundary becomes several partitions whose partials are merged afterwards ("[FlyDSL]
 // pa_decode: MXFP4 K/V ...", commit messages: planned tasks, direct output with one
 // partition, tasks from a CU budget; max_partitions caps the split).  Equal chunks keep
-// every CTA busy for the same number of tiles whatever the mix of context lengths.
+// every CTA busy for the same time whatever the mix of context lengths.
 // ------------------------------------------------------------------------------------
 __device__ __forceinline__ int clamp_len(int L, int cap, int* clamped) {
   if (L < 0) return 0;
@@ -59,11 +61,11 @@ __device__ T block_exclusive_scan(T v, T* total, T* sh) {  // sh: >= 32 elements
   return before;
 }
 
-// How a unit of n tiles starting at global tile U splits: one partition per chunk it
-// touches (one in all when it is empty or splitting is off).  Tile counts are 32-bit:
-// the plan serves fewer than 2^31 tiles (5.5e11 tokens) in one call.
+// How a unit of n tiles whose first tile sits at position U of the line splits: one
+// partition per chunk it touches (one in all when it is empty or splitting is off).
+// Positions are 32-bit: the plan serves lines shorter than 2^31 tiles in one call.
 struct ChunkGrid {
-  uint32_t C;        // tiles per chunk
+  uint32_t C;        // line positions (tiles and unit gaps) per chunk
   uint32_t nchunks;  // chunks that hold tiles (>= 1)
   int maxp;
 };
@@ -125,8 +127,9 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   if (clamped) atomicOr(pp.status, ST_CLAMPED);
   long long seq_tiles;
   (void)block_exclusive_scan<long long>(local, &seq_tiles, sh64);  // also orders shmax
-  long long T64 = seq_tiles * pp.Hkv;
-  if (T64 > 0x7FFFFFFFll) {  // beyond the plan's range: flag it (the host bounds make this unreachable)
+  const int w = kUnitCostTiles;
+  long long T64 = (seq_tiles + (long long)w * pp.B) * pp.Hkv;  // length of the line
+  if (T64 > 0x7FFFFFFFll) {  // beyond the plan's range (2^31 tiles): flag it, results undefined
     if (tid == 0) atomicOr(pp.status, ST_CLAMPED);
     T64 = 0x7FFFFFFFll;
   }
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   cg.maxp = pp.max_partitions;
   cg.C = (T + (uint32_t)pp.budget - 1) / (uint32_t)pp.budget;
   if (cg.C < 1) cg.C = 1;
-  if (cg.maxp >= 2) {  // no unit may touch more than max_partitions chunks
+  if (cg.maxp >= 2 && shmax > 0) {  // no unit may touch more than max_partitions chunks
     const uint32_t cmin = (uint32_t)(shmax - 1) / (uint32_t)(cg.maxp - 1) + 1;
     if (cg.C < cmin) cg.C = cmin;
   }
@@ -152,15 +155,17 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     }
     long long round_tiles;
     const long long before = block_exclusive_scan<long long>((long long)n, &round_tiles, sh64);
-    const uint32_t U0 = (uint32_t)((carry_tiles + before) * pp.Hkv);  // first tile of unit (s, 0)
+    // position of the first tile of unit (s, 0); unit (s, h) starts h * (n + w) later
+    const uint32_t U0 =
+        (uint32_t)((carry_tiles + before) * pp.Hkv + (long long)w * ((long long)s * pp.Hkv + 1));
     int ntask = 0, nslot = 0;
     if (s < pp.B) {
       for (int h = 0; h < pp.Hkv; ++h) {
-        const int P = unit_parts(cg, U0 + (uint32_t)(h * n), n);
+        const int P = unit_parts(cg, U0 + (uint32_t)(h * (n + w)), n);
         ntask += P;
         nslot += P >= 2 ? P : 0;
       }
-      sh_last[tid] = unit_last_chunk(cg, U0 + (uint32_t)((pp.Hkv - 1) * n), n);
+      sh_last[tid] = unit_last_chunk(cg, U0 + (uint32_t)((pp.Hkv - 1) * (n + w)), n);
     }
     int tot_t, tot_s;
     const int off_t = block_exclusive_scan<int>(ntask, &tot_t, sh32);  // its syncs order sh_last
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
       // [chunk_first[c], chunk_first[c + 1]); every chunk that begins at a task is set here
       int prev = tid > 0 ? sh_last[tid - 1] : carry_chunk;
       for (int h = 0; h < pp.Hkv; ++h) {
-        const uint32_t U = U0 + (uint32_t)(h * n);
+        const uint32_t U = U0 + (uint32_t)(h * (n + w));
         const int P = unit_parts(cg, U, n);
         const int u = s * pp.Hkv + h;
         pp.nparts[u] = P;
@@ -345,6 +350,7 @@ pa_status validate(const pa_decode_args* a) {
   if (a->head_dim < 1 || a->page_size < 1 || a->num_blocks < 1 || a->max_blocks_per_seq < 1)
     return PA_ERR_INVALID_ARG;
   if ((int64_t)a->max_blocks_per_seq * a->page_size > (int64_t)1 << 30) return PA_ERR_UNSUPPORTED;
+  if ((int64_t)a->batch * a->num_kv_heads > ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
   if (a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
   switch (a->page_size) {
     case 16: case 32: case 64: case 128: case 256: break;

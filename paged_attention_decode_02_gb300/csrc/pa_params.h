@@ -9,6 +9,10 @@
 namespace pa {
 
 constexpr int kTileTokens = 256;  // the plan's work unit: ceil(L / 256) tiles per sequence
+// What the plan charges each (sequence, KV head) unit on top of its tiles: a task's fixed
+// cost (query load, first-slice latency, masked tail, merge and store) measured at about
+// two tiles' worth of streaming on the long-context workloads.
+constexpr int kUnitCostTiles = 2;
 
 // One task = a run of consecutive 256-token tiles of one (sequence, KV head) unit.
 struct PlanTask {

@@ -56,6 +56,11 @@ struct TileCfg {
   static constexpr int SLOT_KV = 2 * SLOT_V;       // K + V bytes of one slot
   static constexpr int SLOT_SC = 8 * TW;           // K then V scales (fp32 or 4 e8m0 bytes)
   static constexpr bool Q_IN_REGS = MT * NKCH * 4 <= 32;
+  // The last task of a chunk merges its token groups in one pass through the (then idle)
+  // load ring when every group's accumulator fits there.
+  static constexpr bool PAR_MERGE = NCW * MT * NTD * 32 * 16 <= NCW * NSTAGE * SLOT_KV;
+  // Query words are loaded ahead of a task when they take few registers.
+  static constexpr bool Q_EARLY = ((RPAD + NCW - 1) / NCW) * (D / 64 + 1) <= 8;
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_SC = OFF_RING + NCW * NSTAGE * SLOT_KV;
   static constexpr int OFF_Q = OFF_SC + NCW * NSTAGE * SLOT_SC;
@@ -70,7 +75,8 @@ struct TileCfg {
   static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
   static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
   static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
-  static constexpr int SMEM = OFF_FLAG + 16 + 1024;  // + slack to align the base to 1 KiB
+  static constexpr int OFF_NXT = OFF_FLAG + 16;  // the next task's record (16 bytes)
+  static constexpr int SMEM = OFF_NXT + 16 + 1024;  // + slack to align the base to 1 KiB
   static_assert(TW % 16 == 0, "a warp slice holds whole 16-token k-chunks");
   static_assert(WBYTES % 64 == 0, "a warp row slice is whole ldmatrix.x4 groups");
   static_assert(NSUB % NDW == 0, "head-dim split on sub-tile boundaries");
@@ -165,43 +171,79 @@ __device__ __forceinline__ float exp2i(int k) {
   return k < -126 ? 0.f : __int_as_float((k + 127) << 23);
 }
 
-// Load and convert the query rows of (s, hkv) into shared memory, with the per-row
-// logit factor (softmax scale * log2 e * q scale * row normalisation * k scale).
+// The query words a lane reads for its rows of one task: loaded ahead of their use
+// (before the ring is first filled, or while the previous task merges) and converted
+// when the task starts.
 template <class C>
-__device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int cw, int lane,
-                       float k_scale_tensor) {
-  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::OFF_Q);
-  float* cr = reinterpret_cast<float*>(smem + C::OFF_CR);
-  constexpr int EPL = C::D / 32;
-  for (int r = cw; r < C::RPAD; r += C::NCW) {
-    float x[EPL];
-    float crv = 0.f;
-    if (r < p.R) {
+struct QRaw {
+  static constexpr int ROWS = (C::RPAD + C::NCW - 1) / C::NCW;  // rows per warp
+  static constexpr int EPL = C::D / 32;                          // elements per lane per row
+  static constexpr int NW = EPL / 2;  // 32-bit words per row (bf16; e4m3 uses EPL / 4)
+  uint32_t w[ROWS][NW];
+  float qsc[ROWS];
+};
+
+template <class C>
+__device__ __forceinline__ void load_q_issue(const DecodeParams& p, int s, int hkv, int cw,
+                                             int lane, QRaw<C>& q) {
+  constexpr int EPL = QRaw<C>::EPL;
+#pragma unroll
+  for (int k = 0; k < QRaw<C>::ROWS; ++k) {
+    const int r = cw + k * C::NCW;
+    q.qsc[k] = 1.f;
+    if (r < C::RPAD && r < p.R) {
       const int i = r / p.G, h = hkv * p.G + r % p.G;
       const int64_t row = (int64_t)s * p.qlen + i;
       const int64_t off = row * p.q_st + (int64_t)h * p.q_sh + lane * EPL;
-      float qsc = 1.f;
       if (p.q_fp8) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + off;
-        uint32_t w[EPL / 4];
+        const uint32_t* src =
+            reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.q) + off);
 #pragma unroll
-        for (int k = 0; k < EPL / 4; ++k) w[k] = reinterpret_cast<const uint32_t*>(src)[k];
-#pragma unroll
-        for (int k = 0; k < EPL / 4; ++k) {
-          uint32_t lo = e4m3x2_to_f16x2(w[k] & 0xFFFF), hi = e4m3x2_to_f16x2(w[k] >> 16);
-          __half2 l2 = *reinterpret_cast<__half2*>(&lo), h2 = *reinterpret_cast<__half2*>(&hi);
-          x[4 * k + 0] = __low2float(l2);
-          x[4 * k + 1] = __high2float(l2);
-          x[4 * k + 2] = __low2float(h2);
-          x[4 * k + 3] = __high2float(h2);
-        }
-        qsc = p.q_scale_per_row ? p.q_scale[row * p.Hq + h] : p.q_scale[0];
+        for (int j = 0; j < EPL / 4; ++j) q.w[k][j] = src[j];
+        q.qsc[k] = p.q_scale_per_row ? p.q_scale[row * p.Hq + h] : p.q_scale[0];
       } else {
-        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(p.q) + off;
+        const uint32_t* src =
+            reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + off);
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) x[k] = __bfloat162float(src[k]);
+        for (int j = 0; j < QRaw<C>::NW; ++j) q.w[k][j] = src[j];
       }
-      crv = p.scale_log2 * qsc;
+    }
+  }
+}
+
+// Converts a task's query words into shared memory, with the per-row logit factor
+// (softmax scale * log2 e * q scale * row normalisation * k scale).
+template <class C>
+__device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C>& q, int cw,
+                              int lane, float k_scale_tensor) {
+  uint16_t* qs = reinterpret_cast<uint16_t*>(smem + C::OFF_Q);
+  float* cr = reinterpret_cast<float*>(smem + C::OFF_CR);
+  constexpr int EPL = QRaw<C>::EPL;
+#pragma unroll
+  for (int k = 0; k < QRaw<C>::ROWS; ++k) {
+    const int r = cw + k * C::NCW;
+    if (r >= C::RPAD) break;
+    float x[EPL];
+    float crv = 0.f;
+    if (r < p.R) {
+      if (p.q_fp8) {
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j) {
+          uint32_t lo = e4m3x2_to_f16x2(q.w[k][j] & 0xFFFF), hi = e4m3x2_to_f16x2(q.w[k][j] >> 16);
+          __half2 l2 = *reinterpret_cast<__half2*>(&lo), h2 = *reinterpret_cast<__half2*>(&hi);
+          x[4 * j + 0] = __low2float(l2);
+          x[4 * j + 1] = __high2float(l2);
+          x[4 * j + 2] = __low2float(h2);
+          x[4 * j + 3] = __high2float(h2);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < QRaw<C>::NW; ++j) {  // bf16 pair: low half first
+          x[2 * j] = __uint_as_float(q.w[k][j] << 16);
+          x[2 * j + 1] = __uint_as_float(q.w[k][j] & 0xFFFF0000u);
+        }
+      }
+      crv = p.scale_log2 * q.qsc[k];
       if constexpr (C::KIND == KIND_FP8) {
         if (p.scale_kind == SK_TENSOR) crv *= k_scale_tensor;
       }
@@ -209,7 +251,7 @@ __device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int
         // f16 operands: bring the row's largest magnitude into [256, 512) by a power of 2.
         float amax = 0.f;
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) amax = fmaxf(amax, fabsf(x[k]));
+        for (int j = 0; j < EPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
 #pragma unroll
         for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         int kx = 0;
@@ -219,18 +261,18 @@ __device__ void load_q(const DecodeParams& p, uint8_t* smem, int s, int hkv, int
         }
         const float down = exp2i(-kx);
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) x[k] *= down;
+        for (int j = 0; j < EPL; ++j) x[j] *= down;
         crv *= exp2i(kx);
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < EPL; ++k) x[k] = 0.f;
+      for (int j = 0; j < EPL; ++j) x[j] = 0.f;
     }
     uint16_t* dst = qs + r * C::D + lane * EPL;
 #pragma unroll
-    for (int k = 0; k < EPL; k += 2) {
-      const uint32_t v = C::KIND == KIND_BF16 ? pack_bf16x2(x[k], x[k + 1]) : pack_f16x2(x[k], x[k + 1]);
-      *reinterpret_cast<uint32_t*>(dst + k) = v;
+    for (int j = 0; j < EPL; j += 2) {
+      const uint32_t v = C::KIND == KIND_BF16 ? pack_bf16x2(x[j], x[j + 1]) : pack_f16x2(x[j], x[j + 1]);
+      *reinterpret_cast<uint32_t*>(dst + j) = v;
     }
     if (lane == 0) cr[r] = crv;
   }
@@ -795,6 +837,13 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     }
   }
 
+  QRaw<C> qn;  // query words of the next task to start
+  if constexpr (C::Q_EARLY) {
+    if (t_begin < t_end) {
+      const PlanTask tk0 = p.tasks[t_begin];
+      load_q_issue<C>(p, tk0.seq, tk0.hkv_part & 0xFFFF, cw, lane, qn);
+    }
+  }
   // prologue: fill the ring
   SliceIt ld;
   ld.task = t_begin;
@@ -827,8 +876,14 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     const int nparts = p.nparts[unit];
     const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
 
-    load_q<C>(p, smem, s, hkv, cw, lane, k_scale_tensor);
+    if constexpr (!C::Q_EARLY) load_q_issue<C>(p, s, hkv, cw, lane, qn);
+    load_q_finish<C>(p, smem, qn, cw, lane, k_scale_tensor);
     named_bar(BAR_CONSUMERS, C::NCW * 32);
+    // The next task's record, read at this task's merge, copied without waiting for it.
+    if (C::Q_EARLY && task + 1 < t_end && cw == 0 && lane == 0) {
+      cp_async16(smem + C::OFF_NXT, p.tasks + task + 1);
+      cp_async_commit();
+    }
     // Touch this task's output rows now, so that their address translation is not first
     // needed by the stores at the end of the task, with the memory system under load.
     if (cw == 0 && lane == 0) {
@@ -904,6 +959,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     }
 
     // ---------------- merge the token groups (fixed order) and store ----------------
+    if (C::Q_EARLY && task + 1 < t_end && cw == 0 && lane == 0) cp_async_wait_all();
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
@@ -915,6 +971,12 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         if (dw == 0 && t == 0) ml[tg * C::RPAD + 16 * mt + g + 8 * hr] = make_float2(A.m[mt][hr], l);
       }
     named_bar(BAR_CONSUMERS, C::NCW * 32);
+    if constexpr (C::Q_EARLY) {  // the next task's query rows load while this one merges
+      if (task + 1 < t_end) {
+        const PlanTask tn = *reinterpret_cast<const PlanTask*>(smem + C::OFF_NXT);
+        load_q_issue<C>(p, tn.seq, tn.hkv_part & 0xFFFF, cw, lane, qn);
+      }
+    }
     float fac[C::MT][2], Mrow[C::MT][2], Lrow[C::MT][2];
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt)
@@ -945,44 +1007,71 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         bfac[b] = C::TOK_SCALE ? A.vref : v_scale_tensor;
       }
     }
-    // The groups add their scaled accumulators, one group at a time, into a buffer kept in
-    // fragment order (each lane owns float4 columns: no bank conflicts); the last group
-    // also leaves 1 / sum per row.  Then all threads store the rows, 4 consecutive head
-    // dims each, with coalesced writes.
+    // The token groups' scaled accumulators are summed in group order into a buffer kept
+    // in fragment order (each lane owns float4 columns: no bank conflicts): for the last
+    // task of the chunk all groups write to the idle load ring at once and every thread
+    // sums one column over the groups; otherwise the groups add in, one at a time.  Then
+    // all threads store the rows, 4 consecutive head dims each, with coalesced writes.
     float4* ob4 = reinterpret_cast<float4*>(obuf) + dw * (C::MT * C::NTD * 32) + lane;
     float* fin = reinterpret_cast<float*>(smem + C::OFF_FIN);
+    if (tg == C::NTG - 1 && dw == 0 && t == 0) {
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = 16 * mt + g + 8 * hr;
+          fin[row] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
+          if (nparts > 1 && row < p.R)
+            reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] =
+                make_float2(Mrow[mt][hr], Lrow[mt][hr]);
+        }
+    }
+    if (C::PAR_MERGE && task + 1 == t_end && !*abort_flag) {
+      constexpr int NF = C::NDW * C::MT * C::NTD * 32;  // float4 per token group
+      float4* all = reinterpret_cast<float4*>(smem + C::OFF_RING);
+      float4* mine = all + tg * NF + dw * (C::MT * C::NTD * 32) + lane;
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < C::NTD; ++n) {
+          const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
+          const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
+          mine[(mt * C::NTD + n) * 32] = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0,
+                                                     A.o[mt][n][2] * f1, A.o[mt][n][3] * f1);
+        }
+      named_bar(BAR_CONSUMERS, C::NCW * 32);
+      for (int f = cw * 32 + lane; f < NF; f += C::NTHREADS) {
+        float4 a = all[f];
+#pragma unroll
+        for (int i = 1; i < C::NTG; ++i) {
+          const float4 b = all[i * NF + f];
+          a = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        }
+        reinterpret_cast<float4*>(obuf)[f] = a;
+      }
+      named_bar(BAR_CONSUMERS, C::NCW * 32);
+    } else {
 #pragma unroll 1
-    for (int i = 0; i < C::NTG; ++i) {
-      if (tg == i) {
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-          for (int n = 0; n < C::NTD; ++n) {
-            const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
-            const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
-            float4 v = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0, A.o[mt][n][2] * f1,
-                                   A.o[mt][n][3] * f1);
-            float4* dst = ob4 + (mt * C::NTD + n) * 32;
-            if (i > 0) {
-              const float4 w = *dst;
-              v = make_float4(w.x + v.x, w.y + v.y, w.z + v.z, w.w + v.w);
-            }
-            *dst = v;
-          }
-        if (i == C::NTG - 1 && dw == 0 && t == 0) {
+      for (int i = 0; i < C::NTG; ++i) {
+        if (tg == i) {
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int row = 16 * mt + g + 8 * hr;
-              fin[row] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
-              if (nparts > 1 && row < p.R)
-                reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] =
-                    make_float2(Mrow[mt][hr], Lrow[mt][hr]);
+            for (int n = 0; n < C::NTD; ++n) {
+              const float bb = C::KIND == KIND_FP4 ? bfac[n >> 2] : bfac[0];
+              const float f0 = fac[mt][0] * bb, f1 = fac[mt][1] * bb;
+              float4 v = make_float4(A.o[mt][n][0] * f0, A.o[mt][n][1] * f0,
+                                     A.o[mt][n][2] * f1, A.o[mt][n][3] * f1);
+              float4* dst = ob4 + (mt * C::NTD + n) * 32;
+              if (i > 0) {
+                const float4 w = *dst;
+                v = make_float4(w.x + v.x, w.y + v.y, w.z + v.z, w.w + v.w);
+              }
+              *dst = v;
             }
         }
+        named_bar(BAR_CONSUMERS, C::NCW * 32);
       }
-      named_bar(BAR_CONSUMERS, C::NCW * 32);
     }
     {
       constexpr int Q4 = C::D / 4;

@@ -1,10 +1,12 @@
 """The work split that pa_decode_plan builds, restated on the host for tests.
 
 Units are (sequence, KV head) pairs in sequence-major order, each with ceil(L/256)
-tiles.  All units' tiles, laid end to end, are cut into `budget` chunks of C tiles
-(C = ceil(total / budget), raised when needed so that no unit touches more than
-max_partitions chunks); a unit becomes one partition per chunk it touches.  With
-max_partitions 1, or an empty unit, the unit is one task in the chunk it starts in.
+tiles.  The units are laid end to end on a line, each as a gap of UNIT_COST positions
+(the fixed cost of a task) followed by its tiles, and the line is cut into `budget`
+chunks of C positions (C = ceil(length / budget), raised when needed so that no unit
+touches more than max_partitions chunks); a unit becomes one partition per chunk its
+tiles touch.  With max_partitions 1, or an empty unit, the unit is one task in the
+chunk its tiles start in.
 
 The workspace layout mirrors the library's (256-byte aligned regions): status word and
 task count, then nparts, part_base, counters (int32 per unit), tasks (4 x int32 per
@@ -15,24 +17,27 @@ import math
 import numpy as np
 
 TILE = 256
+UNIT_COST = 2  # line positions charged per unit before its tiles
 
 
 def _align(x, a=256):
     return (x + a - 1) // a * a
 
 
-def plan(context_lens, hkv, budget, max_partitions, cap_tokens):
+def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_COST):
     tiles = [(min(max(int(L), 0), cap_tokens) + TILE - 1) // TILE for L in context_lens]
-    total = sum(tiles) * hkv
+    total = (sum(tiles) + unit_cost * len(tiles)) * hkv  # length of the line
     maxt = max(tiles, default=0)
     C = max(1, -(-total // budget))
     if max_partitions >= 2 and maxt > 0:
         C = max(C, (maxt - 1) // (max_partitions - 1) + 1)
     nchunks = -(-total // C) if total > 0 else 1
-    tasks, chunks, nparts, part_base = [], [], [], []
+    tasks, chunks, nparts, part_base, unit_pos = [], [], [], [], []
     U, slot = 0, 0
     for s, n in enumerate(tiles):
         for h in range(hkv):
+            U += unit_cost  # the unit's gap; its first tile sits at U
+            unit_pos.append(U)
             if n == 0 or max_partitions < 2:
                 pieces = [(0, n, min(U // C, nchunks - 1))]
             else:
@@ -53,7 +58,8 @@ def plan(context_lens, hkv, budget, max_partitions, cap_tokens):
             first[k] = t
         prev = c
     return {"tiles": tiles, "C": C, "nchunks": nchunks, "tasks": tasks, "chunks": chunks,
-            "nparts": nparts, "part_base": part_base, "chunk_first": first, "slots": slot}
+            "nparts": nparts, "part_base": part_base, "chunk_first": first, "slots": slot,
+            "length": total, "unit_pos": unit_pos, "hkv": hkv, "unit_cost": unit_cost}
 
 
 def capacity(batch, hkv, budget):
@@ -87,6 +93,17 @@ def chunk_tiles(model):
     out = np.zeros(len(model["chunk_first"]) - 1, dtype=np.int64)
     for (s, hp, b, e), c in zip(model["tasks"], model["chunks"]):
         out[c] += e - b
+    return out
+
+
+def chunk_load(model):
+    """Line positions (tiles and unit gaps) inside each chunk's range."""
+    C, w = model["C"], model["unit_cost"]
+    out = np.zeros(len(model["chunk_first"]) - 1, dtype=np.int64)
+    for c in range(len(out)):
+        lo, hi = c * C, min((c + 1) * C, model["length"])
+        if hi > lo:
+            out[c] = hi - lo
     return out
 
 

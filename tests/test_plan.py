@@ -54,26 +54,43 @@ def test_plan_arithmetic(name, lens, hkv, budget, maxp):
     assert first[-1] == len(m["tasks"]) and all(a <= b for a, b in zip(first, first[1:]))
     for c in range(budget):
         assert all(m["chunks"][t] == c for t in range(first[c], first[c + 1]))
-    # balance: with splitting on, no chunk runs more than C tiles and all but the last
-    # non-empty chunk run exactly C
+    # balance: with splitting on, every task's tiles lie inside its chunk's range of the
+    # line (each unit is a gap of UNIT_COST followed by its tiles), so no chunk runs more
+    # than C tiles, and every chunk but the last covers exactly C positions
     if maxp >= 2:
+        C = m["C"]
+        unit_of = {}
+        for u, pos in enumerate(m["unit_pos"]):
+            unit_of[(u // hkv, u % hkv)] = pos
+        for (s, hp, b, e), c in zip(m["tasks"], m["chunks"]):
+            if e > b:
+                pos = unit_of[(s, hp & 0xFFFF)]
+                assert c * C <= pos + b and pos + e <= (c + 1) * C
         per = pm.chunk_tiles(m)
-        assert per.max(initial=0) <= m["C"]
+        assert per.max(initial=0) <= C
         assert m["nchunks"] <= budget
-        full = per[: m["nchunks"] - 1]
-        assert np.all(full == m["C"])
+        load = pm.chunk_load(m)
+        assert np.all(load[: m["nchunks"] - 1] == C)
+        assert m["length"] == (sum(tiles) + pm.UNIT_COST * len(tiles)) * hkv
         if sum(tiles) > 0:
-            assert m["C"] == max(pm.ceil_div(sum(tiles) * hkv, budget),
-                                 (max(tiles) - 1) // (maxp - 1) + 1)
+            assert C == max(pm.ceil_div(m["length"], budget), (max(tiles) - 1) // (maxp - 1) + 1)
 
 
 def test_plan_balance_long_context():
-    # 16 long sequences over 152 CTAs: the busiest CTA runs at most one tile more than
-    # the mean (the proportional split it replaces left ~10% of the GPU idle)
+    # 16 long sequences over 152 CTAs: counting each task start at UNIT_COST tiles, the
+    # busiest CTA runs at most one tile more than the mean (the proportional split this
+    # replaces left ~10% of the GPU idle), and a CTA that finishes one sequence and starts
+    # the next runs UNIT_COST tiles fewer than one inside a sequence
     lens = MIXES[0][1]
     m = pm.plan(lens, 1, 152, 128, 1 << 20)
     per = pm.chunk_tiles(m)
-    assert per.max() - per.sum() / 152 <= 1.0
+    starts = np.zeros_like(per)
+    for (s, hp, b, e), c in zip(m["tasks"], m["chunks"]):
+        starts[c] += 1
+    work = per + pm.UNIT_COST * (starts - 1)
+    assert work.max() - work.sum() / 152 <= 1.0
+    two = per[starts == 2]
+    assert len(two) > 0 and two.max() <= m["C"] - pm.UNIT_COST
 
 
 @pytest.mark.gpu
