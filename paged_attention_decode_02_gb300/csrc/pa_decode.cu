@@ -104,15 +104,17 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   __shared__ long long sh64[32];
   __shared__ int sh32[32];
   __shared__ int sh32b[32];
-  __shared__ int shmax;
+  __shared__ int shmax, shclamp;
   __shared__ int sh_last[1024];  // chunk of each thread's last task in the current round
   const int tid = threadIdx.x;
   const int cap = pp.W * pp.S;
-  pdl_wait_prior();          // the previous kernel may still read this workspace
+  // Until the first write this kernel only reads the context lengths, which no kernel of
+  // this library writes: it runs that part while the previous kernel in the stream
+  // finishes (that kernel may still read this workspace), and waits before writing.
   pdl_launch_dependents();  // the tile kernel may launch now; it waits for this grid
   if (tid == 0) {
-    *pp.status = 0;
     shmax = 0;
+    shclamp = 0;
   }
   __syncthreads();
   int clamped = 0, lmax = 0, n_own = 0;  // n_own: tiles of sequence tid (one round of sequences)
@@ -124,15 +126,13 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     lmax = n > lmax ? n : lmax;
   }
   if (lmax > 0) atomicMax(&shmax, lmax);
-  if (clamped) atomicOr(pp.status, ST_CLAMPED);
+  if (clamped) atomicOr(&shclamp, 1);
   long long seq_tiles;
   (void)block_exclusive_scan<long long>(local, &seq_tiles, sh64);  // also orders shmax
   const int w = kUnitCostTiles;
   long long T64 = (seq_tiles + (long long)w * pp.B) * pp.Hkv;  // length of the line
-  if (T64 > 0x7FFFFFFFll) {  // beyond the plan's range (2^31 tiles): flag it, results undefined
-    if (tid == 0) atomicOr(pp.status, ST_CLAMPED);
-    T64 = 0x7FFFFFFFll;
-  }
+  const bool overflow = T64 > 0x7FFFFFFFll;  // beyond the plan's range: flagged, results undefined
+  if (overflow) T64 = 0x7FFFFFFFll;
   const uint32_t T = (uint32_t)T64;
   ChunkGrid cg;
   cg.maxp = pp.max_partitions;
@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     int tot_t, tot_s;
     const int off_t = block_exclusive_scan<int>(ntask, &tot_t, sh32);  // its syncs order sh_last
     const int off_s = block_exclusive_scan<int>(nslot, &tot_s, sh32b);
+    if (base == 0) {  // first write: the previous kernel is done with the workspace
+      pdl_wait_prior();
+      if (tid == 0) *pp.status = (shclamp || overflow) ? ST_CLAMPED : ST_OK;
+    }
     if (s < pp.B) {
       int t = carry_tasks + off_t, slot = carry_slots + off_s;
       // tasks are in unit order, hence in non-decreasing chunk order: chunk c runs tasks
@@ -215,22 +219,37 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   __shared__ float wsh[8][128];  // normalised partition weights of each warp's row
-  pdl_wait_prior();  // the tile kernel's partials are complete and visible from here on
   pdl_launch_dependents();  // a following plan may launch; it waits before writing
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long long row = (long long)blockIdx.x * 8 + wid;
   const long long rows = (long long)rp.B * rp.qlen * rp.Hq;
-  if (row >= rows) return;
-  const int s = (int)(row / ((long long)rp.qlen * rp.Hq));
-  const int rem = (int)(row % ((long long)rp.qlen * rp.Hq));
-  const int i = rem / rp.Hq, h = rem % rp.Hq, hkv = h / rp.G;
-  const int u = s * rp.Hkv + hkv;
-  const int P = rp.nparts[u];
+  // The partition counts and bases come from the plan, which completed before the tile
+  // kernel (the grid this one follows) let it launch: they are read before the wait.
+  int P = 0;
+  long long base = 0;
+  int s = 0, i = 0, h = 0;
+  if (row < rows) {
+    s = (int)(row / ((long long)rp.qlen * rp.Hq));
+    const int rem = (int)(row % ((long long)rp.qlen * rp.Hq));
+    i = rem / rp.Hq;
+    h = rem % rp.Hq;
+    const int u = s * rp.Hkv + h / rp.G;
+    P = __ldcg(rp.nparts + u);  // through L2: no line cached in L1 by an earlier grid
+    base = __ldcg(rp.part_base + u);
+  }
+  pdl_wait_prior();  // the tile kernel's partials are complete and visible from here on
   if (P < 2) return;
   const int r = i * rp.G + h % rp.G;
-  const long long base = rp.part_base[u];
   const float2* ml = reinterpret_cast<const float2*>(rp.part_ml);
   float* w = wsh[wid];
+  // The first partials' outputs load together with the (max, sum) pairs.
+  constexpr int PRE = 8;
+  float4 pre[PRE];
+  if (rp.D == 128) {
+#pragma unroll
+    for (int q = 0; q < PRE; ++q)
+      if (q < P) pre[q] = *reinterpret_cast<const float4*>(rp.part_o + ((base + q) * rp.R + r) * 128 + 4 * lane);
+  }
   // M and the weights: lanes over partitions, then a fixed shuffle tree
   float M = -INFINITY;
   for (int q = lane; q < P; q += 32) M = fmaxf(M, ml[(base + q) * rp.R + r].x);
@@ -254,6 +273,17 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   for (int d0 = 4 * lane; d0 < rp.D; d0 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int q = 0;
+    if (rp.D == 128) {
+#pragma unroll
+      for (int k = 0; k < PRE; ++k)
+        if (k < P) {
+          acc.x += w[k] * pre[k].x;
+          acc.y += w[k] * pre[k].y;
+          acc.z += w[k] * pre[k].z;
+          acc.w += w[k] * pre[k].w;
+        }
+      q = P < PRE ? P : PRE;
+    }
     for (; q + 4 <= P; q += 4) {
       float4 v[4];
 #pragma unroll
@@ -274,10 +304,7 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
       acc.z += w[q] * v.z;
       acc.w += w[q] * v.w;
     }
-    dst[d0] = __float2bfloat16_rn(acc.x);
-    dst[d0 + 1] = __float2bfloat16_rn(acc.y);
-    dst[d0 + 2] = __float2bfloat16_rn(acc.z);
-    dst[d0 + 3] = __float2bfloat16_rn(acc.w);
+    *reinterpret_cast<uint2*>(dst + d0) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
 }
 

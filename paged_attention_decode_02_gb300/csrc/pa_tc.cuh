@@ -990,8 +990,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  pdl_launch_dependents();  // the reduce kernel may launch; it waits for this grid's results
   pdl_wait_prior();         // the plan's task list is complete and visible from here on
+  pdl_launch_dependents();  // the reduce kernel may launch (after the plan completed); it
+                            // waits for this grid's results
   const int tb = p.chunk_first[blockIdx.x], te = p.chunk_first[blockIdx.x + 1];
   if (warp == 0) {
     tc_producer<C>(p, &tmk, &tmv, sm, bars, abort_flag, tb, te, lane);

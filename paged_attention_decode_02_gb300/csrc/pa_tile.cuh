@@ -1189,8 +1189,9 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_launch_dependents();  // the reduce kernel may launch; it waits for this grid's results
   pdl_wait_prior();         // the plan's task list is complete and visible from here on
+  pdl_launch_dependents();  // the reduce kernel may launch (after the plan completed); it
+                            // waits for this grid's results
   const int t_begin = p.chunk_first[blockIdx.x], t_end = p.chunk_first[blockIdx.x + 1];
   warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, t_begin, t_end, threadIdx.x >> 5,
                threadIdx.x & 31);
