@@ -145,13 +145,20 @@ size_t pa_decode_workspace_size(const pa_decode_args* args);
 pa_status pa_decode_validate(const pa_decode_args* args);
 
 /* Builds the tile/partition work list on the device from context_lens: ceil(L/256)
- * tiles per (sequence, KV head) unit; all units' tiles, laid end to end, are cut into
+ * tiles per (sequence, KV head) unit; the units are laid end to end, each as a gap of
+ * two tiles (a task's fixed cost) followed by its tiles, and the line is cut into
  * task_budget chunks of equal length (one per tile-kernel CTA), longer when needed so
  * that no unit touches more than max_partitions chunks.  A unit crossing chunk
  * boundaries becomes one partition per chunk it touches; with max_partitions 1 each
  * unit is one task, run by the chunk it starts in.  Clears the device status word.  One
  * launch, 1 CTA.  ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit messages: planned tasks,
- * direct output with one partition, tasks from a CU budget.) */
+ * direct output with one partition, tasks from a CU budget.)
+ * All launches of this library use programmatic dependent launch: a kernel may begin
+ * before the previous kernel in the stream has finished when that kernel allows it (this
+ * library's kernels do; others do only if they execute griddepcontrol.launch_dependents).
+ * Each kernel waits for its predecessor before touching the workspace or the output, but
+ * the plan reads context_lens before that wait: a kernel that writes context_lens and
+ * allows early launch must do so before it allows it. */
 pa_status pa_decode_plan(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                          void* stream);
 
