@@ -71,7 +71,7 @@ struct TileCfg {
   static constexpr int OFF_OB = OFF_X + X_BYTES;
   static constexpr int OFF_ML = OFF_OB + RPAD * D * 4;
   static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;  // 1 / sum per row
-  static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 6 : 0;  // e8m0 factor tables
+  static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 2 : 0;  // V e8m0 factor table
   static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
   static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
   static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
@@ -442,10 +442,9 @@ __device__ __forceinline__ void stage_compute(
   const float* vsc = reinterpret_cast<const float*>(sc + 4 * C::TW);
   const uint32_t* kex = reinterpret_cast<const uint32_t*>(sc);
   const uint32_t* vex = reinterpret_cast<const uint32_t*>(sc + 4 * C::TW);
-  float* ktab = reinterpret_cast<float*>(smem + C::OFF_TAB + cw * C::TAB_BYTES);
-  uint16_t* vtab = reinterpret_cast<uint16_t*>(ktab + C::NBLK * C::TW);
+  uint16_t* vtab = reinterpret_cast<uint16_t*>(smem + C::OFF_TAB + cw * C::TAB_BYTES);
 
-  // ---------------- V-scale references (lazy) and MXFP4 factor tables ----------------
+  // ---------------- fp8 per-token V-scale reference (lazy) ----------------
   float beta[C::NBLK];
 #pragma unroll
   for (int b = 0; b < C::NBLK; ++b) beta[b] = 1.f;
@@ -453,10 +452,12 @@ __device__ __forceinline__ void stage_compute(
   float vinv = 1.f;
   if constexpr (tok_scale) {
     static_assert(C::TW <= 32, "one lane per slice token");
-    // |v_scale| of owned tokens; non-negative floats order like their bit patterns
+    // |v_scale| of owned tokens; non-negative floats order like their bit patterns.  The
+    // reference moves only when a token passes it by more than kLazyVref: one vote decides,
+    // the maximum is reduced only then.
     const float vs = (lane < C::TW && (!MASKED || lane < vw)) ? fabsf(vsc[lane]) : 0.f;
-    const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs)));
-    if (mx > A.vref * kLazyVref) {  // warp-uniform
+    if (__any_sync(0xffffffffu, vs > A.vref * kLazyVref)) {
+      const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs)));
       beta[0] = A.vref / mx;
       A.vref = mx;
       A.vinv = 1.f / mx;
@@ -464,40 +465,6 @@ __device__ __forceinline__ void stage_compute(
     }
     vinv = A.vinv;
   }
-  if constexpr (C::KIND == KIND_FP4) {
-    const bool own = !MASKED || lane < vw;  // one lane per slice token
-    const uint32_t kw = kex[lane], vwd = vex[lane];
-    int cm[C::NBLK];
-#pragma unroll
-    for (int b = 0; b < C::NBLK; ++b) {
-      const uint32_t e = (vwd >> (8 * b)) & 0xFF;
-      cm[b] = (int)__reduce_max_sync(0xffffffffu, own ? e : 0u);
-    }
-    bool need = false;
-#pragma unroll
-    for (int b = 0; b < C::NBLK; ++b) need |= A.emax[b] < 0 || cm[b] > A.emax[b] + kLazyExp;
-    if (need) {
-#pragma unroll
-      for (int b = 0; b < C::NBLK; ++b) {
-        const int ne = max(A.emax[b], cm[b]);
-        beta[b] = A.emax[b] < 0 ? 0.f : exp2i(A.emax[b] - ne);
-        A.emax[b] = ne;
-      }
-      rescale_v = true;
-    }
-    // K: 2^(e-127) as fp32; V: 2^(e-emax) as f16 (factors below 2^-14 flush to zero: such
-    // a block is at least 2^14 times smaller than the largest one seen for that block)
-    const uint32_t kown = own ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-    for (int b = 0; b < C::NBLK; ++b) {
-      const uint32_t ek = (kw >> (8 * b)) & 0xFF;
-      const int ev = (int)((vwd >> (8 * b)) & 0xFF);
-      ktab[b * C::TW + lane] = __uint_as_float((ek << 23) & kown);
-      vtab[b * C::TW + lane] = (uint16_t)(((uint32_t)max(ev - A.emax[b] + 15, 0) << 10) & kown);
-    }
-    __syncwarp();
-  }
-
   // ---------------- S = Q K^T over this warp's dims ----------------
   float sacc[C::MT][C::NT][4];
   // fp8 with one m-tile: odd k-chunks accumulate separately (two independent MMA chains
@@ -556,6 +523,11 @@ __device__ __forceinline__ void stage_compute(
           }
         }
     } else {
+      // K block factors 2^(e-127) of the lane's tokens 8nt + 2t and 8nt + 2t + 1, from the
+      // raw e8m0 words (unowned tokens' scores are overwritten by the boundary mask)
+      uint2 kw[C::NT];
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt) kw[nt] = *reinterpret_cast<const uint2*>(kex + 8 * nt + 2 * t);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         float tmp[C::MT][C::NT][4];
@@ -570,7 +542,8 @@ __device__ __forceinline__ void stage_compute(
         }
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
-          const float2 kf = *reinterpret_cast<const float2*>(ktab + b * C::TW + 8 * nt + 2 * t);
+          const float2 kf = make_float2(__uint_as_float(((kw[nt].x >> (8 * b)) & 0xFFu) << 23),
+                                        __uint_as_float(((kw[nt].y >> (8 * b)) & 0xFFu) << 23));
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt) {
             sacc[mt][nt][0] = fmaf(tmp[mt][nt][0], kf.x, sacc[mt][nt][0]);
@@ -611,6 +584,38 @@ __device__ __forceinline__ void stage_compute(
         }
     xbuf ^= 1;
   }
+  // ---------------- MXFP4 V references (lazy) and factor table ----------------
+  if constexpr (C::KIND == KIND_FP4) {
+    const bool own = !MASKED || lane < vw;  // one lane per slice token
+    const uint32_t vwd = vex[lane];
+    // A reference moves when none is set yet or a token's exponent passes it by more than
+    // kLazyExp: one vote decides; the block maxima are reduced only then.
+    bool over = false;
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b)
+      over |= A.emax[b] < 0 || (own && (int)((vwd >> (8 * b)) & 0xFF) > A.emax[b] + kLazyExp);
+    if (__any_sync(0xffffffffu, over)) {
+#pragma unroll
+      for (int b = 0; b < C::NBLK; ++b) {
+        const uint32_t e = (vwd >> (8 * b)) & 0xFF;
+        const int cm = (int)__reduce_max_sync(0xffffffffu, own ? e : 0u);
+        const int ne = max(A.emax[b], cm);
+        beta[b] = A.emax[b] < 0 ? 0.f : exp2i(A.emax[b] - ne);
+        A.emax[b] = ne;
+      }
+      rescale_v = true;
+    }
+    // V: 2^(e-emax) as f16 (factors below 2^-14 flush to zero: such a block is at least
+    // 2^14 times smaller than the largest one seen for that block); 0 for unowned tokens
+    const uint32_t kown = own ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b) {
+      const int ev = (int)((vwd >> (8 * b)) & 0xFF);
+      vtab[b * C::TW + lane] = (uint16_t)(((uint32_t)max(ev - A.emax[b] + 15, 0) << 10) & kown);
+    }
+    __syncwarp();
+  }
+
   // ---------------- logits and boundary mask ----------------
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
