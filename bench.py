@@ -166,22 +166,37 @@ def per_config(device, peak, calls=10, warmup=3):
         ws = ops.alloc_workspace(args, device)
         for _ in range(warmup):
             ops.pa_decode_run(args, ws, stream)
-        ts = []
+        # the same call captured once in a CUDA graph (how a serving loop issues it)
+        gs = torch.cuda.Stream(device)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            ops.pa_decode_run(args, ws, gs)
+            with torch.cuda.graph(graph, stream=gs):
+                ops.pa_decode_run(args, ws, gs)
+        stream.wait_stream(gs)
+        torch.cuda.synchronize()
+        ts, tg = [], []
         for _ in range(calls):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            ops.pa_decode_run(args, ws, stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
+            for launch, acc in ((lambda: ops.pa_decode_run(args, ws, stream), ts),
+                                (graph.replay, tg)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                acc.append(e0.elapsed_time(e1))
         assert ops.pa_decode_read_status(ws) == 0, case.name
         nbytes = synth.algorithmic_bytes(case, p["context_lens"].cpu().tolist())
-        med = statistics.median(ts)
+        med, medg = statistics.median(ts), statistics.median(tg)
         name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
-        res[name] = {"us_per_call": round(med * 1e3, 2), "algorithmic_bytes": nbytes,
+        res[name] = {"us_per_call": round(med * 1e3, 2),
+                     "us_per_call_graph": round(medg * 1e3, 2), "algorithmic_bytes": nbytes,
                      "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
+                     "GBps_graph": round(nbytes / (medg * 1e-3) / 1e9, 1),
                      "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
+        del graph
         del p, out, ws
     del flush
     torch.cuda.empty_cache()

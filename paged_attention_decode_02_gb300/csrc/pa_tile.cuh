@@ -171,6 +171,12 @@ __device__ __forceinline__ float exp2i(int k) {
   return k < -126 ? 0.f : __int_as_float((k + 127) << 23);
 }
 
+// MXFP4 K block factors are applied as 2^(e - 127 - 17): a 32-dim partial score of the
+// normalised query (|q| < 512, |k| <= 6) stays below 2^17, so the scaled partial stays finite
+// for every exponent byte up to 254 (P2 reports logits going to inf at byte 249 when the
+// factor is applied unbiased); 2^17 moves into the row's logit factor.
+constexpr float kKFactorBias = 1.f / 131072.f;
+
 // The query words a lane reads for its rows of one task: loaded ahead of their use
 // (before the ring is first filled, or while the previous task merges) and converted
 // when the task starts.
@@ -263,6 +269,7 @@ __device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C
 #pragma unroll
         for (int j = 0; j < EPL; ++j) x[j] *= down;
         crv *= exp2i(kx);
+        if constexpr (C::KIND == KIND_FP4) crv *= 1.f / kKFactorBias;
       }
     } else {
 #pragma unroll
@@ -524,7 +531,8 @@ __device__ __forceinline__ void stage_compute(
         }
     } else {
       // K block factors 2^(e-127) of the lane's tokens 8nt + 2t and 8nt + 2t + 1, from the
-      // raw e8m0 words (unowned tokens' scores are overwritten by the boundary mask)
+      // raw e8m0 words (unowned tokens' scores are overwritten by the boundary mask), times
+      // kKFactorBias (the row's logit factor carries the inverse)
       uint2 kw[C::NT];
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt) kw[nt] = *reinterpret_cast<const uint2*>(kex + 8 * nt + 2 * t);
@@ -542,8 +550,8 @@ __device__ __forceinline__ void stage_compute(
         }
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
-          const float2 kf = make_float2(__uint_as_float(((kw[nt].x >> (8 * b)) & 0xFFu) << 23),
-                                        __uint_as_float(((kw[nt].y >> (8 * b)) & 0xFFu) << 23));
+          const float2 kf = make_float2(__uint_as_float(((kw[nt].x >> (8 * b)) & 0xFFu) << 23) * kKFactorBias,
+                                        __uint_as_float(((kw[nt].y >> (8 * b)) & 0xFFu) << 23) * kKFactorBias);
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt) {
             sacc[mt][nt][0] = fmaf(tmp[mt][nt][0], kf.x, sacc[mt][nt][0]);

@@ -49,6 +49,7 @@ class Case:
     tensor_scale: float = 0.05   # fp8 per-tensor k_scale = v_scale
     token_scale: tuple = (0.01, 0.1)
     e8m0_range: tuple = (120, 130)
+    k_e8m0_range: Optional[tuple] = None  # MXFP4 K exponents, when they differ from V's
     pad_columns: int = 2
     extra_blocks: int = 0
     # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and
@@ -216,9 +217,10 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
         kc = torch.randint(0, 256, (NB, Hkv, S, rb), generator=g, dtype=torch.int32).to(torch.uint8)
         vc = torch.randint(0, 256, (NB, Hkv, S, rb), generator=g, dtype=torch.int32).to(torch.uint8)
         caches = [kc, vc]
-        lo, hi = case.e8m0_range
+        lo, hi = case.k_e8m0_range or case.e8m0_range
         key_scale = torch.randint(lo, hi + 1, (NB, Hkv, S, D // 32), generator=g,
                                   dtype=torch.int32).to(torch.uint8)
+        lo, hi = case.e8m0_range
         value_scale = torch.randint(lo, hi + 1, (NB, Hkv, S, D // 32), generator=g,
                                     dtype=torch.int32).to(torch.uint8)
 

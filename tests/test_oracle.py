@@ -223,6 +223,27 @@ def test_context_one_returns_that_v_row(kv):
             assert np.array_equal(got[s, 0, h], V[blk, h // 2, 0].numpy())
 
 
+def test_huge_k_exponents_select_the_top_token():
+    # e8m0 K bytes up to 249 (P2: the byte that sent the logits to inf): the logits lie
+    # ~2^120 apart, so the softmax is one-hot and each output row is exactly the V row of
+    # the token with the largest q.k, found here on the dense dequantised cache
+    case = synth.Case("k249", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=2, qlen=1,
+                      num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
+                      context_lens=[37, 70], seed=31, k_e8m0_range=(236, 249))
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    K, V, Q = _dequant_dense(p, "k"), _dequant_dense(p, "v"), _query_dense(p)
+    bt = p["block_tables"].cpu()
+    for s, L in enumerate([37, 70]):
+        rows = [(int(bt[s, t // 16]), t % 16) for t in range(L)]
+        keys = torch.stack([K[b, 0, r] for b, r in rows])
+        for h in range(4):
+            top = int(torch.argmax(keys @ Q.reshape(2, 4, 128)[s, h]))
+            b, r = rows[top]
+            assert np.all(np.isfinite(got[s, 0, h]))
+            assert np.array_equal(got[s, 0, h], V[b, 0, r].numpy())
+
+
 def test_identical_keys_give_mean_of_v():
     case = synth.Case("samek", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=1,
                       qlen=1, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,

@@ -96,6 +96,26 @@ def test_tensor_core_kernel_matches_oracle(case, mode, monkeypatch):
                        util.oracle_decode(p), case.kv, case.name + " tcgen05")
 
 
+HUGE_K = [
+    synth.replace(synth.config4(batch=6, seed=2601), k_e8m0_range=(236, 249)),
+    synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2602),
+                  k_e8m0_range=(236, 249)),
+]
+
+
+@pytest.mark.parametrize("case", HUGE_K, ids=lambda c: f"{c.name}-b{c.batch}")
+@pytest.mark.parametrize("mode", ["split", "direct"])
+@pytest.mark.parametrize("kernel", ["mma", "tc"])
+def test_mxfp4_huge_k_exponents(case, mode, kernel, monkeypatch):
+    # K block exponents up to byte 249 (P2: logits went to inf there): scores near 2^122
+    # must stay finite, and the one-hot softmax must pick the oracle's token
+    monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16)
+    assert np.all(np.isfinite(got))
+    util.assert_parity(got, util.oracle_decode(p), case.kv, f"{case.name} huge K {kernel}")
+
+
 _LENS30 = [int(x) for x in np.random.default_rng(2504).integers(1, 800, 30)]
 MANY_TASKS = [
     synth.config4(batch=64, seed=2501),
