@@ -20,6 +20,10 @@
  *     x_t = softmax_scale * q_scale * sum_d q[d] * k_t[d]
  *     out = sum_t exp(x_t - M) v_t / sum_t exp(x_t - M),  M = max_t x_t
  *   computed in two passes, in double precision.
+ *   With causal set (query length > 1; the first page notes a causal option that a later
+ *   change adds next to the masking flag), query position i sees only the tokens
+ *   t < L - qlen + 1 + i: the context ends with the qlen query tokens themselves, and
+ *   each sees itself and what precedes it.  A position that sees no token gives zeros.
  *
  * Storage formats are decoded from their definitions:
  *   bf16      : the high half of an IEEE binary32
@@ -69,6 +73,7 @@ typedef struct {
   const void* value_scale;
   const int32_t* block_tables;
   const int32_t* context_lens;
+  int32_t causal;
 } orc_args;
 
 /* ---- format decoders ---------------------------------------------------- */
@@ -172,7 +177,8 @@ static double q_elem(const orc_args* a, int s, int i, int h, int d) {
  * Softmax attention of one (s, hkv) group over owned tokens [t0, t1), for every
  * query row of the group (qlen * G rows).  Writes, per row r:
  *   m[r] = max_t x_t, l[r] = sum_t exp(x_t - m[r]), o[r][:] = sum_t exp(x_t - m) v_t / l.
- * An empty range gives m = -inf, l = 0, o = 0.
+ * A row that sees no token of the range (an empty range, or causal masking) gives
+ * m = -inf, l = 0, o = 0.
  */
 static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, double* m,
                          double* l, double* o, double* x, double* qv, double* kv) {
@@ -182,6 +188,7 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
   const int S = a->page_size;
   const int32_t* bt = a->block_tables + (int64_t)s * a->max_blocks_per_seq;
   const int n = t1 - t0;
+  const int L = a->context_lens[s];
 
   for (int r = 0; r < R; ++r) {
     int i = r / G, h = hkv * G + r % G;
@@ -194,6 +201,10 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
     int64_t blk = bt[t / S];
     for (int d = 0; d < D; ++d) kv[d] = kv_elem(a, a->key_cache, a->key_scale, blk, hkv, t % S, d);
     for (int r = 0; r < R; ++r) {
+      if (a->causal && t >= L - a->qlen + 1 + r / G) {  /* after query position r / G */
+        x[(int64_t)r * n + j] = -INFINITY;
+        continue;
+      }
       double dot = 0.0;
       for (int d = 0; d < D; ++d) dot += qv[(int64_t)r * D + d] * kv[d];
       double xs = a->softmax_scale * dot;
@@ -212,6 +223,7 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
     for (int d = 0; d < D; ++d)
       kv[d] = kv_elem(a, a->value_cache, a->value_scale, blk, hkv, t % S, d);
     for (int r = 0; r < R; ++r) {
+      if (x[(int64_t)r * n + j] == -INFINITY) continue; /* not seen by this row */
       double w = exp(x[(int64_t)r * n + j] - m[r]);
       l[r] += w;
       for (int d = 0; d < D; ++d) o[(int64_t)r * D + d] += w * kv[d];
@@ -224,6 +236,7 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
 
 static int check_args(const orc_args* a) {
   if (a->batch < 0 || a->qlen < 1 || a->num_kv_heads < 1 || a->num_q_heads < 1) return -1;
+  if (a->causal != 0 && a->causal != 1) return -1;
   if (a->num_q_heads % a->num_kv_heads) return -1;
   if (a->head_dim < 1 || a->page_size < 1) return -1;
   if (a->kv_format == ORC_KV_MXFP4 && (a->head_dim % 32 || a->scale_kind != ORC_SCALE_E8M0))

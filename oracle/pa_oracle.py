@@ -50,6 +50,7 @@ class OrcArgs(ctypes.Structure):
         ("value_scale", ctypes.c_void_p),
         ("block_tables", ctypes.c_void_p),
         ("context_lens", ctypes.c_void_p),
+        ("causal", ctypes.c_int32),
     ]
 
 
@@ -130,7 +131,7 @@ class Problem:
     def __init__(self, *, batch, qlen, num_q_heads, num_kv_heads, head_dim, page_size,
                  num_blocks, kv_format, scale_kind, q_format, softmax_scale, query,
                  key_cache, value_cache, block_tables, context_lens, key_scale=None,
-                 value_scale=None, q_scale=None):
+                 value_scale=None, q_scale=None, causal=False):
         self.keep = []
         a = OrcArgs()
         a.batch, a.qlen, a.num_q_heads, a.num_kv_heads = batch, qlen, num_q_heads, num_kv_heads
@@ -140,6 +141,7 @@ class Problem:
         a.max_blocks_per_seq = bt.shape[1] if bt.ndim == 2 else 0
         a.kv_format, a.scale_kind, a.q_format = kv_format, scale_kind, q_format
         a.softmax_scale = float(softmax_scale)
+        a.causal = int(bool(causal))
         q = _np(query)
         kc, vc = _np(key_cache), _np(value_cache)
         ks = _np(key_scale)

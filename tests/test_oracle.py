@@ -147,6 +147,11 @@ def brute_force(p: dict, head_map=None) -> np.ndarray:
             v = V[blk, hkv, t % S]
             for i in range(qlen):
                 x = (k @ Q[s, i, h]) * case.scale_qk()
+                if case.causal:  # position i sees the tokens before L - qlen + 1 + i
+                    seen = t < L - qlen + 1 + i
+                    if not bool(seen.any()):
+                        continue
+                    x = torch.where(seen, x, torch.tensor(-math.inf, dtype=x.dtype))
                 w = torch.softmax(x, dim=0)
                 out[s, i, h] = w @ v
     return out.numpy()
@@ -167,6 +172,10 @@ def _tiny_cases():
         synth.Case("t_mxfp4_bfq", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=2,
                    qlen=2, num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=32,
                    context_lens=[33, 64], fill=synth.FILL_RANDOM, seed=15),
+        synth.Case("t_fp8_causal", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+                   qlen=4, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+                   context_lens=[2, 4, 17, 40], fill=synth.FILL_NAN, seed=17, kv_std=20.0,
+                   causal=True),
     ]
 
 
@@ -242,6 +251,36 @@ def test_huge_k_exponents_select_the_top_token():
             b, r = rows[top]
             assert np.all(np.isfinite(got[s, 0, h]))
             assert np.array_equal(got[s, 0, h], V[b, 0, r].numpy())
+
+
+def test_causal_with_one_query_position_is_the_plain_result():
+    case = synth.Case("c1", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3, qlen=1,
+                      num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                      context_lens=[5, 16, 33], seed=41)
+    p = synth.make(case)
+    pc = dict(p)
+    pc["case"] = synth.replace(case, causal=True)
+    assert np.array_equal(util.oracle_decode(pc), util.oracle_decode(p))
+
+
+def test_causal_position_sees_the_context_up_to_itself():
+    # query position i of a causal call equals the plain call on the same cache with the
+    # context cut to L - qlen + 1 + i (zeros when that is empty)
+    qlen = 4
+    case = synth.Case("ci", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=3, qlen=qlen,
+                      num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                      context_lens=[2, 19, 48], fill=synth.FILL_NAN, seed=42, kv_std=20.0,
+                      causal=True)
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    plain = synth.replace(case, causal=False)
+    for i in range(qlen):
+        pi = dict(p)
+        pi["case"] = plain
+        pi["context_lens"] = (p["context_lens"] - (qlen - 1 - i)).clamp(min=0)
+        ref = util.oracle_decode(pi)
+        assert np.array_equal(got[:, i], ref[:, i]), i
+    assert np.all(got[0, :2] == 0.0)  # L = 2 < qlen: the first two positions see nothing
 
 
 def test_identical_keys_give_mean_of_v():
