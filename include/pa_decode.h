@@ -131,10 +131,15 @@ typedef struct pa_decode_args {
   void* out;                  /* [B*qlen, Hq, D] bf16 */
   int64_t out_stride_token;
   int64_t out_stride_head;
+  /* 0 or 1.  With 1 and qlen > 1 the context is taken to end with the qlen query tokens:
+   * query position i sees tokens t < context_len - qlen + 1 + i only (a position that
+   * sees none gets a zero row).  The first page notes such a causal option, added by a
+   * later change next to the masking flag.  bf16 and fp8 caches; MXFP4 takes qlen 1. */
+  int32_t causal;
 } pa_decode_args;
 
 /* ABI version of this header; a mismatched library refuses nothing but reports it here. */
-#define PA_DECODE_ABI_VERSION 1
+#define PA_DECODE_ABI_VERSION 2
 int32_t pa_decode_abi_version(void);
 
 /* Bytes of workspace the three calls need for these shapes (plan, partition scratch,

@@ -391,6 +391,7 @@ pa_status validate(const pa_decode_args* a) {
   if (!combo) return PA_ERR_UNSUPPORTED;
   if (a->q_dtype != PA_Q_BF16 && a->q_dtype != PA_Q_FP8_E4M3) return PA_ERR_INVALID_ARG;
   if (a->merge_in_decode != 0 && a->merge_in_decode != 1) return PA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return PA_ERR_INVALID_ARG;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
@@ -446,13 +447,14 @@ pa_status split_params(const pa_decode_args* a, int* budget, int* maxp) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
-// and pages of at least 8 tokens, with the separate reduce.  It runs when
+// and pages of at least 8 tokens, with the separate reduce, not causal.  It runs when
 // PA_DECODE_KERNEL=tc is set in the environment (read at each call); otherwise every
 // shape runs the mma.sync kernel, the faster of the two on the long-context workloads.
 bool tc_kernel_applies(const pa_decode_args* a, int rows) {
   const char* e = getenv("PA_DECODE_KERNEL");
   const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
-  return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode;
+  return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
+         !(a->causal && a->qlen > 1);
 }
 
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
@@ -626,6 +628,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   pa::DecodeParams p;
   p.B = a->batch;
   p.qlen = a->qlen;
+  p.causal = a->causal && a->qlen > 1;
   p.Hq = a->num_q_heads;
   p.Hkv = a->num_kv_heads;
   p.G = G;

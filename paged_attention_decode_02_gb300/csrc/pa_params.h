@@ -46,6 +46,7 @@ struct DecodeParams {
   int64_t bt_stride;
   float scale_log2;  // softmax_scale * log2(e)
   int q_fp8, q_scale_per_row, scale_kind;
+  int causal;  // qlen > 1: query position i sees tokens < L - qlen + 1 + i
   const void* q;
   int64_t q_st, q_sh;
   const float* q_scale;

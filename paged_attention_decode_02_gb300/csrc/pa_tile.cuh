@@ -440,7 +440,7 @@ __device__ __forceinline__ void stage_compute(
     WarpAcc<C>& A, const uint8_t* kv, const uint8_t* sc, uint8_t* smem, int vw, int lane, int dw,
     int tg, const uint32_t (&qa)[C::Q_IN_REGS ? C::MT : 1][C::Q_IN_REGS ? C::NKCH : 1][4],
     const uint16_t* qs, const float (&crow)[C::MT][2], const uint32_t (&koff)[C::NGRP],
-    const uint32_t (&voff)[C::NCP], int cw, int& xbuf) {
+    const uint32_t (&voff)[C::NCP], int cw, int& xbuf, int cq, int G) {
   constexpr bool tok_scale = C::TOK_SCALE;
   const int g = lane >> 2, t = lane & 3;
   const uint32_t kbase = smem_u32(kv);
@@ -625,6 +625,16 @@ __device__ __forceinline__ void stage_compute(
   }
 
   // ---------------- logits and boundary mask ----------------
+  // Row limits: tokens at or past vw are unowned; with causal masking (cq = qlen - 1 > 0)
+  // query position i = row / G sees only the tokens before vw - (cq - i).
+  int lim[C::MT][2];
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = (16 * mt + g + 8 * hr) / G;
+      lim[mt][hr] = MASKED ? vw - (cq > i ? cq - i : 0) : vw;
+    }
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
     const int tk0 = 8 * nt + 2 * t;
@@ -636,7 +646,7 @@ __device__ __forceinline__ void stage_compute(
       for (int j = 0; j < 4; ++j) {
         float x = sacc[mt][nt][j] * crow[mt][j >> 1];
         if constexpr (tok_scale) x *= (j & 1) ? ks.y : ks.x;
-        if (MASKED && tk0 + (j & 1) >= vw) x = -INFINITY;
+        if (MASKED && tk0 + (j & 1) >= lim[mt][j >> 1]) x = -INFINITY;
         sacc[mt][nt][j] = x;
       }
   }
@@ -877,6 +887,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   int cslot = 0;      // ring slot of the next compute
   uint32_t cpar = 0;  // its phase parity
   int xbuf = 0;
+  const int cq = p.causal ? p.qlen - 1 : 0;  // tokens a query position may not see past
 
   for (int task = t_begin; task < t_end; ++task) {
     const PlanTask tk = p.tasks[task];
@@ -947,12 +958,12 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       const uint8_t* kv = ring + cslot * C::SLOT_KV;
       const uint8_t* sc = scring + cslot * C::SLOT_SC;
       const int vw = L - (c0 + r0);  // owned tokens in the slice (> 0 here)
-      if (vw >= C::TW) {
+      if (vw - cq >= C::TW) {
         stage_compute<C, false>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
-                                xbuf);
+                                xbuf, cq, p.G);
       } else {
         stage_compute<C, true>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
-                               xbuf);
+                               xbuf, cq, p.G);
       }
       const int done_slot = cslot;
       ++consumed;

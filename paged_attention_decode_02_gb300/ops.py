@@ -50,7 +50,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("scale_stride_head", ctypes.c_int64), ("block_tables", ctypes.c_void_p),
         ("bt_stride", ctypes.c_int64), ("context_lens", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
-        ("out_stride_head", ctypes.c_int64),
+        ("out_stride_head", ctypes.c_int64), ("causal", ctypes.c_int32),
     ]
 
 
@@ -119,7 +119,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               key_scale: Optional[torch.Tensor] = None, value_scale: Optional[torch.Tensor] = None,
               q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
               max_partitions: int = 0, task_budget: int = 0,
-              merge_in_decode: bool = False) -> PaDecodeArgs:
+              merge_in_decode: bool = False, causal: bool = False) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -162,6 +162,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     a.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)
     a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
     a.merge_in_decode = int(bool(merge_in_decode))
+    a.causal = int(bool(causal))
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
@@ -268,7 +269,8 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      problem["context_lens"], out, key_scale=problem["key_scale"],
                      value_scale=problem["value_scale"], q_scale=problem["q_scale"],
                      softmax_scale=case.scale_qk(), max_partitions=max_partitions,
-                     task_budget=task_budget, merge_in_decode=merge_in_decode)
+                     task_budget=task_budget, merge_in_decode=merge_in_decode,
+                     causal=getattr(case, "causal", False))
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

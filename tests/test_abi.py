@@ -29,13 +29,14 @@ def test_header_declarations_are_exported(lib):
     assert set(ops.EXPORTED) == set(names), names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.pa_decode_abi_version() == 1
+    assert lib.pa_decode_abi_version() == 2
 
 
 def test_args_struct_layout_matches_header():
-    # 16 int32/float fields, then pointers and int64s
-    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 19 * 8
+    # 16 int32/float fields, then 19 pointers and int64s, then the causal flag (padded)
+    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 20 * 8
     assert ops.PaDecodeArgs.query.offset == 64
+    assert ops.PaDecodeArgs.causal.offset == 64 + 19 * 8
 
 
 def _valid_args():

@@ -116,6 +116,36 @@ def test_mxfp4_huge_k_exponents(case, mode, kernel, monkeypatch):
     util.assert_parity(got, util.oracle_decode(p), case.kv, f"{case.name} huge K {kernel}")
 
 
+CAUSAL = [
+    synth.Case("causal_fp8_token", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=5,
+               qlen=4, num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[1, 3, 4, 257, 2000], seed=2701, kv_std=20.0, causal=True),
+    synth.replace(synth.config3(qlen=4, batch=4, context_lens=(200, 900), seed=2702), causal=True),
+    synth.replace(synth.config2("b", batch=5, seed=2703), causal=True),
+    synth.Case("causal_bf16", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=4, qlen=2,
+               num_kv_heads=1, num_q_heads=8, head_dim=128, page_size=16,
+               context_lens=[1, 2, 33, 300], seed=2704, causal=True),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL, ids=lambda c: f"{c.name}-q{c.qlen}")
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_causal_matches_oracle(case, mode):
+    # query position i sees tokens < L - qlen + 1 + i; contexts shorter than qlen leave the
+    # first positions with nothing to see (zero rows)
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
+
+
+def test_causal_runs_on_the_mma_kernel_when_tcgen05_is_requested(monkeypatch):
+    monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+    case = CAUSAL[0]
+    p = synth.make(case)
+    util.assert_parity(run_gpu(p, task_budget=24), util.oracle_decode(p), case.kv, case.name)
+
+
 _LENS30 = [int(x) for x in np.random.default_rng(2504).integers(1, 800, 30)]
 MANY_TASKS = [
     synth.config4(batch=64, seed=2501),
