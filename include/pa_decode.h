@@ -46,8 +46,12 @@
  *                                         [NB, Hkv, S, D/32], 2^(b-127) per 32 values
  *   ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary: the MXFP4 page layout.)
  *   row_bytes = 2D (bf16), D (e4m3), D/2 (MXFP4).  q_dtype PA_Q_BF16 reads a bf16
- *   query; PA_Q_FP8_E4M3 reads e4m3 bytes multiplied by q_scale (fp32 [1], or
- *   [B, qlen, Hq] when q_scale_per_row != 0).
+ *   query exactly; PA_Q_FP8_E4M3 reads e4m3 bytes multiplied by q_scale (fp32 [1], or
+ *   [B, qlen, Hq] when q_scale_per_row != 0); PA_Q_BF16_TO_E4M3 (MXFP4 KV only) reads a
+ *   bf16 query and quantises each head row in the kernel as the MXFP4 page does
+ *   ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary): s = amax / 448 and y = q / s in fp32
+ *   (round to nearest), y rounded to the nearest e4m3 (ties to even, saturating at
+ *   448), used as e4m3(y) * s; q_scale is not read.
  *
  * Supported shapes (others return PA_ERR_UNSUPPORTED): head_dim 128 or 256
  * (MXFP4: 128); page_size 16, 32, 64, 128 or 256; G * qlen <= 32 (MXFP4: <= 16,
@@ -82,6 +86,7 @@ typedef int32_t pa_status;
 
 #define PA_Q_BF16 0
 #define PA_Q_FP8_E4M3 1
+#define PA_Q_BF16_TO_E4M3 2
 
 /* Device status word (first int32 of the workspace), read with pa_decode_read_status. */
 #define PA_DEVICE_OK 0

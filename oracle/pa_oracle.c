@@ -40,7 +40,12 @@
  *               high nibble (the OCP MX packing; the pages do not say).
  *
  * All tensors are dense and contiguous:
- *   query        [B, qlen, Hq, D]        bf16 or e4m3 bytes
+ *   query        [B, qlen, Hq, D]        bf16 or e4m3 bytes.  A bf16 query may also be read
+ *                as the MXFP4 page quantises it ("[FlyDSL] pa_decode: MXFP4 K/V ...",
+ *                Summary: bf16 Q is quantised to e4m3 per head row in the kernel): per
+ *                row, s = amax / 448 and y = q / s in fp32 (round to nearest), y rounded
+ *                to the nearest e4m3 value (ties to even, finite at +-448), read back as
+ *                e4m3(y) * s; a zero row stays zero.
  *   q_scale      scalar or [B, qlen, Hq] fp32 (e4m3 query only)
  *   key/value    [NB, Hkv, S, row_bytes] (row_bytes = 2D bf16, D e4m3, D/2 MXFP4)
  *   scales       per-tensor: fp32 [1]; per-token: fp32 [NB, Hkv, S];
@@ -58,7 +63,7 @@
 
 enum { ORC_KV_BF16 = 0, ORC_KV_E4M3 = 1, ORC_KV_MXFP4 = 2 };
 enum { ORC_SCALE_NONE = 0, ORC_SCALE_TENSOR = 1, ORC_SCALE_TOKEN = 2, ORC_SCALE_E8M0 = 3 };
-enum { ORC_Q_BF16 = 0, ORC_Q_E4M3 = 1 };
+enum { ORC_Q_BF16 = 0, ORC_Q_E4M3 = 1, ORC_Q_BF16_TO_E4M3 = 2 };
 
 typedef struct {
   int32_t batch, qlen, num_q_heads, num_kv_heads, head_dim, page_size;
@@ -115,6 +120,23 @@ double orc_e8m0(uint8_t b) {
   return ldexp(1.0, (int)b - 127);
 }
 
+/* Nearest e4m3 (OCP) value to y, ties to even, saturating at +-448 (the largest finite
+ * e4m3); the spacing is 2^(E-3) in the binade [2^E, 2^(E+1)), E >= -6 (below 2^-6 the
+ * subnormal spacing 2^-9 continues). */
+double orc_e4m3_round(float y) {
+  if (isnan(y)) return NAN;
+  double a = fabs((double)y);
+  if (a >= 448.0) return y < 0 ? -448.0 : 448.0;
+  if (a == 0.0) return (double)y;
+  int e;
+  (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): binade E = e - 1 */
+  int E = e - 1 < -6 ? -6 : e - 1;
+  double quantum = ldexp(1.0, E - 3);
+  double r = rint(a / quantum) * quantum; /* rint: nearest, ties to even */
+  if (r > 448.0) r = 448.0;
+  return y < 0 ? -r : r;
+}
+
 /* ---- element access ------------------------------------------------------ */
 
 static int64_t row_bytes(const orc_args* a) {
@@ -161,7 +183,7 @@ static double kv_elem(const orc_args* a, const void* cache, const void* scale, i
 
 static double q_elem(const orc_args* a, int s, int i, int h, int d) {
   const int64_t qrow = ((int64_t)s * a->qlen + i) * a->num_q_heads + h;
-  if (a->q_format == ORC_Q_BF16) {
+  if (a->q_format == ORC_Q_BF16 || a->q_format == ORC_Q_BF16_TO_E4M3) {
     uint16_t bits;
     memcpy(&bits, (const uint8_t*)a->query + 2 * (qrow * a->head_dim + d), 2);
     return orc_bf16(bits);
@@ -193,6 +215,18 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
   for (int r = 0; r < R; ++r) {
     int i = r / G, h = hkv * G + r % G;
     for (int d = 0; d < D; ++d) qv[(int64_t)r * D + d] = q_elem(a, s, i, h, d);
+    if (a->q_format == ORC_Q_BF16_TO_E4M3) { /* quantise the row (see the header) */
+      float amax = 0.0f;
+      for (int d = 0; d < D; ++d) {
+        float q = (float)qv[(int64_t)r * D + d];
+        if (fabsf(q) > amax) amax = fabsf(q);
+      }
+      float sc = amax / 448.0f;
+      for (int d = 0; d < D; ++d) {
+        float q = (float)qv[(int64_t)r * D + d];
+        qv[(int64_t)r * D + d] = amax > 0.0f ? orc_e4m3_round(q / sc) * (double)sc : 0.0;
+      }
+    }
   }
   /* pass 1: scores */
   for (int r = 0; r < R; ++r) m[r] = -INFINITY;

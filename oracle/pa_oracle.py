@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_BUILD, "libpa_oracle.so")
 
 KV_BF16, KV_E4M3, KV_MXFP4 = 0, 1, 2
 SCALE_NONE, SCALE_TENSOR, SCALE_TOKEN, SCALE_E8M0 = 0, 1, 2, 3
-Q_BF16, Q_E4M3 = 0, 1
+Q_BF16, Q_E4M3, Q_BF16_TO_E4M3 = 0, 1, 2
 
 
 class OrcArgs(ctypes.Structure):
@@ -93,6 +93,8 @@ def lib():
                 getattr(L, name).restype = ctypes.c_double
             L.orc_bf16.argtypes = [ctypes.c_uint16]
             L.orc_bf16.restype = ctypes.c_double
+            L.orc_e4m3_round.argtypes = [ctypes.c_float]
+            L.orc_e4m3_round.restype = ctypes.c_double
             L.orc_max_threads.restype = ctypes.c_int
             _lib = L
         return _lib
@@ -122,7 +124,8 @@ def _ptr(a):
 class Problem:
     """Stored bytes of one decode call, in the dense layouts the oracle reads.
 
-    kv_format: KV_BF16 | KV_E4M3 | KV_MXFP4; scale_kind: SCALE_*; q_format: Q_BF16 | Q_E4M3.
+    kv_format: KV_BF16 | KV_E4M3 | KV_MXFP4; scale_kind: SCALE_*; q_format: Q_BF16 | Q_E4M3 |
+    Q_BF16_TO_E4M3 (bf16 query quantised per head row to e4m3, scale amax / 448).
     query: [B, qlen, Hq, D] (bf16 bits as uint16/int16, or e4m3 bytes);
     key/value: [NB, Hkv, S, row_bytes] bytes (bf16 as 16-bit words);
     key_scale/value_scale: float32 [1] | float32 [NB, Hkv, S] | uint8 [NB, Hkv, S, D/32].
@@ -181,6 +184,11 @@ class Problem:
 
 def decode_e4m3(b: int) -> float:
     return lib().orc_e4m3(b)
+
+
+def round_e4m3(y: float) -> float:
+    """The oracle's nearest-e4m3 rounding (ties to even, saturating at +-448) of float32 y."""
+    return lib().orc_e4m3_round(y)
 
 
 def decode_e2m1(n: int) -> float:

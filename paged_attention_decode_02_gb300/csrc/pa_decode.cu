@@ -389,7 +389,9 @@ pa_status validate(const pa_decode_args* a) {
                      (a->kv_dtype == PA_KV_MXFP4 && a->kv_scale == PA_SCALE_E8M0_32);
   if (a->kv_dtype < 0 || a->kv_dtype > 2 || a->kv_scale < 0 || a->kv_scale > 3) return PA_ERR_INVALID_ARG;
   if (!combo) return PA_ERR_UNSUPPORTED;
-  if (a->q_dtype != PA_Q_BF16 && a->q_dtype != PA_Q_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  if (a->q_dtype != PA_Q_BF16 && a->q_dtype != PA_Q_FP8_E4M3 && a->q_dtype != PA_Q_BF16_TO_E4M3)
+    return PA_ERR_INVALID_ARG;
+  if (a->q_dtype == PA_Q_BF16_TO_E4M3 && a->kv_dtype != PA_KV_MXFP4) return PA_ERR_UNSUPPORTED;
   if (a->merge_in_decode != 0 && a->merge_in_decode != 1) return PA_ERR_INVALID_ARG;
   if (a->causal != 0 && a->causal != 1) return PA_ERR_INVALID_ARG;
   const int G = a->num_q_heads / a->num_kv_heads;
@@ -402,7 +404,7 @@ pa_status validate(const pa_decode_args* a) {
   if (a->q_dtype == PA_Q_FP8_E4M3 && !a->q_scale) return PA_ERR_INVALID_ARG;
   if (a->kv_scale != PA_SCALE_NONE && (!a->key_scale || !a->value_scale)) return PA_ERR_INVALID_ARG;
   // query / output: head_dim contiguous; vector loads need 16-byte aligned rows
-  const int qel = a->q_dtype == PA_Q_BF16 ? 2 : 1;
+  const int qel = a->q_dtype == PA_Q_FP8_E4M3 ? 1 : 2;
   if (a->q_stride_head < a->head_dim || a->q_stride_token < 0) return PA_ERR_INVALID_ARG;
   if (!aligned16(a->query) || (a->q_stride_head * qel) % 16 || (a->q_stride_token * qel) % 16)
     return PA_ERR_UNSUPPORTED;
@@ -454,7 +456,7 @@ bool tc_kernel_applies(const pa_decode_args* a, int rows) {
   const char* e = getenv("PA_DECODE_KERNEL");
   const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
   return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
-         !(a->causal && a->qlen > 1);
+         !(a->causal && a->qlen > 1) && a->q_dtype != PA_Q_BF16_TO_E4M3;
 }
 
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
@@ -641,6 +643,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   const float sc = a->softmax_scale > 0.f ? a->softmax_scale : 1.0f / sqrtf((float)a->head_dim);
   p.scale_log2 = sc * 1.4426950408889634f;
   p.q_fp8 = a->q_dtype == PA_Q_FP8_E4M3;
+  p.q_quant = a->q_dtype == PA_Q_BF16_TO_E4M3;
   p.q_scale_per_row = a->q_scale_per_row != 0;
   p.scale_kind = a->kv_scale;
   p.q = a->query;

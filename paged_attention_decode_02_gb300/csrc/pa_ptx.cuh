@@ -165,6 +165,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 // ---- conversions ------------------------------------------------------------------
+// x rounded to the nearest e4m3 value (ties to even, saturating at +-448), as a float.
+__device__ __forceinline__ float round_e4m3(float x) {
+  uint16_t b;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(b) : "f"(x));  // both bytes: e4m3(x)
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFF)));
+}
 // Two OCP e4m3 values (low byte -> low half) to f16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x16) {
   uint32_t d;

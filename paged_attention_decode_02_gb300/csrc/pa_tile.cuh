@@ -249,7 +249,21 @@ __device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C
           x[2 * j + 1] = __uint_as_float(q.w[k][j] & 0xFFFF0000u);
         }
       }
-      crv = p.scale_log2 * q.qsc[k];
+      float qsck = q.qsc[k];
+      if constexpr (C::KIND == KIND_FP4) {
+        if (p.q_quant) {  // the row quantised to e4m3, scale amax / 448 (fp32, nearest)
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < EPL; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+          for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float sq = __fdiv_rn(amax, 448.f);
+#pragma unroll
+          for (int j = 0; j < EPL; ++j) x[j] = amax > 0.f ? round_e4m3(__fdiv_rn(x[j], sq)) : 0.f;
+          qsck = amax > 0.f ? sq : 0.f;
+        }
+      }
+      crv = p.scale_log2 * qsck;
       if constexpr (C::KIND == KIND_FP8) {
         if (p.scale_kind == SK_TENSOR) crv *= k_scale_tensor;
       }

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libpa_decode.so")
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1, -2, -3, -4
 PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_MXFP4 = 0, 1, 2
 PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN, PA_SCALE_E8M0_32 = 0, 1, 2, 3
-PA_Q_BF16, PA_Q_FP8_E4M3 = 0, 1
+PA_Q_BF16, PA_Q_FP8_E4M3, PA_Q_BF16_TO_E4M3 = 0, 1, 2
 PA_DEVICE_WAIT_TIMEOUT, PA_DEVICE_CONTEXT_CLAMPED = 1, 2
 
 EXPORTED = ["pa_decode_abi_version", "pa_decode_workspace_size", "pa_decode_validate",
@@ -119,7 +119,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               key_scale: Optional[torch.Tensor] = None, value_scale: Optional[torch.Tensor] = None,
               q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
               max_partitions: int = 0, task_budget: int = 0,
-              merge_in_decode: bool = False, causal: bool = False) -> PaDecodeArgs:
+              merge_in_decode: bool = False, causal: bool = False,
+              q_quant: bool = False) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -157,7 +158,10 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
         a.kv_dtype, a.kv_scale = PA_KV_MXFP4, PA_SCALE_E8M0_32
     else:
         raise ValueError(f"cannot infer the KV format from {tuple(key_cache.shape)} and D={D}")
-    a.q_dtype = PA_Q_BF16 if query.dtype == torch.bfloat16 else PA_Q_FP8_E4M3
+    if query.dtype == torch.bfloat16:
+        a.q_dtype = PA_Q_BF16_TO_E4M3 if q_quant else PA_Q_BF16
+    else:
+        a.q_dtype = PA_Q_FP8_E4M3
     a.q_scale_per_row = int(q_scale is not None and q_scale.numel() > 1)
     a.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)
     a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
@@ -270,7 +274,7 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      value_scale=problem["value_scale"], q_scale=problem["q_scale"],
                      softmax_scale=case.scale_qk(), max_partitions=max_partitions,
                      task_budget=task_budget, merge_in_decode=merge_in_decode,
-                     causal=getattr(case, "causal", False))
+                     causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False))
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -51,6 +51,7 @@ class Case:
     e8m0_range: tuple = (120, 130)
     k_e8m0_range: Optional[tuple] = None  # MXFP4 K exponents, when they differ from V's
     causal: bool = False  # query length > 1: position i sees tokens < L - qlen + 1 + i
+    q_quant: bool = False  # bf16 query quantised to e4m3 per head row by the kernel (MXFP4)
     pad_columns: int = 2
     extra_blocks: int = 0
     # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and

@@ -283,6 +283,73 @@ def test_causal_position_sees_the_context_up_to_itself():
     assert np.all(got[0, :2] == 0.0)  # L = 2 < qlen: the first two positions see nothing
 
 
+def test_e4m3_rounding_matches_torch():
+    # every finite e4m3 value, every midpoint between neighbours (ties go to the even
+    # code), and random floats, against torch's float32 -> float8_e4m3fn cast
+    codes = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    vals = np.array(sorted({orc.decode_e4m3(c) for c in codes}), dtype=np.float64)
+    pos = vals[vals >= 0]
+    mids = (pos[1:] + pos[:-1]) / 2
+    rng = np.random.default_rng(7)
+    rnd = np.concatenate([rng.uniform(-448, 448, 4000), rng.uniform(-0.02, 0.02, 2000)])
+    x = np.concatenate([vals, mids, -mids, rnd]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([orc.round_e4m3(float(v)) for v in x])
+    assert np.array_equal(got, ref)
+    assert orc.round_e4m3(500.0) == 448.0 and orc.round_e4m3(-1e6) == -448.0
+
+
+def _quant_rows_torch(Q: torch.Tensor) -> torch.Tensor:
+    """Per head row: s = amax / 448, y = q / s in float32, torch's e4m3 cast, times s."""
+    q32 = Q.to(torch.float32)
+    amax = q32.abs().amax(dim=-1, keepdim=True)
+    s = amax / torch.tensor(448.0, dtype=torch.float32)
+    y = torch.where(amax > 0, q32 / torch.where(amax > 0, s, torch.ones_like(s)), torch.zeros_like(q32))
+    e = y.to(torch.float8_e4m3fn).to(torch.float64)
+    return e * s.to(torch.float64)
+
+
+def test_quantised_query_matches_dense_torch_path():
+    case = synth.Case("qq", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=3, qlen=1,
+                      num_kv_heads=2, num_q_heads=8, head_dim=128, page_size=16,
+                      context_lens=[5, 40, 77], fill=synth.FILL_RANDOM, seed=51, q_quant=True)
+    p = synth.make(case)
+    got = util.oracle_decode(p)
+    K, V = _dequant_dense(p, "k"), _dequant_dense(p, "v")
+    Q = _quant_rows_torch(_query_dense(p).reshape(3, 8, 128))
+    bt = p["block_tables"].cpu()
+    for s, L in enumerate([5, 40, 77]):
+        rows = [(int(bt[s, t // 16]), t % 16) for t in range(L)]
+        for h in range(8):
+            k = torch.stack([K[b, h // 4, r] for b, r in rows])
+            v = torch.stack([V[b, h // 4, r] for b, r in rows])
+            w = torch.softmax((k @ Q[s, h]) * case.scale_qk(), dim=0)
+            np.testing.assert_allclose(got[s, 0, h], (w @ v).numpy(), rtol=1e-11, atol=1e-12)
+    # and the quantisation is not a no-op on this data
+    plain = dict(p)
+    plain["case"] = synth.replace(case, q_quant=False)
+    assert util.rel_l2(util.oracle_decode(plain), got) > 1e-4
+
+
+def test_quantised_query_of_exact_rows_is_the_plain_query():
+    # rows that are e4m3 codes times 2^-4 with |max| = 448 * 2^-4: s = 2^-4 exactly and
+    # every y is already an e4m3 value, so the quantised query equals the stored one
+    case = synth.Case("qx", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=2, qlen=1,
+                      num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
+                      context_lens=[9, 30], fill=synth.FILL_RANDOM, seed=52, q_quant=True)
+    p = synth.make(case)
+    rng = np.random.default_rng(53)
+    finite = np.array([orc.decode_e4m3(c) for c in range(256) if (c & 0x7F) != 0x7F])
+    q = rng.choice(finite, size=(2, 4, 128)) / 16.0
+    q[..., 0] = 448.0 / 16.0
+    p["query"] = torch.from_numpy(q).to(torch.bfloat16).reshape(p["query"].shape)
+    assert torch.equal(torch.from_numpy(q).to(torch.bfloat16).to(torch.float64),
+                       torch.from_numpy(q))  # bf16-exact
+    plain = dict(p)
+    plain["case"] = synth.replace(case, q_quant=False)
+    assert np.array_equal(util.oracle_decode(p), util.oracle_decode(plain))
+
+
 def test_identical_keys_give_mean_of_v():
     case = synth.Case("samek", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=1,
                       qlen=1, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,

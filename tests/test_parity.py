@@ -146,6 +146,23 @@ def test_causal_runs_on_the_mma_kernel_when_tcgen05_is_requested(monkeypatch):
     util.assert_parity(run_gpu(p, task_budget=24), util.oracle_decode(p), case.kv, case.name)
 
 
+QQUANT = [
+    synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
+    synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
+                  q_quant=True),
+]
+
+
+@pytest.mark.parametrize("case", QQUANT, ids=lambda c: f"{c.name}-b{c.batch}")
+@pytest.mark.parametrize("mode", ["split", "direct"])
+def test_mxfp4_with_query_quantised_in_kernel(case, mode):
+    # the MXFP4 page's query mode: each bf16 head row quantised to e4m3 (scale amax / 448)
+    # in the kernel; the oracle quantises the same way, in the same precision
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16)
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name + " quantised query")
+
+
 _LENS30 = [int(x) for x in np.random.default_rng(2504).integers(1, 800, 30)]
 MANY_TASKS = [
     synth.config4(batch=64, seed=2501),

@@ -32,7 +32,8 @@ def oracle_problem(p: dict, seqs=None) -> orc.Problem:
         batch=batch, qlen=case.qlen, num_q_heads=case.num_q_heads,
         num_kv_heads=case.num_kv_heads, head_dim=case.head_dim, page_size=case.page_size,
         num_blocks=p["num_blocks"], kv_format=_KV[case.kv], scale_kind=_SC[case.scale],
-        q_format=_Q[case.q], softmax_scale=case.scale_qk(), query=q,
+        q_format=orc.Q_BF16_TO_E4M3 if case.q_quant else _Q[case.q],
+        softmax_scale=case.scale_qk(), query=q,
         key_cache=cpu(p["key_cache"]), value_cache=cpu(p["value_cache"]),
         key_scale=cpu(p["key_scale"]), value_scale=cpu(p["value_scale"]), q_scale=qs,
         block_tables=bt, context_lens=cl, causal=case.causal)
