@@ -71,7 +71,7 @@ struct TileCfg {
   static constexpr int OFF_OB = OFF_X + X_BYTES;
   static constexpr int OFF_ML = OFF_OB + RPAD * D * 4;
   static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;  // 1 / sum per row
-  static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 2 : 0;  // V e8m0 factor table
+  static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 6 : 0;  // K and V e8m0 factor tables
   static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
   static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
   static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
@@ -463,7 +463,8 @@ __device__ __forceinline__ void stage_compute(
   const float* vsc = reinterpret_cast<const float*>(sc + 4 * C::TW);
   const uint32_t* kex = reinterpret_cast<const uint32_t*>(sc);
   const uint32_t* vex = reinterpret_cast<const uint32_t*>(sc + 4 * C::TW);
-  uint16_t* vtab = reinterpret_cast<uint16_t*>(smem + C::OFF_TAB + cw * C::TAB_BYTES);
+  float* ktab = reinterpret_cast<float*>(smem + C::OFF_TAB + cw * C::TAB_BYTES);
+  uint16_t* vtab = reinterpret_cast<uint16_t*>(ktab + C::NBLK * C::TW);
 
   // ---------------- fp8 per-token V-scale reference (lazy) ----------------
   float beta[C::NBLK];
@@ -485,6 +486,16 @@ __device__ __forceinline__ void stage_compute(
       rescale_v = true;
     }
     vinv = A.vinv;
+  }
+  if constexpr (C::KIND == KIND_FP4) {
+    // K: this lane's token's block factors 2^(e-127) x kKFactorBias (the row's logit factor
+    // carries the inverse), read back per score pair after the MMAs; an unowned token's
+    // scores are overwritten by the boundary mask
+    const uint32_t kw = kex[lane];
+#pragma unroll
+    for (int b = 0; b < C::NBLK; ++b)
+      ktab[b * C::TW + lane] = __uint_as_float(((kw >> (8 * b)) & 0xFFu) << 23) * kKFactorBias;
+    __syncwarp();
   }
   // ---------------- S = Q K^T over this warp's dims ----------------
   float sacc[C::MT][C::NT][4];
@@ -544,12 +555,6 @@ __device__ __forceinline__ void stage_compute(
           }
         }
     } else {
-      // K block factors 2^(e-127) of the lane's tokens 8nt + 2t and 8nt + 2t + 1, from the
-      // raw e8m0 words (unowned tokens' scores are overwritten by the boundary mask), times
-      // kKFactorBias (the row's logit factor carries the inverse)
-      uint2 kw[C::NT];
-#pragma unroll
-      for (int nt = 0; nt < C::NT; ++nt) kw[nt] = *reinterpret_cast<const uint2*>(kex + 8 * nt + 2 * t);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         float tmp[C::MT][C::NT][4];
@@ -564,8 +569,7 @@ __device__ __forceinline__ void stage_compute(
         }
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
-          const float2 kf = make_float2(__uint_as_float(((kw[nt].x >> (8 * b)) & 0xFFu) << 23) * kKFactorBias,
-                                        __uint_as_float(((kw[nt].y >> (8 * b)) & 0xFFu) << 23) * kKFactorBias);
+          const float2 kf = *reinterpret_cast<const float2*>(ktab + b * C::TW + 8 * nt + 2 * t);
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt) {
             sacc[mt][nt][0] = fmaf(tmp[mt][nt][0], kf.x, sacc[mt][nt][0]);
@@ -901,7 +905,8 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   int cslot = 0;      // ring slot of the next compute
   uint32_t cpar = 0;  // its phase parity
   int xbuf = 0;
-  const int cq = p.causal ? p.qlen - 1 : 0;  // tokens a query position may not see past
+  // tokens a query position may not see past (MXFP4 takes one query position: none)
+  const int cq = (C::KIND != KIND_FP4 && p.causal) ? p.qlen - 1 : 0;
 
   for (int task = t_begin; task < t_end; ++task) {
     const PlanTask tk = p.tasks[task];
