@@ -644,6 +644,10 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.scale_log2 = sc * 1.4426950408889634f;
   p.q_fp8 = a->q_dtype == PA_Q_FP8_E4M3;
   p.q_quant = a->q_dtype == PA_Q_BF16_TO_E4M3;
+  {  // test hook (environment, read at each call): make one pipeline wait run out
+    const char* d = getenv("PA_DECODE_TEST_DROP_SLICE");
+    p.drop_first_slice = d != nullptr && strcmp(d, "1") == 0;
+  }
   p.q_scale_per_row = a->q_scale_per_row != 0;
   p.scale_kind = a->kv_scale;
   p.q = a->query;

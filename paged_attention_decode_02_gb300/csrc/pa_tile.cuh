@@ -893,10 +893,18 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   if (!ld.done) it_load_task(ld, p);
   it_settle<C>(ld, p, t_end, r0, lane, box_shift, page_shift);
   uint32_t issued = 0, consumed = 0;
+  // Consumption index of this warp's first wait that gave up (or that it skipped because
+  // another warp of the CTA gave up); from there on it issues no load, and before leaving
+  // it waits, with a limit, for every slice it issued but did not wait for.
+  constexpr uint32_t kNoAbort = 0xFFFFFFFFu;
+  uint32_t abort_at = kNoAbort;
   int lslot = 0;  // ring slot of the next load
   while (!ld.done && issued < (uint32_t)C::NSTAGE) {
-    issue_slice<C>(p, tmk, tmv, ring + lslot * C::SLOT_KV, scring + lslot * C::SLOT_SC,
-                   &bars[lslot], ld, r0, dw, lane, box_shift, page_mask);
+    // (test hook: with drop_first_slice, warp 0 of every CTA leaves its first slot empty,
+    // so the wait for it gives up after its time limit and the status reports the timeout)
+    if (!(p.drop_first_slice && cw == 0 && issued == 0))
+      issue_slice<C>(p, tmk, tmv, ring + lslot * C::SLOT_KV, scring + lslot * C::SLOT_SC,
+                     &bars[lslot], ld, r0, dw, lane, box_shift, page_mask);
     ++issued;
     lslot = lslot + 1 == C::NSTAGE ? 0 : lslot + 1;
     ld.c0 += C::TC;
@@ -968,10 +976,13 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     for (int b = 0; b < C::NBLK; ++b) A.emax[b] = -1;
 
     for (int c0 = t0; c0 + r0 < t1; c0 += C::TC) {
-      if (!*abort_flag) {
-        if (!mbar_wait_bounded(&bars[cslot], cpar)) {
+      if (abort_at == kNoAbort) {
+        if (*abort_flag) {
+          abort_at = consumed;
+        } else if (!mbar_wait_bounded(&bars[cslot], cpar)) {
           *abort_flag = 1;
           if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
+          abort_at = consumed;
         }
       }
       const uint8_t* kv = ring + cslot * C::SLOT_KV;
@@ -991,7 +1002,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         cpar ^= 1;
       }
       __syncwarp();
-      if (!ld.done) {  // refill the slot just read with the slice NSTAGE ahead
+      if (!ld.done && abort_at == kNoAbort) {  // refill the slot just read with the slice NSTAGE ahead
         issue_slice<C>(p, tmk, tmv, ring + done_slot * C::SLOT_KV, scring + done_slot * C::SLOT_SC,
                        &bars[done_slot], ld, r0, dw, lane, box_shift, page_mask);
         ++issued;
@@ -1207,14 +1218,9 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     }
   }
   // Never leave while a copy into this CTA's shared memory may still be in flight (only
-  // possible after a timed-out wait).
-  for (; consumed < issued; ++consumed) {
-    (void)mbar_wait_bounded(&bars[cslot], cpar, 200000000ull);
-    if (++cslot == C::NSTAGE) {
-      cslot = 0;
-      cpar ^= 1;
-    }
-  }
+  // possible after a wait gave up): slice idx went to slot idx mod NSTAGE, phase idx / NSTAGE.
+  for (uint32_t idx = abort_at; idx < issued; ++idx)
+    (void)mbar_wait_bounded(&bars[idx % C::NSTAGE], (idx / C::NSTAGE) & 1, 200000000ull);
 }
 
 template <class C>
