@@ -76,7 +76,8 @@ struct TileCfg {
   static constexpr int OFF_BAR = (OFF_TAB + NCW * TAB_BYTES + 15) / 16 * 16;
   static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
   static constexpr int OFF_NXT = OFF_FLAG + 16;  // the next task's record (16 bytes)
-  static constexpr int SMEM = OFF_NXT + 16 + 1024;  // + slack to align the base to 1 KiB
+  static constexpr int OFF_ABT = OFF_NXT + 16;  // per warp: where its waits stopped
+  static constexpr int SMEM = OFF_ABT + NCW * 4 + 1024;  // + slack to align the base to 1 KiB
   static_assert(TW % 16 == 0, "a warp slice holds whole 16-token k-chunks");
   static_assert(WBYTES % 64 == 0, "a warp row slice is whole ldmatrix.x4 groups");
   static_assert(NSUB % NDW == 0, "head-dim split on sub-tile boundaries");
@@ -88,6 +89,7 @@ struct TileCfg {
 };
 
 constexpr int BAR_CONSUMERS = 15;  // named barrier id for all warps of the CTA
+constexpr uint32_t kNoAbort = 0xFFFFFFFFu;  // a warp's waits have not stopped
 
 template <class C>
 __device__ __forceinline__ int swz(int row) {
@@ -893,11 +895,10 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   if (!ld.done) it_load_task(ld, p);
   it_settle<C>(ld, p, t_end, r0, lane, box_shift, page_shift);
   uint32_t issued = 0, consumed = 0;
-  // Consumption index of this warp's first wait that gave up (or that it skipped because
-  // another warp of the CTA gave up); from there on it issues no load, and before leaving
-  // it waits, with a limit, for every slice it issued but did not wait for.
-  constexpr uint32_t kNoAbort = 0xFFFFFFFFu;
-  uint32_t abort_at = kNoAbort;
+  // abort_at: consumption index of this warp's first wait that gave up (or that it skipped
+  // because another warp of the CTA gave up); from there on it issues no load, and before
+  // leaving it waits, with a limit, for every slice it issued but did not wait for.
+  volatile uint32_t* abort_at = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_ABT) + cw;
   int lslot = 0;  // ring slot of the next load
   while (!ld.done && issued < (uint32_t)C::NSTAGE) {
     // (test hook: with drop_first_slice, warp 0 of every CTA leaves its first slot empty,
@@ -976,14 +977,16 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     for (int b = 0; b < C::NBLK; ++b) A.emax[b] = -1;
 
     for (int c0 = t0; c0 + r0 < t1; c0 += C::TC) {
-      if (abort_at == kNoAbort) {
-        if (*abort_flag) {
-          abort_at = consumed;
-        } else if (!mbar_wait_bounded(&bars[cslot], cpar)) {
+      bool stop = *abort_flag;  // this warp loads nothing more once set
+      if (!stop) {
+        if (!mbar_wait_bounded(&bars[cslot], cpar)) {
           *abort_flag = 1;
           if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
-          abort_at = consumed;
+          *abort_at = consumed;
+          stop = true;
         }
+      } else if (*abort_at == kNoAbort) {
+        *abort_at = consumed;
       }
       const uint8_t* kv = ring + cslot * C::SLOT_KV;
       const uint8_t* sc = scring + cslot * C::SLOT_SC;
@@ -1002,7 +1005,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         cpar ^= 1;
       }
       __syncwarp();
-      if (!ld.done && abort_at == kNoAbort) {  // refill the slot just read with the slice NSTAGE ahead
+      if (!ld.done && !stop) {  // refill the slot just read with the slice NSTAGE ahead
         issue_slice<C>(p, tmk, tmv, ring + done_slot * C::SLOT_KV, scring + done_slot * C::SLOT_SC,
                        &bars[done_slot], ld, r0, dw, lane, box_shift, page_mask);
         ++issued;
@@ -1219,7 +1222,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   }
   // Never leave while a copy into this CTA's shared memory may still be in flight (only
   // possible after a wait gave up): slice idx went to slot idx mod NSTAGE, phase idx / NSTAGE.
-  for (uint32_t idx = abort_at; idx < issued; ++idx)
+  for (uint32_t idx = *abort_at; idx < issued; ++idx)
     (void)mbar_wait_bounded(&bars[idx % C::NSTAGE], (idx / C::NSTAGE) & 1, 200000000ull);
 }
 
@@ -1235,6 +1238,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NCW * C::NSTAGE; ++i) mbar_init(&full[i], 1);
     *abort_flag = 0;
+    for (int w = 0; w < C::NCW; ++w) reinterpret_cast<uint32_t*>(smem + C::OFF_ABT)[w] = kNoAbort;
     fence_barrier_init();
   }
   __syncthreads();
