@@ -12,11 +12,11 @@ namespace pa {
 
 using CfgBf16D128M1 = TileCfg<KIND_BF16, SK_NONE, 128, 1, 8, 1, 16, 3>;
 using CfgBf16D128M2 = TileCfg<KIND_BF16, SK_NONE, 128, 2, 4, 1, 16, 4>;
-using CfgBf16D256M1 = TileCfg<KIND_BF16, SK_NONE, 256, 1, 2, 2, 16, 4>;
+using CfgBf16D256M1 = TileCfg<KIND_BF16, SK_NONE, 256, 1, 4, 2, 16, 2>;
 using CfgBf16D256M2 = TileCfg<KIND_BF16, SK_NONE, 256, 2, 2, 2, 16, 4>;
 template <int SKT> using CfgFp8D128M1 = TileCfg<KIND_FP8, SKT, 128, 1, 8, 1, 32, 3>;
 template <int SKT> using CfgFp8D128M2 = TileCfg<KIND_FP8, SKT, 128, 2, 8, 1, 16, 4>;
-template <int SKT> using CfgFp8D256M1 = TileCfg<KIND_FP8, SKT, 256, 1, 2, 2, 32, 4>;
+template <int SKT> using CfgFp8D256M1 = TileCfg<KIND_FP8, SKT, 256, 1, 4, 2, 32, 2>;
 template <int SKT> using CfgFp8D256M2 = TileCfg<KIND_FP8, SKT, 256, 2, 4, 2, 16, 3>;
 using CfgFp4D128M1 = TileCfg<KIND_FP4, SK_E8M0, 128, 1, 8, 1, 32, 5>;
 
