@@ -27,12 +27,14 @@ enum { SK_NONE = 0, SK_TENSOR = 1, SK_TOKEN = 2, SK_E8M0 = 3 };
 enum { ST_OK = 0, ST_TIMEOUT = 1, ST_CLAMPED = 2 };
 
 // TileCfg<format, scale kind, head_dim, m-tiles (query rows / 16), token groups, warps per
-// token group (head-dim split), tokens per warp slice, slots per warp ring, CTAs per SM>.
+// token group (head-dim split), tokens per warp slice, slots per warp ring, CTAs per SM,
+// a merge buffer of its own (every task merges in one pass, not only a chunk's last)>.
 template <int KIND_, int SKT_, int D_, int MT_, int NTG_, int NDW_, int TW_, int NSTAGE_,
-          int MINB_ = 1>
+          int MINB_ = 1, int MRG_ = 0>
 struct TileCfg {
   static constexpr int KIND = KIND_, SKT = SKT_, D = D_, MT = MT_, NTG = NTG_, NDW = NDW_;
   static constexpr int TW = TW_, NSTAGE = NSTAGE_, MINB = MINB_;
+  static constexpr bool MRG = MRG_ != 0;
   static constexpr bool TOK_SCALE = SKT == SK_TOKEN;                 // fp8 per-token scales
   static constexpr bool SCALES = SKT == SK_TOKEN || SKT == SK_E8M0;  // staged per slice
   static constexpr int NCW = NTG * NDW;  // warps (all compute; each loads its own slices)
@@ -77,7 +79,9 @@ struct TileCfg {
   static constexpr int OFF_FLAG = OFF_BAR + NCW * NSTAGE * 8;
   static constexpr int OFF_NXT = OFF_FLAG + 16;  // the next task's record (16 bytes)
   static constexpr int OFF_ABT = OFF_NXT + 16;  // per warp: where its waits stopped
-  static constexpr int SMEM = OFF_ABT + NCW * 4 + 1024;  // + slack to align the base to 1 KiB
+  static constexpr int OFF_MRG = (OFF_ABT + NCW * 4 + 15) / 16 * 16;
+  static constexpr int MRG_BYTES = MRG ? NCW * MT * (D / NDW / 8) * 32 * 16 : 0;
+  static constexpr int SMEM = OFF_MRG + MRG_BYTES + 1024;  // + slack to align the base to 1 KiB
   static_assert(TW % 16 == 0, "a warp slice holds whole 16-token k-chunks");
   static_assert(WBYTES % 64 == 0, "a warp row slice is whole ldmatrix.x4 groups");
   static_assert(NSUB % NDW == 0, "head-dim split on sub-tile boundaries");
@@ -1065,10 +1069,11 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       }
     }
     // The token groups' scaled accumulators are summed in group order into a buffer kept
-    // in fragment order (each lane owns float4 columns: no bank conflicts): for the last
-    // task of the chunk all groups write to the idle load ring at once and every thread
-    // sums one column over the groups; otherwise the groups add in, one at a time.  Then
-    // all threads store the rows, 4 consecutive head dims each, with coalesced writes.
+    // in fragment order (each lane owns float4 columns: no bank conflicts): all groups write
+    // at once -- into the config's own merge buffer, or for the chunk's last task into the
+    // idle load ring -- and every thread sums one column over the groups; otherwise the
+    // groups add in, one at a time.  Then all threads store the rows, 4 consecutive head
+    // dims each, with coalesced writes.
     float4* ob4 = reinterpret_cast<float4*>(obuf) + dw * (C::MT * C::NTD * 32) + lane;
     float* fin = reinterpret_cast<float*>(smem + C::OFF_FIN);
     if (tg == C::NTG - 1 && dw == 0 && t == 0) {
@@ -1083,9 +1088,9 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
                 make_float2(Mrow[mt][hr], Lrow[mt][hr]);
         }
     }
-    if (C::PAR_MERGE && task + 1 == t_end && !*abort_flag) {
+    if (C::MRG || (C::PAR_MERGE && task + 1 == t_end && !*abort_flag)) {
       constexpr int NF = C::NDW * C::MT * C::NTD * 32;  // float4 per token group
-      float4* all = reinterpret_cast<float4*>(smem + C::OFF_RING);
+      float4* all = reinterpret_cast<float4*>(smem + (C::MRG ? C::OFF_MRG : C::OFF_RING));
       float4* mine = all + tg * NF + dw * (C::MT * C::NTD * 32) + lane;
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt)
