@@ -24,6 +24,11 @@
  *   change adds next to the masking flag), query position i sees only the tokens
  *   t < L - qlen + 1 + i: the context ends with the qlen query tokens themselves, and
  *   each sees itself and what precedes it.  A position that sees no token gives zeros.
+ *   With a sliding window W > 0 (the first page lists sliding-window plans among the
+ *   variants its probe covers; the pages do not define it further), query position i,
+ *   whose own place in the context is p = L - qlen + i, sees only the tokens t > p - W:
+ *   the W tokens ending at itself, cut further by causal masking when that is set.
+ *   Tokens before every position's window (t < L - qlen - W + 1) are never read.
  *
  * Storage formats are decoded from their definitions:
  *   bf16      : the high half of an IEEE binary32
@@ -79,6 +84,7 @@ typedef struct {
   const int32_t* block_tables;
   const int32_t* context_lens;
   int32_t causal;
+  int32_t window; /* sliding window W (0: none) */
 } orc_args;
 
 /* ---- format decoders ---------------------------------------------------- */
@@ -239,6 +245,10 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
         x[(int64_t)r * n + j] = -INFINITY;
         continue;
       }
+      if (a->window > 0 && t <= L - a->qlen + r / G - a->window) { /* before its window */
+        x[(int64_t)r * n + j] = -INFINITY;
+        continue;
+      }
       double dot = 0.0;
       for (int d = 0; d < D; ++d) dot += qv[(int64_t)r * D + d] * kv[d];
       double xs = a->softmax_scale * dot;
@@ -271,6 +281,7 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
 static int check_args(const orc_args* a) {
   if (a->batch < 0 || a->qlen < 1 || a->num_kv_heads < 1 || a->num_q_heads < 1) return -1;
   if (a->causal != 0 && a->causal != 1) return -1;
+  if (a->window < 0) return -1;
   if (a->num_q_heads % a->num_kv_heads) return -1;
   if (a->head_dim < 1 || a->page_size < 1) return -1;
   if (a->kv_format == ORC_KV_MXFP4 && (a->head_dim % 32 || a->scale_kind != ORC_SCALE_E8M0))
@@ -326,7 +337,10 @@ int orc_pa_decode(const orc_args* a, double* out, int nthreads) {
 #pragma omp for schedule(dynamic, 1)
       for (int u = 0; u < units; ++u) {
         int s = u / a->num_kv_heads, hkv = u % a->num_kv_heads;
-        attend_range(a, s, hkv, 0, a->context_lens[s], m, l, o, x, qv, kv);
+        const int L = a->context_lens[s];
+        int t0 = 0; /* first token any query position's window holds */
+        if (a->window > 0 && L - a->qlen - a->window + 1 > 0) t0 = L - a->qlen - a->window + 1;
+        attend_range(a, s, hkv, t0, L, m, l, o, x, qv, kv);
         for (int r = 0; r < R; ++r) {
           int i = r / G, h = hkv * G + r % G;
           double* dst = out + ((((int64_t)s * a->qlen + i) * a->num_q_heads + h) * D);

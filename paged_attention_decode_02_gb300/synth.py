@@ -52,6 +52,9 @@ class Case:
     k_e8m0_range: Optional[tuple] = None  # MXFP4 K exponents, when they differ from V's
     causal: bool = False  # query length > 1: position i sees tokens < L - qlen + 1 + i
     q_quant: bool = False  # bf16 query quantised to e4m3 per head row by the kernel (MXFP4)
+    # sliding window W > 0: query position i (place p = L - qlen + i) sees tokens t > p - W;
+    # rows before every position's window hold the fill, like rows no sequence owns
+    window: int = 0
     pad_columns: int = 2
     extra_blocks: int = 0
     # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and
@@ -174,6 +177,10 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
             owned[blks[:-1].long()] = True
             tail = L - (n - 1) * S
             owned[int(blks[-1]), :tail] = True
+            lo = max(0, L - case.qlen - case.window + 1) if case.window > 0 else 0
+            if lo > 0:
+                owned[blks[:lo // S].long()] = False
+                owned[int(blks[lo // S]), :lo % S] = False
     own4 = owned[:, None, :].expand(NB, Hkv, S)
     frac = torch.zeros((NB, S), dtype=torch.float32)  # position / length of owned rows
     if case.ramp > 0:

@@ -126,8 +126,9 @@ def _query_dense(p: dict) -> torch.Tensor:
     return q.view(torch.float8_e4m3fn).to(torch.float64) * p["q_scale"].cpu().to(torch.float64)[..., None]
 
 
-def brute_force(p: dict, head_map=None) -> np.ndarray:
+def brute_force(p: dict, head_map=None, window=None) -> np.ndarray:
     case = p["case"]
+    W = case.window if window is None else window
     K = _dequant_dense(p, "k")
     V = _dequant_dense(p, "v")
     Q = _query_dense(p)
@@ -147,13 +148,17 @@ def brute_force(p: dict, head_map=None) -> np.ndarray:
             v = V[blk, hkv, t % S]
             for i in range(qlen):
                 x = (k @ Q[s, i, h]) * case.scale_qk()
+                seen = torch.ones(L, dtype=torch.bool)
                 if case.causal:  # position i sees the tokens before L - qlen + 1 + i
-                    seen = t < L - qlen + 1 + i
-                    if not bool(seen.any()):
-                        continue
-                    x = torch.where(seen, x, torch.tensor(-math.inf, dtype=x.dtype))
+                    seen &= t < L - qlen + 1 + i
+                if W > 0:  # and, in a window, the W tokens that end at its own place
+                    seen &= t > (L - qlen + i) - W
+                if not bool(seen.any()):
+                    continue
+                # unseen rows may hold NaN: select, never multiply
+                x = torch.where(seen, x, torch.tensor(-math.inf, dtype=x.dtype))
                 w = torch.softmax(x, dim=0)
-                out[s, i, h] = w @ v
+                out[s, i, h] = torch.where(seen[:, None], v, torch.zeros_like(v)).mul(w[:, None]).sum(0)
     return out.numpy()
 
 
@@ -176,6 +181,20 @@ def _tiny_cases():
                    qlen=4, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
                    context_lens=[2, 4, 17, 40], fill=synth.FILL_NAN, seed=17, kv_std=20.0,
                    causal=True),
+        synth.Case("t_bf16_window", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3,
+                   qlen=1, num_kv_heads=1, num_q_heads=4, head_dim=64, page_size=16,
+                   context_lens=[3, 40, 77], fill=synth.FILL_NAN, seed=18, window=20),
+        synth.Case("t_fp8_window_q4", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+                   qlen=4, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+                   context_lens=[2, 9, 33, 70], fill=synth.FILL_NAN, seed=19, kv_std=20.0,
+                   window=7),
+        synth.Case("t_fp8_window_causal", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16,
+                   batch=4, qlen=3, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,
+                   context_lens=[1, 5, 18, 60], fill=synth.FILL_INF, seed=20, kv_std=20.0,
+                   causal=True, window=5),
+        synth.Case("t_mxfp4_window", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_E4M3, batch=2,
+                   qlen=1, num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
+                   context_lens=[20, 45], fill=synth.FILL_RANDOM, seed=24, window=17),
     ]
 
 
@@ -281,6 +300,65 @@ def test_causal_position_sees_the_context_up_to_itself():
         ref = util.oracle_decode(pi)
         assert np.array_equal(got[:, i], ref[:, i]), i
     assert np.all(got[0, :2] == 0.0)  # L = 2 < qlen: the first two positions see nothing
+
+
+def test_window_of_one_is_the_positions_own_v_row():
+    # W = 1 with causal masking: every query position sees exactly the token at its own
+    # place L - qlen + i; without it, position i sees [L - qlen + i, L), and only the last
+    # one a single token
+    qlen = 3
+    for causal in (False, True):
+        case = synth.Case("w1", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=2,
+                          qlen=qlen, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,
+                          context_lens=[5, 33], fill=synth.FILL_NAN, seed=61, kv_std=20.0,
+                          causal=causal, window=1)
+        p = synth.make(case)
+        got = util.oracle_decode(p)
+        V = _dequant_dense(p, "v")
+        for s, L in enumerate([5, 33]):
+            for i in range(qlen) if causal else [qlen - 1]:
+                t = L - qlen + i
+                want = V[int(p["block_tables"][s, t // 16]), 0, t % 16].numpy()
+                for h in range(2):
+                    assert np.array_equal(got[s, i, h], want), (causal, s, i)
+
+
+def test_window_wider_than_the_context_changes_nothing():
+    for causal in (False, True):
+        case = synth.Case("ww", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3, qlen=2,
+                          num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                          context_lens=[1, 17, 50], seed=62, causal=causal)
+        p = synth.make(case)
+        pw = dict(p)
+        pw["case"] = synth.replace(case, window=51)  # = L_max + qlen - 1: holds every token
+        assert np.array_equal(util.oracle_decode(pw), util.oracle_decode(p))
+
+
+def test_window_equals_attention_over_its_token_range():
+    # one query position: the window [L - W, L) through the range entry point of the same
+    # cache without a window (a separate path of the oracle: an explicit token range)
+    W = 23
+    case = synth.Case("wr", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=3, qlen=1,
+                      num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+                      context_lens=[10, 40, 90], fill=synth.FILL_ZERO, seed=63, kv_std=20.0)
+    p = synth.make(case)
+    pw = dict(p)
+    pw["case"] = synth.replace(case, window=W)
+    got = util.oracle_decode(pw)
+    plain = util.oracle_problem(p)
+    for s, L in enumerate([10, 40, 90]):
+        for hkv in range(2):
+            _, _, o = plain.attend_range(s, hkv, max(0, L - W), L)
+            np.testing.assert_array_equal(got[s, 0, 4 * hkv:4 * hkv + 4], o.reshape(4, 64))
+
+
+def test_window_pins_catch_off_by_one():
+    # a window one token wider or narrower is a different result on this data
+    case = [c for c in _tiny_cases() if c.name == "t_fp8_window_q4"][0]
+    p = synth.make(synth.replace(case, fill=synth.FILL_ZERO))
+    got = util.oracle_decode(p)
+    for w in (case.window - 1, case.window + 1):
+        assert util.rel_l2(got, brute_force(p, window=w)) > 1e-3, w
 
 
 def test_e4m3_rounding_matches_torch():
