@@ -141,10 +141,19 @@ typedef struct pa_decode_args {
    * sees none gets a zero row).  The first page notes such a causal option, added by a
    * later change next to the masking flag.  bf16 and fp8 caches; MXFP4 takes qlen 1. */
   int32_t causal;
+  /* Sliding window W >= 0 (0: none).  With W > 0, query position i, whose own place in the
+   * context is p = context_len - qlen + i, sees only the tokens t > p - W: the W tokens
+   * ending at itself (cut further by `causal` when that is set).  The first page lists
+   * sliding-window plans among the variants its probe covers and defines them no further;
+   * this is the plain reading.  Tokens before every position's window have no effect,
+   * whatever their bytes: pages holding none of a window's tokens are not loaded, and
+   * their block-table entries are never used as addresses.  Every format; the tcgen05
+   * kernel does not take a window (the tile kernel runs).  Negative: PA_ERR_INVALID_ARG. */
+  int32_t sliding_window;
 } pa_decode_args;
 
 /* ABI version of this header; a mismatched library refuses nothing but reports it here. */
-#define PA_DECODE_ABI_VERSION 2
+#define PA_DECODE_ABI_VERSION 3
 int32_t pa_decode_abi_version(void);
 
 /* Bytes of workspace the three calls need for these shapes (plan, partition scratch,

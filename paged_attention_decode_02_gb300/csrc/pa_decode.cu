@@ -34,6 +34,16 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int* clamped) {
   return L;
 }
 
+// Tiles of a (sequence, KV head) unit: [*first, ceil(L / 256)), where *first is the tile
+// holding the first token that any query position's sliding window reaches (0 without a
+// window).  Returns the count.
+__device__ __forceinline__ int unit_tiles(int L, int qlen, int window, int* first) {
+  int lo = window > 0 ? L - qlen - window + 1 : 0;
+  lo = lo > 0 ? lo : 0;
+  *first = lo / kTileTokens;
+  return (L + kTileTokens - 1) / kTileTokens - *first;
+}
+
 template <typename T>
 __device__ T block_exclusive_scan(T v, T* total, T* sh) {  // sh: >= 32 elements
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -118,10 +128,15 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   }
   __syncthreads();
   int clamped = 0, lmax = 0, n_own = 0;  // n_own: tiles of sequence tid (one round of sequences)
+  int f_own = 0;                          // and the first of them
   long long local = 0;
   for (int s = tid; s < pp.B; s += blockDim.x) {
-    const int n = (clamp_len(pp.ctx[s], cap, &clamped) + kTileTokens - 1) / kTileTokens;
-    if (s == tid) n_own = n;
+    int f;
+    const int n = unit_tiles(clamp_len(pp.ctx[s], cap, &clamped), pp.qlen, pp.window, &f);
+    if (s == tid) {
+      n_own = n;
+      f_own = f;
+    }
     local += n;
     lmax = n > lmax ? n : lmax;
   }
@@ -148,10 +163,15 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   int carry_tasks = 0, carry_slots = 0, carry_chunk = -1;  // chunk of the last task so far
   for (int base = 0; base < pp.B; base += blockDim.x) {
     const int s = base + tid;
-    int n = 0;
+    int n = 0, first = 0;
     if (s < pp.B) {
       int dummy = 0;
-      n = base == 0 ? n_own : (clamp_len(pp.ctx[s], cap, &dummy) + kTileTokens - 1) / kTileTokens;
+      if (base == 0) {
+        n = n_own;
+        first = f_own;
+      } else {
+        n = unit_tiles(clamp_len(pp.ctx[s], cap, &dummy), pp.qlen, pp.window, &first);
+      }
     }
     long long round_tiles;
     const long long before = block_exclusive_scan<long long>((long long)n, &round_tiles, sh64);
@@ -193,6 +213,8 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
           tk.seq = s;
           tk.hkv_part = h | (q << 16);
           unit_part(cg, U, n, q, &tk.tile_begin, &tk.tile_end, &chunk);
+          tk.tile_begin += first;
+          tk.tile_end += first;
           pp.tasks[t] = tk;
           pp.task_chunk[t] = chunk;
           for (int k = prev + 1; k <= chunk; ++k) pp.chunk_first[k] = t;
@@ -394,6 +416,7 @@ pa_status validate(const pa_decode_args* a) {
   if (a->q_dtype == PA_Q_BF16_TO_E4M3 && a->kv_dtype != PA_KV_MXFP4) return PA_ERR_UNSUPPORTED;
   if (a->merge_in_decode != 0 && a->merge_in_decode != 1) return PA_ERR_INVALID_ARG;
   if (a->causal != 0 && a->causal != 1) return PA_ERR_INVALID_ARG;
+  if (a->sliding_window < 0) return PA_ERR_INVALID_ARG;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
@@ -449,14 +472,15 @@ pa_status split_params(const pa_decode_args* a, int* budget, int* maxp) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
-// and pages of at least 8 tokens, with the separate reduce, not causal.  It runs when
-// PA_DECODE_KERNEL=tc is set in the environment (read at each call); otherwise every
-// shape runs the mma.sync kernel, the faster of the two on the long-context workloads.
+// and pages of at least 8 tokens, with the separate reduce, not causal and without a
+// sliding window.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
+// each call); otherwise every shape runs the mma.sync kernel, the faster of the two on
+// the long-context workloads.
 bool tc_kernel_applies(const pa_decode_args* a, int rows) {
   const char* e = getenv("PA_DECODE_KERNEL");
   const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
   return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
-         !(a->causal && a->qlen > 1) && a->q_dtype != PA_Q_BF16_TO_E4M3;
+         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && a->q_dtype != PA_Q_BF16_TO_E4M3;
 }
 
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
@@ -578,6 +602,8 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   pp.Hkv = a->num_kv_heads;
   pp.W = a->max_blocks_per_seq;
   pp.S = a->page_size;
+  pp.qlen = a->qlen;
+  pp.window = a->sliding_window;
   pp.max_partitions = L.max_partitions;
   pp.budget = L.budget;
   pp.ctx = a->context_lens;
@@ -631,6 +657,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.B = a->batch;
   p.qlen = a->qlen;
   p.causal = a->causal && a->qlen > 1;
+  p.window = a->sliding_window;
   p.Hq = a->num_q_heads;
   p.Hkv = a->num_kv_heads;
   p.G = G;

@@ -47,6 +47,7 @@ struct DecodeParams {
   float scale_log2;  // softmax_scale * log2(e)
   int q_fp8, q_scale_per_row, scale_kind;
   int causal;  // qlen > 1: query position i sees tokens < L - qlen + 1 + i
+  int window;  // > 0: query position i sees tokens > L - qlen + i - window
   int q_quant;  // bf16 query quantised per head row to e4m3 (scale amax / 448)
   int drop_first_slice;  // test hook: warp 0 of each CTA never loads its first slice
   const void* q;
@@ -73,6 +74,7 @@ struct DecodeParams {
 
 struct PlanParams {
   int B, Hkv, W, S;
+  int qlen, window;  // a unit's tiles start at the first tile any position's window holds
   int max_partitions;
   int budget;
   const int32_t* ctx;

@@ -312,6 +312,7 @@ __device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C
 // held by lanes 0..nbox-1) so that no refill waits on a dependent global load.
 struct SliceIt {
   int task, c0, t0, t1, s, hkv, L;
+  int lo;  // first token of the lowest query position's sliding window (0: none)
   const int32_t* btrow;
   int blk;
   bool done;
@@ -323,6 +324,8 @@ __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p)
   it.s = tk.seq;
   it.hkv = tk.hkv_part & 0xFFFF;
   it.L = clamped_context(p, it.s);
+  it.lo = p.window > 0 ? it.L - p.qlen - p.window + 1 : 0;
+  it.lo = it.lo > 0 ? it.lo : 0;
   it.c0 = tk.tile_begin * kTileTokens;
   it.t0 = it.c0;
   const int t1 = tk.tile_end * kTileTokens;
@@ -375,6 +378,8 @@ __device__ __forceinline__ void it_settle(SliceIt& it, const DecodeParams& p, in
 
 // Issue the TMA / bulk copies of one warp slice (tokens [a, min(a + TW, L)) of the
 // iterator's sequence and KV head) into ring slot `kv` / `sc`, completing on `bar`.
+// Boxes that end at or before the first token of any sliding window are not loaded
+// (their slot rows keep stale bytes, which the masked path never lets through).
 template <class C>
 __device__ __forceinline__ void issue_slice(const DecodeParams& p, const CUtensorMap* tmk,
                                             const CUtensorMap* tmv, uint8_t* kv, uint8_t* sc,
@@ -384,11 +389,13 @@ __device__ __forceinline__ void issue_slice(const DecodeParams& p, const CUtenso
   const int ntok = (it.L - a) < C::TW ? (it.L - a) : C::TW;
   const int box = 1 << box_shift;
   const int nbox = (ntok + box - 1) >> box_shift;
+  int fbox = it.lo > a ? (it.lo - a) >> box_shift : 0;  // boxes wholly before the window
+  fbox = fbox < nbox ? fbox : nbox;
   if (lane == 0)
-    mbar_arrive_expect_tx(
-        bar, (uint32_t)((nbox << box_shift) * (2 * C::NSUBW * C::SUB + (C::SCALES ? 8 : 0))));
+    mbar_arrive_expect_tx(bar, (uint32_t)(((nbox - fbox) << box_shift) *
+                                          (2 * C::NSUBW * C::SUB + (C::SCALES ? 8 : 0))));
   __syncwarp();
-  if (lane < nbox) {
+  if (lane >= fbox && lane < nbox) {
     fence_proxy_async();  // the slot was last read through the generic proxy
     const int tok = a + (lane << box_shift);
     int blk = it.blk;
@@ -454,17 +461,20 @@ __device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4]
 }
 
 // One slice of one warp: QK^T, online softmax, PV over the slice's tokens.  MASKED is
-// the boundary path (tokens >= vw are unowned); full slices run no masking instruction.
+// the boundary path (tokens >= vw are unowned; with a sliding window, tokens before
+// wl - (qm1 - i) are outside query position i's window, and tokens before wl - qm1 are
+// outside every window); full slices run no masking instruction.
 template <class C, bool MASKED>
 __device__ __forceinline__ void stage_compute(
     WarpAcc<C>& A, const uint8_t* kv, const uint8_t* sc, uint8_t* smem, int vw, int lane, int dw,
     int tg, const uint32_t (&qa)[C::Q_IN_REGS ? C::MT : 1][C::Q_IN_REGS ? C::NKCH : 1][4],
     const uint16_t* qs, const float (&crow)[C::MT][2], const uint32_t (&koff)[C::NGRP],
-    const uint32_t (&voff)[C::NCP], int cw, int& xbuf, int cq, int G) {
+    const uint32_t (&voff)[C::NCP], int cw, int& xbuf, int cq, int G, int wl, int qm1) {
   constexpr bool tok_scale = C::TOK_SCALE;
   const int g = lane >> 2, t = lane & 3;
   const uint32_t kbase = smem_u32(kv);
   const uint32_t vbase = kbase + C::SLOT_V;
+  const int vlo = wl - qm1;  // tokens before vlo: outside every window (stale slot rows)
   const float* ksc = reinterpret_cast<const float*>(sc);
   const float* vsc = reinterpret_cast<const float*>(sc + 4 * C::TW);
   const uint32_t* kex = reinterpret_cast<const uint32_t*>(sc);
@@ -483,7 +493,8 @@ __device__ __forceinline__ void stage_compute(
     // |v_scale| of owned tokens; non-negative floats order like their bit patterns.  The
     // reference moves only when a token passes it by more than kLazyVref: one vote decides,
     // the maximum is reduced only then.
-    const float vs = (lane < C::TW && (!MASKED || lane < vw)) ? fabsf(vsc[lane]) : 0.f;
+    const float vs =
+        (lane < C::TW && (!MASKED || (lane < vw && lane >= vlo))) ? fabsf(vsc[lane]) : 0.f;
     if (__any_sync(0xffffffffu, vs > A.vref * kLazyVref)) {
       const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vs)));
       beta[0] = A.vref / mx;
@@ -618,7 +629,7 @@ __device__ __forceinline__ void stage_compute(
   }
   // ---------------- MXFP4 V references (lazy) and factor table ----------------
   if constexpr (C::KIND == KIND_FP4) {
-    const bool own = !MASKED || lane < vw;  // one lane per slice token
+    const bool own = !MASKED || (lane < vw && lane >= vlo);  // one lane per slice token
     const uint32_t vwd = vex[lane];
     // A reference moves when none is set yet or a token's exponent passes it by more than
     // kLazyExp: one vote decides; the block maxima are reduced only then.
@@ -650,14 +661,16 @@ __device__ __forceinline__ void stage_compute(
 
   // ---------------- logits and boundary mask ----------------
   // Row limits: tokens at or past vw are unowned; with causal masking (cq = qlen - 1 > 0)
-  // query position i = row / G sees only the tokens before vw - (cq - i).
-  int lim[C::MT][2];
+  // query position i = row / G sees only the tokens before vw - (cq - i), and with a
+  // sliding window only those from wl - (qm1 - i) on.
+  int lim[C::MT][2], low[C::MT][2];
 #pragma unroll
   for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int i = (16 * mt + g + 8 * hr) / G;
       lim[mt][hr] = MASKED ? vw - (cq > i ? cq - i : 0) : vw;
+      low[mt][hr] = MASKED ? wl - (qm1 - i) : 0;
     }
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
@@ -670,7 +683,8 @@ __device__ __forceinline__ void stage_compute(
       for (int j = 0; j < 4; ++j) {
         float x = sacc[mt][nt][j] * crow[mt][j >> 1];
         if constexpr (tok_scale) x *= (j & 1) ? ks.y : ks.x;
-        if (MASKED && tk0 + (j & 1) >= lim[mt][j >> 1]) x = -INFINITY;
+        if (MASKED && (tk0 + (j & 1) >= lim[mt][j >> 1] || tk0 + (j & 1) < low[mt][j >> 1]))
+          x = -INFINITY;
         sacc[mt][nt][j] = x;
       }
   }
@@ -744,9 +758,11 @@ __device__ __forceinline__ void stage_compute(
     if (MASKED && 16 * kc >= vw) break;
     const int tb = 16 * kc + 2 * t;  // tokens tb, tb+1 (low pair) and tb+8, tb+9 (high pair)
     uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+    // a token's V row passes if it is owned and inside some window
+    auto in = [&](int x) { return x < vw && x >= vlo; };
     if (MASKED) {
-      mlo = (tb < vw ? 0x0000FFFFu : 0u) | (tb + 1 < vw ? 0xFFFF0000u : 0u);
-      mhi = (tb + 8 < vw ? 0x0000FFFFu : 0u) | (tb + 9 < vw ? 0xFFFF0000u : 0u);
+      mlo = (in(tb) ? 0x0000FFFFu : 0u) | (in(tb + 1) ? 0xFFFF0000u : 0u);
+      mhi = (in(tb + 8) ? 0x0000FFFFu : 0u) | (in(tb + 9) ? 0xFFFF0000u : 0u);
     }
     uint32_t pa[C::MT][4];
 #pragma unroll
@@ -761,10 +777,10 @@ __device__ __forceinline__ void stage_compute(
       } else if constexpr (tok_scale) {
         const float2 a = *reinterpret_cast<const float2*>(vsc + tb);
         const float2 c = *reinterpret_cast<const float2*>(vsc + tb + 8);
-        const float vf0 = (MASKED && tb >= vw) ? 0.f : a.x * vinv;
-        const float vf1 = (MASKED && tb + 1 >= vw) ? 0.f : a.y * vinv;
-        const float vf2 = (MASKED && tb + 8 >= vw) ? 0.f : c.x * vinv;
-        const float vf3 = (MASKED && tb + 9 >= vw) ? 0.f : c.y * vinv;
+        const float vf0 = (MASKED && !in(tb)) ? 0.f : a.x * vinv;
+        const float vf1 = (MASKED && !in(tb + 1)) ? 0.f : a.y * vinv;
+        const float vf2 = (MASKED && !in(tb + 8)) ? 0.f : c.x * vinv;
+        const float vf3 = (MASKED && !in(tb + 9)) ? 0.f : c.y * vinv;
         pa[mt][0] = pack_f16x2(pl[0] * vf0, pl[1] * vf1);
         pa[mt][1] = pack_f16x2(pl[2] * vf0, pl[3] * vf1);
         pa[mt][2] = pack_f16x2(ph[0] * vf2, ph[1] * vf3);
@@ -920,6 +936,9 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   int xbuf = 0;
   // tokens a query position may not see past (MXFP4 takes one query position: none)
   const int cq = (C::KIND != KIND_FP4 && p.causal) ? p.qlen - 1 : 0;
+  const int qm1 = C::KIND != KIND_FP4 ? p.qlen - 1 : 0;
+  // a slice runs the full path only if it starts inside every position's window
+  const int wcap = p.window > 0 ? p.window : 0x7FFFFFFF;
 
   for (int task = t_begin; task < t_end; ++task) {
     const PlanTask tk = p.tasks[task];
@@ -995,12 +1014,14 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       const uint8_t* kv = ring + cslot * C::SLOT_KV;
       const uint8_t* sc = scring + cslot * C::SLOT_SC;
       const int vw = L - (c0 + r0);  // owned tokens in the slice (> 0 here)
-      if (vw - cq >= C::TW) {
+      if (vw - cq >= C::TW && vw <= wcap) {
         stage_compute<C, false>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
-                                xbuf, cq, p.G);
+                                xbuf, cq, p.G, 0, qm1);
       } else {
+        // the last query position's window starts at slice token vw - window
+        const int wl = p.window > 0 ? vw - p.window : -0x40000000;
         stage_compute<C, true>(A, kv, sc, smem, vw, lane, dw, tg, qa, qs, crow, koff, voff, cw,
-                               xbuf, cq, p.G);
+                               xbuf, cq, p.G, wl, qm1);
       }
       const int done_slot = cslot;
       ++consumed;

@@ -51,6 +51,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("bt_stride", ctypes.c_int64), ("context_lens", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
         ("out_stride_head", ctypes.c_int64), ("causal", ctypes.c_int32),
+        ("sliding_window", ctypes.c_int32),
     ]
 
 
@@ -120,7 +121,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
               max_partitions: int = 0, task_budget: int = 0,
               merge_in_decode: bool = False, causal: bool = False,
-              q_quant: bool = False) -> PaDecodeArgs:
+              q_quant: bool = False, sliding_window: int = 0) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -129,6 +130,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     (uint8 / float8_e4m3fn) with fp32 scales [1] (per tensor) or [NB, Hkv, S]
     (per token), or [NB, Hkv, S, D/2] uint8 MXFP4 with uint8 e8m0 scales
     [NB, Hkv, S, D/32].  block_tables int32 [B, W]; context_lens int32 [B].
+    causal: query position i sees tokens < L - qlen + 1 + i.  sliding_window W > 0: query
+    position i sees only tokens > L - qlen + i - W.
     """
     D = query.shape[-1]
     Hq = query.shape[-2]
@@ -167,6 +170,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
     a.merge_in_decode = int(bool(merge_in_decode))
     a.causal = int(bool(causal))
+    a.sliding_window = int(sliding_window)
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
@@ -274,7 +278,8 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      value_scale=problem["value_scale"], q_scale=problem["q_scale"],
                      softmax_scale=case.scale_qk(), max_partitions=max_partitions,
                      task_budget=task_budget, merge_in_decode=merge_in_decode,
-                     causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False))
+                     causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False),
+                     sliding_window=getattr(case, "window", 0))
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -1,7 +1,9 @@
 """The work split that pa_decode_plan builds, restated on the host for tests.
 
-Units are (sequence, KV head) pairs in sequence-major order, each with ceil(L/256)
-tiles.  The units are laid end to end on a line, each as a gap of UNIT_COST positions
+Units are (sequence, KV head) pairs in sequence-major order, each with the tiles
+[first, ceil(L/256)), where first is the tile holding the first token any query
+position's sliding window reaches (0 without a window).  Task tile ranges carry that
+offset.  The units are laid end to end on a line, each as a gap of UNIT_COST positions
 (the fixed cost of a task) followed by its tiles, and the line is cut into `budget`
 chunks of C positions (C = ceil(length / budget), raised when needed so that no unit
 touches more than max_partitions chunks); a unit becomes one partition per chunk its
@@ -24,8 +26,18 @@ def _align(x, a=256):
     return (x + a - 1) // a * a
 
 
-def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_COST):
-    tiles = [(min(max(int(L), 0), cap_tokens) + TILE - 1) // TILE for L in context_lens]
+def unit_tiles(L, qlen=1, window=0):
+    """(first tile, tile count) of a unit with context L."""
+    lo = max(0, L - qlen - window + 1) if window > 0 else 0
+    first = lo // TILE
+    return first, (L + TILE - 1) // TILE - first
+
+
+def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_COST, qlen=1,
+         window=0):
+    clamped = [min(max(int(L), 0), cap_tokens) for L in context_lens]
+    firsts = [unit_tiles(L, qlen, window)[0] for L in clamped]
+    tiles = [unit_tiles(L, qlen, window)[1] for L in clamped]
     total = (sum(tiles) + unit_cost * len(tiles)) * hkv  # length of the line
     maxt = max(tiles, default=0)
     C = max(1, -(-total // budget))
@@ -48,7 +60,7 @@ def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_C
             if len(pieces) >= 2:
                 slot += len(pieces)
             for q, (b, e, c) in enumerate(pieces):
-                tasks.append((s, h | (q << 16), b, e))
+                tasks.append((s, h | (q << 16), b + firsts[s], e + firsts[s]))
                 chunks.append(c)
             U += n
     first = [len(tasks)] * (budget + 1)
@@ -57,7 +69,7 @@ def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_C
         for k in range(prev + 1, c + 1):
             first[k] = t
         prev = c
-    return {"tiles": tiles, "C": C, "nchunks": nchunks, "tasks": tasks, "chunks": chunks,
+    return {"tiles": tiles, "firsts": firsts, "C": C, "nchunks": nchunks, "tasks": tasks, "chunks": chunks,
             "nparts": nparts, "part_base": part_base, "chunk_first": first, "slots": slot,
             "length": total, "unit_pos": unit_pos, "hkv": hkv, "unit_cost": unit_cost}
 

@@ -29,14 +29,16 @@ def test_header_declarations_are_exported(lib):
     assert set(ops.EXPORTED) == set(names), names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.pa_decode_abi_version() == 2
+    assert lib.pa_decode_abi_version() == 3
 
 
 def test_args_struct_layout_matches_header():
-    # 16 int32/float fields, then 19 pointers and int64s, then the causal flag (padded)
+    # 16 int32/float fields, then 19 pointers and int64s, then the causal flag and the
+    # sliding window
     assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 20 * 8
     assert ops.PaDecodeArgs.query.offset == 64
     assert ops.PaDecodeArgs.causal.offset == 64 + 19 * 8
+    assert ops.PaDecodeArgs.sliding_window.offset == 64 + 19 * 8 + 4
 
 
 def _valid_args():
@@ -76,6 +78,7 @@ REFUSED = [
      ops.PA_ERR_UNSUPPORTED),
     ("unknown kv dtype", dict(kv_dtype=7), ops.PA_ERR_INVALID_ARG),
     ("merge flag not 0/1", dict(merge_in_decode=2), ops.PA_ERR_INVALID_ARG),
+    ("negative sliding window", dict(sliding_window=-1), ops.PA_ERR_INVALID_ARG),
     ("null query", dict(query=None), ops.PA_ERR_INVALID_ARG),
     ("null scales", dict(key_scale=None), ops.PA_ERR_INVALID_ARG),
     ("e4m3 query without scale", dict(q_dtype=ops.PA_Q_FP8_E4M3), ops.PA_ERR_INVALID_ARG),

@@ -146,6 +146,60 @@ def test_causal_runs_on_the_mma_kernel_when_tcgen05_is_requested(monkeypatch):
     util.assert_parity(run_gpu(p, task_budget=24), util.oracle_decode(p), case.kv, case.name)
 
 
+WINDOW = [
+    synth.Case("window_fp8_token", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=5,
+               qlen=1, num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[1, 17, 300, 2000, 5000], seed=2901, kv_std=20.0, window=1000),
+    synth.Case("window_fp8_token_q4", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+               qlen=4, num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[2, 40, 257, 900], seed=2902, kv_std=20.0, window=37),
+    synth.replace(synth.config2("b", batch=5, seed=2903), causal=True, window=500),
+    synth.replace(synth.config1(context_lens=[17, 257, 3000], batch=3, seed=2904), window=100),
+    synth.Case("window_bf16_d256_causal", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
+               batch=3, qlen=2, num_kv_heads=1, num_q_heads=8, head_dim=256, page_size=64,
+               context_lens=[3, 500, 1500], seed=2905, causal=True, window=64),
+    synth.replace(synth.config3(qlen=4, batch=3, context_lens=(200, 900), seed=2906),
+                  window=333),
+    synth.replace(synth.config4(batch=8, seed=2907), window=600),
+    synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2908),
+                  window=2048),
+    synth.Case("window_one", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=3,
+               qlen=3, num_kv_heads=1, num_q_heads=8, head_dim=128, page_size=16,
+               context_lens=[1, 50, 700], fill=synth.FILL_INF, seed=2909, kv_std=20.0,
+               causal=True, window=1),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW, ids=lambda c: f"{c.name}-w{c.window}")
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_sliding_window_matches_oracle(case, mode):
+    # query position i sees tokens > L - qlen + i - W; rows before every window hold the
+    # unowned fill (NaN, +-448, random bytes with e8m0 255) and must have no effect
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name + " window")
+
+
+@pytest.mark.parametrize("case", [WINDOW[0], WINDOW[2], WINDOW[6]], ids=lambda c: c.name)
+def test_window_wider_than_every_context_is_bitwise_no_window(case):
+    # the same plan, the same slices on the same paths: the same bits
+    p = synth.make(synth.replace(case, window=0))
+    plain = run_gpu(p, task_budget=24)
+    pw = dict(p)
+    pw["case"] = synth.replace(case, window=int(p["context_lens"].max()) + case.qlen)
+    assert np.array_equal(run_gpu(pw, task_budget=24), plain)
+
+
+def test_window_on_the_long_context_workload_sampled():
+    case = synth.replace(synth.config5(synth.KV_FP8, batch=4, seed=2910), window=32768)
+    p = synth.make(case)
+    got = run_gpu(p)
+    seqs = [0, 3]
+    util.assert_parity(got[seqs], util.oracle_decode(p, seqs=seqs), case.kv, case.name)
+    assert np.isfinite(got).all()
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),

@@ -23,15 +23,24 @@ MIXES = [
 ]
 BUDGETS = [1, 7, 152, 304]
 MAXP = [1, 2, 3, 128]
+# (query length, sliding window): none, and windows that start inside the first tiles,
+# at a tile edge, and far into long contexts
+WINDOWS = [(1, 0), (4, 3000), (1, 256), (2, 70000)]
 
 
 @pytest.mark.parametrize("name,lens,hkv", MIXES, ids=[m[0] for m in MIXES])
 @pytest.mark.parametrize("budget", BUDGETS)
 @pytest.mark.parametrize("maxp", MAXP)
-def test_plan_arithmetic(name, lens, hkv, budget, maxp):
+@pytest.mark.parametrize("qlen,window", WINDOWS, ids=[f"q{q}w{w}" for q, w in WINDOWS])
+def test_plan_arithmetic(name, lens, hkv, budget, maxp, qlen, window):
     cap = 1 << 20
-    m = pm.plan(lens, hkv, budget, maxp, cap)
+    m = pm.plan(lens, hkv, budget, maxp, cap, qlen=qlen, window=window)
     tiles = m["tiles"]
+    # a unit starts at the tile of the first token that any query position's window holds
+    for s, L in enumerate(lens):
+        lo = max(0, L - qlen - window + 1) if window > 0 else 0
+        assert m["firsts"][s] == lo // pm.TILE
+        assert m["firsts"][s] + tiles[s] == (L + pm.TILE - 1) // pm.TILE
     # every tile of every unit exactly once, partitions in order and contiguous
     by_unit = {}
     for (s, hp, b, e) in m["tasks"]:
@@ -39,7 +48,8 @@ def test_plan_arithmetic(name, lens, hkv, budget, maxp):
     assert len(by_unit) == len(lens) * hkv
     for (s, h), parts in by_unit.items():
         assert [q for q, _, _ in parts] == list(range(len(parts)))
-        assert parts[0][1] == 0 and parts[-1][2] == tiles[s]
+        f = m["firsts"][s]
+        assert parts[0][1] == f and parts[-1][2] == f + tiles[s]
         for (_, _, e0), (_, b1, _) in zip(parts, parts[1:]):
             assert e0 == b1
         assert all(e > b for _, b, e in parts) or tiles[s] == 0
@@ -64,7 +74,7 @@ def test_plan_arithmetic(name, lens, hkv, budget, maxp):
             unit_of[(u // hkv, u % hkv)] = pos
         for (s, hp, b, e), c in zip(m["tasks"], m["chunks"]):
             if e > b:
-                pos = unit_of[(s, hp & 0xFFFF)]
+                pos = unit_of[(s, hp & 0xFFFF)] - m["firsts"][s]
                 assert c * C <= pos + b and pos + e <= (c + 1) * C
         per = pm.chunk_tiles(m)
         assert per.max(initial=0) <= C
@@ -96,7 +106,8 @@ def test_plan_balance_long_context():
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,lens,hkv", MIXES, ids=[m[0] for m in MIXES])
 @pytest.mark.parametrize("budget,maxp", [(152, 128), (7, 3), (304, 1), (1, 2)])
-def test_device_plan_matches_model(name, lens, hkv, budget, maxp):
+@pytest.mark.parametrize("window", [0, 3000])
+def test_device_plan_matches_model(name, lens, hkv, budget, maxp, window):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     from paged_attention_decode_02_gb300 import build, ops
@@ -105,17 +116,19 @@ def test_device_plan_matches_model(name, lens, hkv, budget, maxp):
     B = len(lens)
     S, W, D = 128, max(1, (max(lens) + 127) // 128), 128
     dev = "cuda"
-    q = torch.zeros(B, 1, 8 * hkv, D, dtype=torch.bfloat16, device=dev)
+    qlen = 2 if window else 1
+    q = torch.zeros(B, qlen, 8 * hkv, D, dtype=torch.bfloat16, device=dev)
     kc = torch.zeros(2, hkv, S, D, dtype=torch.bfloat16, device=dev)
     bt = torch.zeros(B, W, dtype=torch.int32, device=dev)
     ctx = torch.tensor(lens, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
-    args = ops.make_args(q, kc, kc, bt, ctx, out, max_partitions=maxp, task_budget=budget)
+    args = ops.make_args(q, kc, kc, bt, ctx, out, max_partitions=maxp, task_budget=budget,
+                         sliding_window=window)
     ws = ops.alloc_workspace(args)
     ops.pa_decode_plan(args, ws)
     torch.cuda.synchronize()
     got = pm.read_workspace(ws.cpu().numpy(), B, hkv, budget)
-    m = pm.plan(lens, hkv, budget, maxp, W * S)
+    m = pm.plan(lens, hkv, budget, maxp, W * S, qlen=qlen, window=window)
     assert got["ntasks"] == len(m["tasks"])
     assert got["tasks"] == m["tasks"]
     assert got["chunks"] == m["chunks"]
