@@ -334,19 +334,27 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
 // tile kernel that serves a format / head_dim / query-row count.
 void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub) {
   if (kind == KIND_BF16) {
-    if (head_dim == 128) {
+    if (head_dim == 64) {
+      *tw = rows <= 16 ? CfgBf16D64M1::TW : CfgBf16D64M2::TW;
+      *sub = CfgBf16D64M1::SUB;
+    } else if (head_dim == 128) {
       *tw = rows <= 16 ? CfgBf16D128M1::TW : CfgBf16D128M2::TW;
+      *sub = CfgBf16D128M1::SUB;
     } else {
       *tw = rows <= 16 ? CfgBf16D256M1::TW : CfgBf16D256M2::TW;
+      *sub = CfgBf16D256M1::SUB;
     }
-    *sub = 128;
   } else if (kind == KIND_FP8) {
-    if (head_dim == 128) {
+    if (head_dim == 64) {
+      *tw = rows <= 16 ? CfgFp8D64M1<SK_TOKEN>::TW : CfgFp8D64M2<SK_TOKEN>::TW;
+      *sub = CfgFp8D64M1<SK_TOKEN>::SUB;
+    } else if (head_dim == 128) {
       *tw = rows <= 16 ? CfgFp8D128M1<SK_TOKEN>::TW : CfgFp8D128M2<SK_TOKEN>::TW;
+      *sub = CfgFp8D128M1<SK_TOKEN>::SUB;
     } else {
       *tw = rows <= 16 ? CfgFp8D256M1<SK_TOKEN>::TW : CfgFp8D256M2<SK_TOKEN>::TW;
+      *sub = CfgFp8D256M1<SK_TOKEN>::SUB;
     }
-    *sub = 128;
   } else {
     *tw = CfgFp4D128M1::TW;
     *sub = CfgFp4D128M1::SUB;
@@ -400,7 +408,7 @@ pa_status validate(const pa_decode_args* a) {
     return PA_ERR_INVALID_ARG;
   if ((int64_t)a->max_blocks_per_seq * a->page_size > (int64_t)1 << 30) return PA_ERR_UNSUPPORTED;
   if ((int64_t)a->batch * a->num_kv_heads > ((int64_t)1 << 30)) return PA_ERR_UNSUPPORTED;
-  if (a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (a->head_dim != 64 && a->head_dim != 128 && a->head_dim != 256) return PA_ERR_UNSUPPORTED;
   switch (a->page_size) {
     case 16: case 32: case 64: case 128: case 256: break;
     default: return PA_ERR_UNSUPPORTED;

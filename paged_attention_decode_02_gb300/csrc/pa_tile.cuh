@@ -44,7 +44,7 @@ struct TileCfg {
   static constexpr int NKC = TW / 16;    // PV k-chunks per slice
   static constexpr int RPAD = MT * 16;
   static constexpr int ROW_BYTES = KIND == KIND_BF16 ? 2 * D : (KIND == KIND_FP8 ? D : D / 2);
-  static constexpr int SUB = KIND == KIND_FP4 ? 64 : 128;  // swizzle span = sub-tile row
+  static constexpr int SUB = ROW_BYTES >= 128 ? 128 : 64;  // swizzle span = sub-tile row
   static constexpr int NSUB = ROW_BYTES / SUB;
   static constexpr int NSUBW = NSUB / NDW;  // sub-tiles one warp loads and reads
   static constexpr int WBYTES = ROW_BYTES / NDW;
@@ -71,7 +71,10 @@ struct TileCfg {
   static constexpr int XW = MT * NT * 4 * 32;  // floats per warp per exchange buffer
   static constexpr int X_BYTES = NDW == 2 ? NTG * 2 * 2 * XW * 4 : 0;
   static constexpr int OFF_OB = OFF_X + X_BYTES;
-  static constexpr int OFF_ML = OFF_OB + RPAD * D * 4;
+  // merged rows (RPAD x D floats), reused by the fused partition merge for its weights
+  // (RPAD x up to 128 partitions)
+  static constexpr int OBW = D > 128 ? D : 128;
+  static constexpr int OFF_ML = OFF_OB + RPAD * OBW * 4;
   static constexpr int OFF_FIN = OFF_ML + NTG * RPAD * 8;  // 1 / sum per row
   static constexpr int TAB_BYTES = KIND == KIND_FP4 ? NBLK * TW * 6 : 0;  // K and V e8m0 factor tables
   static constexpr int OFF_TAB = OFF_FIN + RPAD * 8;
@@ -208,10 +211,13 @@ __device__ __forceinline__ void load_q_issue(const DecodeParams& p, int s, int h
       const int64_t row = (int64_t)s * p.qlen + i;
       const int64_t off = row * p.q_st + (int64_t)h * p.q_sh + lane * EPL;
       if (p.q_fp8) {
-        const uint32_t* src =
-            reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.q) + off);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + off;
+        if constexpr (EPL >= 4) {
 #pragma unroll
-        for (int j = 0; j < EPL / 4; ++j) q.w[k][j] = src[j];
+          for (int j = 0; j < EPL / 4; ++j) q.w[k][j] = reinterpret_cast<const uint32_t*>(src)[j];
+        } else {  // head_dim 64: two e4m3 bytes per lane
+          q.w[k][0] = *reinterpret_cast<const uint16_t*>(src);
+        }
         q.qsc[k] = p.q_scale_per_row ? p.q_scale[row * p.Hq + h] : p.q_scale[0];
       } else {
         const uint32_t* src =
@@ -247,6 +253,12 @@ __device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C
           x[4 * j + 1] = __high2float(l2);
           x[4 * j + 2] = __low2float(h2);
           x[4 * j + 3] = __high2float(h2);
+        }
+        if constexpr (EPL == 2) {
+          uint32_t lo = e4m3x2_to_f16x2(q.w[k][0] & 0xFFFF);
+          __half2 l2 = *reinterpret_cast<__half2*>(&lo);
+          x[0] = __low2float(l2);
+          x[1] = __high2float(l2);
         }
       } else {
 #pragma unroll
@@ -1187,7 +1199,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
         __threadfence();
         const int64_t base = p.part_base[unit];
         const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
-        float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= D)
+        float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= OBW)
         // one warp per row: lanes over partitions, shuffle-tree max and sum
         for (int r = cw; r < p.R; r += C::NCW) {
           float M = -INFINITY;

@@ -6,6 +6,9 @@ namespace pa {
 template <int SKT>
 static int launch_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                       int grid, void* stream) {
+  if (p.D == 64)
+    return p.R <= 16 ? launch_tile<CfgFp8D64M1<SKT>>(p, tk, tv, grid, stream)
+                     : launch_tile<CfgFp8D64M2<SKT>>(p, tk, tv, grid, stream);
   if (p.D == 128)
     return p.R <= 16 ? launch_tile<CfgFp8D128M1<SKT>>(p, tk, tv, grid, stream)
                      : launch_tile<CfgFp8D128M2<SKT>>(p, tk, tv, grid, stream);

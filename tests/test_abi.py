@@ -63,10 +63,16 @@ def test_valid_arguments_pass(lib):
     a = _valid_args()
     assert ops.pa_decode_validate(a) == ops.PA_OK
     assert ops.pa_decode_workspace_size(a) > 0
+    # head_dim 64 with 64-byte e4m3 rows
+    a.head_dim, a.kv_stride_token, a.q_stride_head, a.out_stride_head = 64, 64, 64, 64
+    assert ops.pa_decode_validate(a) == ops.PA_OK
 
 
 REFUSED = [
-    ("head_dim 64", dict(head_dim=64), ops.PA_ERR_UNSUPPORTED),
+    ("head_dim 96", dict(head_dim=96, q_stride_head=96, out_stride_head=96, kv_stride_token=96),
+     ops.PA_ERR_UNSUPPORTED),
+    ("mxfp4 head_dim 64", dict(kv_dtype=ops.PA_KV_MXFP4, kv_scale=ops.PA_SCALE_E8M0_32,
+                               head_dim=64, kv_stride_token=32), ops.PA_ERR_UNSUPPORTED),
     ("page 48", dict(page_size=48), ops.PA_ERR_UNSUPPORTED),
     ("Hq not a multiple of Hkv", dict(num_q_heads=15, num_kv_heads=2), ops.PA_ERR_INVALID_ARG),
     ("qlen 0", dict(qlen=0), ops.PA_ERR_INVALID_ARG),

@@ -200,6 +200,60 @@ def test_window_on_the_long_context_workload_sampled():
     assert np.isfinite(got).all()
 
 
+SHAPES = [
+    # head_dim 64 (64-byte e4m3 rows, 128-byte bf16 rows) and GQA 4 (4 query rows), the
+    # head sizes and GQA ratios of the first page's probe
+    synth.Case("d64_bf16_g4", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=5, qlen=1,
+               num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+               context_lens=[1, 17, 255, 257, 3000], seed=3001),
+    synth.Case("d64_bf16_g8_q4_causal", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=4,
+               qlen=4, num_kv_heads=1, num_q_heads=8, head_dim=64, page_size=64,
+               context_lens=[2, 70, 513, 2000], seed=3002, causal=True),
+    synth.Case("d64_fp8_tensor_g4", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=4,
+               qlen=1, num_kv_heads=4, num_q_heads=16, head_dim=64, page_size=128,
+               context_lens=[1, 129, 1000, 4097], fill=synth.FILL_INF, seed=3003, kv_std=20.0),
+    synth.Case("d64_fp8_token_g16_q2", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+               qlen=2, num_kv_heads=2, num_q_heads=32, head_dim=64, page_size=32,
+               context_lens=[3, 300, 1500, 2500], seed=3004, kv_std=20.0, window=700),
+    synth.Case("d64_fp8_token_e4m3q", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_E4M3, batch=3,
+               qlen=1, num_kv_heads=1, num_q_heads=16, head_dim=64, page_size=16,
+               context_lens=[40, 900, 5000], seed=3005, kv_std=20.0),
+    synth.Case("d64_bf16_e4m3q_g4_q2", synth.KV_BF16, synth.SCALE_NONE, synth.Q_E4M3, batch=3,
+               qlen=2, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+               context_lens=[5, 600, 2100], seed=3006),
+    synth.Case("d128_fp8_token_g4", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+               qlen=1, num_kv_heads=2, num_q_heads=8, head_dim=128, page_size=16,
+               context_lens=[1, 200, 1000, 3000], seed=3007, kv_std=20.0),
+    synth.Case("d256_bf16_g4", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3, qlen=1,
+               num_kv_heads=2, num_q_heads=8, head_dim=256, page_size=64,
+               context_lens=[7, 800, 2500], seed=3008),
+]
+
+
+@pytest.mark.parametrize("case", SHAPES, ids=lambda c: c.name)
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_head_sizes_and_gqa_ratios(case, mode):
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
+
+
+@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8])
+def test_head_dim_64_fused_merge_of_128_partitions(kv):
+    # one long unit cut into 128 partitions: the fused merge's [rows, partitions] weights
+    # are wider than a head_dim-64 output row
+    scale = synth.SCALE_NONE if kv == synth.KV_BF16 else synth.SCALE_TOKEN
+    case = synth.Case("d64_parts128", kv, scale, synth.Q_BF16, batch=1, qlen=2,
+                      num_kv_heads=1, num_q_heads=16, head_dim=64, page_size=128,
+                      context_lens=[60000], seed=3009, kv_std=20.0 if kv == synth.KV_FP8 else 1.0)
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=128, task_budget=152, merge_in_decode=True)
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
+    split = run_gpu(p, max_partitions=128, task_budget=152)
+    util.assert_parity(split, util.oracle_decode(p), case.kv, case.name + " split")
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
