@@ -29,6 +29,10 @@
  *   whose own place in the context is p = L - qlen + i, sees only the tokens t > p - W:
  *   the W tokens ending at itself, cut further by causal masking when that is set.
  *   Tokens before every position's window (t < L - qlen - W + 1) are never read.
+ *   With trans_v set, the value cache stores each page head-dim major: [NB, Hkv, D, S],
+ *   the S tokens of one head dim contiguous (the first page's probe covers fp8
+ *   per-tensor caches with "trans_v" and with plain V, without defining the layout; this
+ *   is the plain transposed reading, and the layout of vLLM's classic value cache).
  *
  * Storage formats are decoded from their definitions:
  *   bf16      : the high half of an IEEE binary32
@@ -52,7 +56,8 @@
  *                to the nearest e4m3 value (ties to even, finite at +-448), read back as
  *                e4m3(y) * s; a zero row stays zero.
  *   q_scale      scalar or [B, qlen, Hq] fp32 (e4m3 query only)
- *   key/value    [NB, Hkv, S, row_bytes] (row_bytes = 2D bf16, D e4m3, D/2 MXFP4)
+ *   key/value    [NB, Hkv, S, row_bytes] (row_bytes = 2D bf16, D e4m3, D/2 MXFP4);
+ *                value [NB, Hkv, D, S] elements with trans_v
  *   scales       per-tensor: fp32 [1]; per-token: fp32 [NB, Hkv, S];
  *                e8m0: uint8 [NB, Hkv, S, D/32]
  *   block_tables [B, max_blocks_per_seq] int32; context_lens [B] int32
@@ -85,6 +90,7 @@ typedef struct {
   const int32_t* context_lens;
   int32_t causal;
   int32_t window; /* sliding window W (0: none) */
+  int32_t trans_v; /* value cache [NB, Hkv, D, S] (bf16 / e4m3 only) */
 } orc_args;
 
 /* ---- format decoders ---------------------------------------------------- */
@@ -153,17 +159,22 @@ static int64_t row_bytes(const orc_args* a) {
 
 /* Dequantized element d of token slot `slot` in page `blk`, KV head `hkv`. */
 static double kv_elem(const orc_args* a, const void* cache, const void* scale, int64_t blk,
-                      int hkv, int slot, int d) {
+                      int hkv, int slot, int d, int transposed) {
   const int64_t rb = row_bytes(a);
   const int64_t token = (blk * a->num_kv_heads + hkv) * a->page_size + slot;
   const uint8_t* row = (const uint8_t*)cache + token * rb;
+  /* transposed page: element (d, slot) of the [D, S] page of (blk, hkv) */
+  const int64_t tel = ((blk * a->num_kv_heads + hkv) * a->head_dim + d) * a->page_size + slot;
   double v;
   if (a->kv_format == ORC_KV_BF16) {
     uint16_t bits;
-    memcpy(&bits, row + 2 * d, 2);
+    if (transposed)
+      memcpy(&bits, (const uint8_t*)cache + 2 * tel, 2);
+    else
+      memcpy(&bits, row + 2 * d, 2);
     v = orc_bf16(bits);
   } else if (a->kv_format == ORC_KV_E4M3) {
-    v = orc_e4m3(row[d]);
+    v = orc_e4m3(transposed ? ((const uint8_t*)cache)[tel] : row[d]);
   } else {
     uint8_t byte = row[d / 2];
     uint8_t nib = (d % 2 == 0) ? (byte & 15) : (byte >> 4);
@@ -239,7 +250,8 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
   for (int j = 0; j < n; ++j) {
     int t = t0 + j;
     int64_t blk = bt[t / S];
-    for (int d = 0; d < D; ++d) kv[d] = kv_elem(a, a->key_cache, a->key_scale, blk, hkv, t % S, d);
+    for (int d = 0; d < D; ++d)
+      kv[d] = kv_elem(a, a->key_cache, a->key_scale, blk, hkv, t % S, d, 0);
     for (int r = 0; r < R; ++r) {
       if (a->causal && t >= L - a->qlen + 1 + r / G) {  /* after query position r / G */
         x[(int64_t)r * n + j] = -INFINITY;
@@ -265,7 +277,7 @@ static void attend_range(const orc_args* a, int s, int hkv, int t0, int t1, doub
     int t = t0 + j;
     int64_t blk = bt[t / S];
     for (int d = 0; d < D; ++d)
-      kv[d] = kv_elem(a, a->value_cache, a->value_scale, blk, hkv, t % S, d);
+      kv[d] = kv_elem(a, a->value_cache, a->value_scale, blk, hkv, t % S, d, a->trans_v);
     for (int r = 0; r < R; ++r) {
       if (x[(int64_t)r * n + j] == -INFINITY) continue; /* not seen by this row */
       double w = exp(x[(int64_t)r * n + j] - m[r]);
@@ -282,6 +294,7 @@ static int check_args(const orc_args* a) {
   if (a->batch < 0 || a->qlen < 1 || a->num_kv_heads < 1 || a->num_q_heads < 1) return -1;
   if (a->causal != 0 && a->causal != 1) return -1;
   if (a->window < 0) return -1;
+  if (a->trans_v != 0 && (a->trans_v != 1 || a->kv_format == ORC_KV_MXFP4)) return -1;
   if (a->num_q_heads % a->num_kv_heads) return -1;
   if (a->head_dim < 1 || a->page_size < 1) return -1;
   if (a->kv_format == ORC_KV_MXFP4 && (a->head_dim % 32 || a->scale_kind != ORC_SCALE_E8M0))

@@ -52,6 +52,7 @@ class OrcArgs(ctypes.Structure):
         ("context_lens", ctypes.c_void_p),
         ("causal", ctypes.c_int32),
         ("window", ctypes.c_int32),
+        ("trans_v", ctypes.c_int32),
     ]
 
 
@@ -135,7 +136,8 @@ class Problem:
     def __init__(self, *, batch, qlen, num_q_heads, num_kv_heads, head_dim, page_size,
                  num_blocks, kv_format, scale_kind, q_format, softmax_scale, query,
                  key_cache, value_cache, block_tables, context_lens, key_scale=None,
-                 value_scale=None, q_scale=None, causal=False, window=0):
+                 value_scale=None, q_scale=None, causal=False, window=0,
+                 trans_v=False):
         self.keep = []
         a = OrcArgs()
         a.batch, a.qlen, a.num_q_heads, a.num_kv_heads = batch, qlen, num_q_heads, num_kv_heads
@@ -147,6 +149,7 @@ class Problem:
         a.softmax_scale = float(softmax_scale)
         a.causal = int(bool(causal))
         a.window = int(window)
+        a.trans_v = int(bool(trans_v))
         q = _np(query)
         kc, vc = _np(key_cache), _np(value_cache)
         ks = _np(key_scale)

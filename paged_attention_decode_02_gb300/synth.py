@@ -55,6 +55,8 @@ class Case:
     # sliding window W > 0: query position i (place p = L - qlen + i) sees tokens t > p - W;
     # rows before every position's window hold the fill, like rows no sequence owns
     window: int = 0
+    # value cache stored head-dim major per page, [NB, Hkv, D, S] (bf16 / fp8 only)
+    trans_v: bool = False
     pad_columns: int = 2
     extra_blocks: int = 0
     # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and
@@ -252,12 +254,16 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
     unowned = ~own4
     _fill(case, caches, key_scale, value_scale, unowned, g)
 
+    vcache = caches[1].view(torch.bfloat16) if case.kv == KV_BF16 else caches[1]
+    if case.trans_v:
+        assert case.kv != KV_MXFP4, "trans_v is a bf16 / fp8 layout"
+        vcache = vcache.transpose(-1, -2).contiguous()  # [NB, Hkv, D, S]
     out = {
         "case": case,
         "query": query,
         "q_scale": q_scale,
         "key_cache": caches[0].view(torch.bfloat16) if case.kv == KV_BF16 else caches[0],
-        "value_cache": caches[1].view(torch.bfloat16) if case.kv == KV_BF16 else caches[1],
+        "value_cache": vcache,
         "key_scale": key_scale,
         "value_scale": value_scale,
         "block_tables": bt,

@@ -100,6 +100,8 @@ def _dequant_dense(p: dict, which: str) -> torch.Tensor:
     """Dequantised cache [NB, Hkv, S, D] in float64, via library casts and tables."""
     case = p["case"]
     c = p["key_cache" if which == "k" else "value_cache"].cpu()
+    if which == "v" and case.trans_v:  # stored [NB, Hkv, D, S]: back to token rows
+        c = c.transpose(-1, -2)
     sc = p["key_scale" if which == "k" else "value_scale"]
     sc = None if sc is None else sc.cpu()
     if case.kv == synth.KV_BF16:
@@ -192,6 +194,13 @@ def _tiny_cases():
                    batch=4, qlen=3, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,
                    context_lens=[1, 5, 18, 60], fill=synth.FILL_INF, seed=20, kv_std=20.0,
                    causal=True, window=5),
+        synth.Case("t_fp8_trans_v", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=3,
+                   qlen=2, num_kv_heads=2, num_q_heads=4, head_dim=64, page_size=16,
+                   context_lens=[1, 30, 70], fill=synth.FILL_NAN, seed=25, kv_std=20.0,
+                   trans_v=True),
+        synth.Case("t_bf16_trans_v_window", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
+                   batch=2, qlen=1, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=32,
+                   context_lens=[40, 90], fill=synth.FILL_NAN, seed=26, trans_v=True, window=33),
         synth.Case("t_mxfp4_window", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_E4M3, batch=2,
                    qlen=1, num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
                    context_lens=[20, 45], fill=synth.FILL_RANDOM, seed=24, window=17),
@@ -359,6 +368,24 @@ def test_window_pins_catch_off_by_one():
     got = util.oracle_decode(p)
     for w in (case.window - 1, case.window + 1):
         assert util.rel_l2(got, brute_force(p, window=w)) > 1e-3, w
+
+
+@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8])
+def test_transposed_value_cache_gives_the_same_result(kv):
+    # the same values stored [NB, Hkv, D, S] instead of [NB, Hkv, S, D]: the same bits
+    scale = synth.SCALE_NONE if kv == synth.KV_BF16 else synth.SCALE_TENSOR
+    case = synth.Case("tv", kv, scale, synth.Q_BF16, batch=3, qlen=2, num_kv_heads=2,
+                      num_q_heads=8, head_dim=64, page_size=16, context_lens=[3, 40, 100],
+                      fill=synth.FILL_ZERO, seed=64, kv_std=20.0)
+    p = synth.make(case)
+    pt = synth.make(synth.replace(case, trans_v=True))
+    assert torch.equal(pt["value_cache"].transpose(-1, -2), p["value_cache"])
+    assert np.array_equal(util.oracle_decode(pt), util.oracle_decode(p))
+    # and the layout is not symmetric: the transposed bytes read as plain V differ
+    wrong = dict(pt)
+    wrong["case"] = synth.replace(case, trans_v=False)
+    wrong["value_cache"] = pt["value_cache"].reshape(p["value_cache"].shape)
+    assert util.rel_l2(util.oracle_decode(wrong), util.oracle_decode(p)) > 1e-2
 
 
 def test_e4m3_rounding_matches_torch():
