@@ -150,10 +150,17 @@ typedef struct pa_decode_args {
    * their block-table entries are never used as addresses.  Every format; the tcgen05
    * kernel does not take a window (the tile kernel runs).  Negative: PA_ERR_INVALID_ARG. */
   int32_t sliding_window;
+  /* 0 or 1.  With 1 the value cache stores each page head-dim major: value_cache is
+   * [NB, Hkv, D, S] e4m3 bytes, the S tokens of one head dim contiguous, with the key
+   * cache's block and head strides (the key cache keeps [NB, Hkv, S, D]).  The first page's
+   * probe covers fp8 per-tensor caches "with trans_v and plain V" without defining the
+   * layout; this is the plain transposed reading.  fp8 with a per-tensor scale only
+   * (PA_ERR_UNSUPPORTED otherwise); the tcgen05 kernel does not take it. */
+  int32_t trans_v;
 } pa_decode_args;
 
 /* ABI version of this header; a mismatched library refuses nothing but reports it here. */
-#define PA_DECODE_ABI_VERSION 3
+#define PA_DECODE_ABI_VERSION 4
 int32_t pa_decode_abi_version(void);
 
 /* Bytes of workspace the three calls need for these shapes (plan, partition scratch,

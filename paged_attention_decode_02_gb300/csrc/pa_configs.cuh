@@ -20,12 +20,13 @@ using CfgBf16D128M1 = TileCfg<KIND_BF16, SK_NONE, 128, 1, 8, 1, 16, 2, 1, 1>;
 using CfgBf16D128M2 = TileCfg<KIND_BF16, SK_NONE, 128, 2, 8, 1, 16, 3>;
 using CfgBf16D256M1 = TileCfg<KIND_BF16, SK_NONE, 256, 1, 4, 2, 16, 2>;
 using CfgBf16D256M2 = TileCfg<KIND_BF16, SK_NONE, 256, 2, 4, 2, 16, 2>;
-template <int SKT> using CfgFp8D64M1 = TileCfg<KIND_FP8, SKT, 64, 1, 8, 1, 32, 4, 1, 1>;
-template <int SKT> using CfgFp8D64M2 = TileCfg<KIND_FP8, SKT, 64, 2, 8, 1, 32, 4, 1, 1>;
-template <int SKT> using CfgFp8D128M1 = TileCfg<KIND_FP8, SKT, 128, 1, 8, 1, 32, 2, 1, 1>;
-template <int SKT> using CfgFp8D128M2 = TileCfg<KIND_FP8, SKT, 128, 2, 8, 1, 16, 4>;
-template <int SKT> using CfgFp8D256M1 = TileCfg<KIND_FP8, SKT, 256, 1, 4, 2, 32, 2>;
-template <int SKT> using CfgFp8D256M2 = TileCfg<KIND_FP8, SKT, 256, 2, 4, 2, 16, 3>;
+// (TRV = 1: transposed value cache, per-tensor scales)
+template <int SKT, int TRV = 0> using CfgFp8D64M1 = TileCfg<KIND_FP8, SKT, 64, 1, 8, 1, 32, 4, 1, 1, TRV>;
+template <int SKT, int TRV = 0> using CfgFp8D64M2 = TileCfg<KIND_FP8, SKT, 64, 2, 8, 1, 32, 4, 1, 1, TRV>;
+template <int SKT, int TRV = 0> using CfgFp8D128M1 = TileCfg<KIND_FP8, SKT, 128, 1, 8, 1, 32, 2, 1, 1, TRV>;
+template <int SKT, int TRV = 0> using CfgFp8D128M2 = TileCfg<KIND_FP8, SKT, 128, 2, 8, 1, 16, 4, 1, 0, TRV>;
+template <int SKT, int TRV = 0> using CfgFp8D256M1 = TileCfg<KIND_FP8, SKT, 256, 1, 4, 2, 32, 2, 1, 0, TRV>;
+template <int SKT, int TRV = 0> using CfgFp8D256M2 = TileCfg<KIND_FP8, SKT, 256, 2, 4, 2, 16, 3, 1, 0, TRV>;
 using CfgFp4D128M1 = TileCfg<KIND_FP4, SK_E8M0, 128, 1, 8, 1, 32, 3, 1, 1>;
 
 }  // namespace pa

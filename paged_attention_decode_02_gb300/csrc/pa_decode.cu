@@ -425,6 +425,9 @@ pa_status validate(const pa_decode_args* a) {
   if (a->merge_in_decode != 0 && a->merge_in_decode != 1) return PA_ERR_INVALID_ARG;
   if (a->causal != 0 && a->causal != 1) return PA_ERR_INVALID_ARG;
   if (a->sliding_window < 0) return PA_ERR_INVALID_ARG;
+  if (a->trans_v != 0 && a->trans_v != 1) return PA_ERR_INVALID_ARG;
+  if (a->trans_v && !(a->kv_dtype == PA_KV_FP8_E4M3 && a->kv_scale == PA_SCALE_PER_TENSOR))
+    return PA_ERR_UNSUPPORTED;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
@@ -480,15 +483,16 @@ pa_status split_params(const pa_decode_args* a, int* budget, int* maxp) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
-// and pages of at least 8 tokens, with the separate reduce, not causal and without a
-// sliding window.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
+// and pages of at least 8 tokens, with the separate reduce, not causal, without a sliding
+// window and with token-major V.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
 // each call); otherwise every shape runs the mma.sync kernel, the faster of the two on
 // the long-context workloads.
 bool tc_kernel_applies(const pa_decode_args* a, int rows) {
   const char* e = getenv("PA_DECODE_KERNEL");
   const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
   return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
-         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && a->q_dtype != PA_Q_BF16_TO_E4M3;
+         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && !a->trans_v &&
+         a->q_dtype != PA_Q_BF16_TO_E4M3;
 }
 
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
@@ -569,6 +573,23 @@ pa_status cache_map(const pa_decode_args* a, const void* base, int sub, int box_
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   sub == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
+// Tensor map of a transposed e4m3 value cache [NB, Hkv, D, S]: boxes of 16 tokens (16
+// bytes) by `dims` head dims, unswizzled (rows of 16 bytes are read conflict-free).
+pa_status cache_map_vt(const pa_decode_args* a, int dims, CUtensorMap* m) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t gdim[4] = {(cuuint64_t)a->page_size, (cuuint64_t)a->head_dim,
+                        (cuuint64_t)a->num_kv_heads, (cuuint64_t)a->num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)a->page_size, (cuuint64_t)a->kv_stride_head,
+                           (cuuint64_t)a->kv_stride_block};
+  cuuint32_t box[4] = {16, (cuuint32_t)dims, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(a->value_cache), gdim,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
@@ -655,10 +676,15 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   } else {
     pa::tile_geometry(kind, a->head_dim, R, &tc, &sub);
   }
-  const int box = a->page_size < tc ? a->page_size : tc;
+  // transposed V is loaded in 16-token pieces, and K in boxes of the same height
+  const int box = a->trans_v ? 16 : (a->page_size < tc ? a->page_size : tc);
   CUtensorMap tk, tv;
   if ((st = cache_map(a, a->key_cache, sub, box, &tk)) != PA_OK) return st;
-  if ((st = cache_map(a, a->value_cache, sub, box, &tv)) != PA_OK) return st;
+  if (a->trans_v)
+    st = cache_map_vt(a, a->head_dim > 128 ? a->head_dim / 2 : a->head_dim, &tv);
+  else
+    st = cache_map(a, a->value_cache, sub, box, &tv);
+  if (st != PA_OK) return st;
 
   uint8_t* w = static_cast<uint8_t*>(ws);
   pa::DecodeParams p;
@@ -666,6 +692,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.qlen = a->qlen;
   p.causal = a->causal && a->qlen > 1;
   p.window = a->sliding_window;
+  p.trans_v = a->trans_v;
   p.Hq = a->num_q_heads;
   p.Hkv = a->num_kv_heads;
   p.G = G;

@@ -48,6 +48,7 @@ struct DecodeParams {
   int q_fp8, q_scale_per_row, scale_kind;
   int causal;  // qlen > 1: query position i sees tokens < L - qlen + 1 + i
   int window;  // > 0: query position i sees tokens > L - qlen + i - window
+  int trans_v;  // value cache [NB, Hkv, D, S] (fp8 per-tensor)
   int q_quant;  // bf16 query quantised per head row to e4m3 (scale amax / 448)
   int drop_first_slice;  // test hook: warp 0 of each CTA never loads its first slice
   const void* q;

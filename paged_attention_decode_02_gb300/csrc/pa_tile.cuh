@@ -28,13 +28,18 @@ enum { ST_OK = 0, ST_TIMEOUT = 1, ST_CLAMPED = 2 };
 
 // TileCfg<format, scale kind, head_dim, m-tiles (query rows / 16), token groups, warps per
 // token group (head-dim split), tokens per warp slice, slots per warp ring, CTAs per SM,
-// a merge buffer of its own (every task merges in one pass, not only a chunk's last)>.
+// a merge buffer of its own (every task merges in one pass, not only a chunk's last),
+// transposed value cache [NB, Hkv, D, S] (fp8)>.
 template <int KIND_, int SKT_, int D_, int MT_, int NTG_, int NDW_, int TW_, int NSTAGE_,
-          int MINB_ = 1, int MRG_ = 0>
+          int MINB_ = 1, int MRG_ = 0, int TRV_ = 0>
 struct TileCfg {
   static constexpr int KIND = KIND_, SKT = SKT_, D = D_, MT = MT_, NTG = NTG_, NDW = NDW_;
   static constexpr int TW = TW_, NSTAGE = NSTAGE_, MINB = MINB_;
   static constexpr bool MRG = MRG_ != 0;
+  // Transposed V: each slice's V arrives as 16-token pieces [DW head dims][16 tokens] (one
+  // e4m3 byte per token), and the score columns take tokens in the order that makes a
+  // lane's 4 consecutive tokens of one head dim its PV B-fragment (see kv_token).
+  static constexpr bool TRV = TRV_ != 0;
   static constexpr bool TOK_SCALE = SKT == SK_TOKEN;                 // fp8 per-token scales
   static constexpr bool SCALES = SKT == SK_TOKEN || SKT == SK_E8M0;  // staged per slice
   static constexpr int NCW = NTG * NDW;  // warps (all compute; each loads its own slices)
@@ -93,7 +98,19 @@ struct TileCfg {
                 "MXFP4 path: D 128, one warp per row, one lane per slice token");
   static_assert(SMEM * MINB <= 227 * 1024, "shared memory budget");
   static_assert(NTG + 1 < 16, "named barrier ids");
+  static_assert(!TRV || KIND == KIND_FP8, "transposed V: e4m3 caches");
+  static constexpr int PIECE_V = DW * 16;  // transposed V: bytes of one 16-token piece
+  static constexpr int KOFFN = TRV ? 2 * NGRP : NGRP;  // K ldmatrix row offsets per lane
 };
+
+// Token (within its 16-token k-chunk) of score column c of a 16-token chunk.  Plain order
+// for the token-major caches; with transposed V the columns 2u, 2u + 1, 8 + 2u, 9 + 2u take
+// tokens 4u .. 4u + 3, the four consecutive tokens a lane reads from one head-dim row.
+template <class C>
+__device__ __forceinline__ int kv_token(int c) {
+  if constexpr (C::TRV) return 4 * ((c & 7) >> 1) + (c & 1) + 2 * (c >> 3);
+  return c;
+}
 
 constexpr int BAR_CONSUMERS = 15;  // named barrier id for all warps of the CTA
 constexpr uint32_t kNoAbort = 0xFFFFFFFFu;  // a warp's waits have not stopped
@@ -137,7 +154,7 @@ __device__ __forceinline__ void load_qa(const uint16_t* qs, int mt, int kap, int
 // Head dim of element j (0..3) of PV n-tile n in this warp's accumulator.
 template <class C>
 __device__ __forceinline__ int o_dim(int n, int j, int dw, int t) {
-  if constexpr (C::KIND == KIND_BF16) {
+  if constexpr (C::KIND == KIND_BF16 || C::TRV) {
     return dw * C::DW + 8 * n + 2 * t + (j & 1);
   } else if constexpr (C::KIND == KIND_FP8) {
     return dw * C::DW + 16 * (n >> 1) + 4 * t + (n & 1) + 2 * (j & 1);
@@ -154,7 +171,7 @@ __device__ __forceinline__ int frag_pos(int row, int d) {
   const int mt = row >> 4, g = row & 7, jh = (row >> 3) & 1;
   const int dw = d / C::DW, dd = d - dw * C::DW;
   int n, t, jl;
-  if constexpr (C::KIND == KIND_BF16) {  // dd = 8n + 2t + jl
+  if constexpr (C::KIND == KIND_BF16 || C::TRV) {  // dd = 8n + 2t + jl
     n = dd >> 3;
     t = (dd >> 1) & 3;
     jl = dd & 1;
@@ -418,8 +435,10 @@ __device__ __forceinline__ void issue_slice(const DecodeParams& p, const CUtenso
       const int sub = dw * C::NSUBW + u;
       const int dst = u * (C::TW * C::SUB) + ((lane << box_shift) * C::SUB);
       tma_load_4d(kv + dst, tmk, bar, sub * C::SUB, slot, it.hkv, blk);
-      tma_load_4d(kv + C::SLOT_V + dst, tmv, bar, sub * C::SUB, slot, it.hkv, blk);
+      if constexpr (!C::TRV) tma_load_4d(kv + C::SLOT_V + dst, tmv, bar, sub * C::SUB, slot, it.hkv, blk);
     }
+    // transposed V: this box is the 16-token piece `lane`, head dims [dw * DW, dw * DW + DW)
+    if constexpr (C::TRV) tma_load_4d(kv + C::SLOT_V + lane * C::PIECE_V, tmv, bar, slot, dw * C::DW, it.hkv, blk);
     if constexpr (C::SCALES) {
       const int64_t off = (int64_t)blk * p.sc_sb + (int64_t)it.hkv * p.sc_sh + (int64_t)slot * 4;
       bulk_load(sc + (lane << box_shift) * 4, p.k_scale + off, box * 4, bar);
@@ -480,7 +499,7 @@ template <class C, bool MASKED>
 __device__ __forceinline__ void stage_compute(
     WarpAcc<C>& A, const uint8_t* kv, const uint8_t* sc, uint8_t* smem, int vw, int lane, int dw,
     int tg, const uint32_t (&qa)[C::Q_IN_REGS ? C::MT : 1][C::Q_IN_REGS ? C::NKCH : 1][4],
-    const uint16_t* qs, const float (&crow)[C::MT][2], const uint32_t (&koff)[C::NGRP],
+    const uint16_t* qs, const float (&crow)[C::MT][2], const uint32_t (&koff)[C::KOFFN],
     const uint32_t (&voff)[C::NCP], int cw, int& xbuf, int cq, int G, int wl, int qm1) {
   constexpr bool tok_scale = C::TOK_SCALE;
   const int g = lane >> 2, t = lane & 3;
@@ -545,7 +564,12 @@ __device__ __forceinline__ void stage_compute(
   for (int gi = 0; gi < C::NGRP; ++gi) {
     uint32_t kr[C::NT][4];
 #pragma unroll
-    for (int nt = 0; nt < C::NT; ++nt) ldsm_x4(kbase + koff[gi] + nt * 8 * C::SUB, kr[nt]);
+    for (int nt = 0; nt < C::NT; ++nt) {
+      if constexpr (C::TRV)  // even / odd n-tiles of a 16-token chunk read their own rows
+        ldsm_x4(kbase + koff[(nt & 1) * C::NGRP + gi] + (nt >> 1) * 16 * C::SUB, kr[nt]);
+      else
+        ldsm_x4(kbase + koff[gi] + nt * 8 * C::SUB, kr[nt]);
+    }
     if constexpr (C::KIND == KIND_BF16) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -686,7 +710,7 @@ __device__ __forceinline__ void stage_compute(
     }
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
-    const int tk0 = 8 * nt + 2 * t;
+    const int tk0 = 16 * (nt >> 1) + kv_token<C>(8 * (nt & 1) + 2 * t);  // its pair: tk0, tk0 + 1
     float2 ks = make_float2(1.f, 1.f);
     if constexpr (tok_scale) ks = *reinterpret_cast<const float2*>(ksc + tk0);
 #pragma unroll
@@ -768,13 +792,14 @@ __device__ __forceinline__ void stage_compute(
 #pragma unroll
   for (int kc = 0; kc < C::NKC; ++kc) {
     if (MASKED && 16 * kc >= vw) break;
-    const int tb = 16 * kc + 2 * t;  // tokens tb, tb+1 (low pair) and tb+8, tb+9 (high pair)
+    // tokens of this lane's low (k = 2t, 2t + 1) and high (k = 2t + 8, 2t + 9) pairs
+    const int tb = 16 * kc + kv_token<C>(2 * t), th = 16 * kc + kv_token<C>(8 + 2 * t);
     uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
     // a token's V row passes if it is owned and inside some window
     auto in = [&](int x) { return x < vw && x >= vlo; };
     if (MASKED) {
       mlo = (in(tb) ? 0x0000FFFFu : 0u) | (in(tb + 1) ? 0xFFFF0000u : 0u);
-      mhi = (in(tb + 8) ? 0x0000FFFFu : 0u) | (in(tb + 9) ? 0xFFFF0000u : 0u);
+      mhi = (in(th) ? 0x0000FFFFu : 0u) | (in(th + 1) ? 0xFFFF0000u : 0u);
     }
     uint32_t pa[C::MT][4];
 #pragma unroll
@@ -788,11 +813,11 @@ __device__ __forceinline__ void stage_compute(
         pa[mt][3] = pack_bf16x2(ph[2], ph[3]);
       } else if constexpr (tok_scale) {
         const float2 a = *reinterpret_cast<const float2*>(vsc + tb);
-        const float2 c = *reinterpret_cast<const float2*>(vsc + tb + 8);
+        const float2 c = *reinterpret_cast<const float2*>(vsc + th);
         const float vf0 = (MASKED && !in(tb)) ? 0.f : a.x * vinv;
         const float vf1 = (MASKED && !in(tb + 1)) ? 0.f : a.y * vinv;
-        const float vf2 = (MASKED && !in(tb + 8)) ? 0.f : c.x * vinv;
-        const float vf3 = (MASKED && !in(tb + 9)) ? 0.f : c.y * vinv;
+        const float vf2 = (MASKED && !in(th)) ? 0.f : c.x * vinv;
+        const float vf3 = (MASKED && !in(th + 1)) ? 0.f : c.y * vinv;
         pa[mt][0] = pack_f16x2(pl[0] * vf0, pl[1] * vf1);
         pa[mt][1] = pack_f16x2(pl[2] * vf0, pl[3] * vf1);
         pa[mt][2] = pack_f16x2(ph[0] * vf2, ph[1] * vf3);
@@ -803,6 +828,27 @@ __device__ __forceinline__ void stage_compute(
         pa[mt][2] = pack_f16x2(ph[0], ph[1]);
         pa[mt][3] = pack_f16x2(ph[2], ph[3]);
       }
+    }
+    if constexpr (C::TRV) {
+      // piece kc, head-dim rows of 16 bytes: lane 8q + j points at row 32 cp + 8q + j and
+      // gets tokens 4t .. 4t + 3 of head dim 8 (4 cp + q) + g, the B-fragment of n-tile 4 cp + q
+#pragma unroll
+      for (int cp = 0; cp < C::NTD / 4; ++cp) {
+        uint32_t v[4];
+        ldsm_x4(vbase + kc * C::PIECE_V + (32 * cp + lane) * 16, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2(v[q], b0, b1);
+          if (MASKED) {
+            b0 &= mlo;
+            b1 &= mhi;
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) mma_f16(A.o[mt][4 * cp + q], pa[mt], b0, b1);
+        }
+      }
+      continue;
     }
 #pragma unroll
     for (int cp = 0; cp < C::NCP; ++cp) {
@@ -886,7 +932,8 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   const float v_scale_tensor = (C::KIND == KIND_FP8 && C::SKT == SK_TENSOR)
                                    ? reinterpret_cast<const float*>(p.v_scale)[0] : 1.f;
   const int page_shift = __ffs(p.S) - 1;  // page sizes are powers of two
-  const int box_shift = p.S < C::TW ? page_shift : __ffs(C::TW) - 1;
+  // boxes: a page piece of at most one slice; 16 tokens with transposed V (pages >= 16)
+  const int box_shift = C::TRV ? 4 : (p.S < C::TW ? page_shift : __ffs(C::TW) - 1);
   const int page_mask = p.S - 1;
   if (lane == 0) {
     tma_prefetch_desc(tmk);
@@ -894,14 +941,18 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   }
   // Per-lane byte offsets of the ldmatrix rows inside a slot (the swizzle phase of a row
   // depends only on its index modulo 8, i.e. on the lane).
-  uint32_t koff[C::NGRP], voff[C::NCP];
+  uint32_t koff[C::KOFFN], voff[C::NCP];
   {
     const int j = lane & 7, q = lane >> 3;
 #pragma unroll
-    for (int gi = 0; gi < C::NGRP; ++gi) {
-      const int off = gi * 64 + q * 16;
-      const int u = off / C::SUB, cin = (off % C::SUB) >> 4;
-      koff[gi] = u * (C::TW * C::SUB) + j * C::SUB + ((cin ^ swz<C>(j)) << 4);
+    for (int par = 0; par < C::KOFFN / C::NGRP; ++par) {
+      const int row = kv_token<C>(8 * par + j);  // token row of score column 8 par + j
+#pragma unroll
+      for (int gi = 0; gi < C::NGRP; ++gi) {
+        const int off = gi * 64 + q * 16;
+        const int u = off / C::SUB, cin = (off % C::SUB) >> 4;
+        koff[par * C::NGRP + gi] = u * (C::TW * C::SUB) + row * C::SUB + ((cin ^ swz<C>(row)) << 4);
+      }
     }
 #pragma unroll
     for (int cp = 0; cp < C::NCP; ++cp) {

@@ -51,7 +51,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("bt_stride", ctypes.c_int64), ("context_lens", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
         ("out_stride_head", ctypes.c_int64), ("causal", ctypes.c_int32),
-        ("sliding_window", ctypes.c_int32),
+        ("sliding_window", ctypes.c_int32), ("trans_v", ctypes.c_int32),
     ]
 
 
@@ -121,7 +121,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               q_scale: Optional[torch.Tensor] = None, softmax_scale: Optional[float] = None,
               max_partitions: int = 0, task_budget: int = 0,
               merge_in_decode: bool = False, causal: bool = False,
-              q_quant: bool = False, sliding_window: int = 0) -> PaDecodeArgs:
+              q_quant: bool = False, sliding_window: int = 0,
+              trans_v: bool = False) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -131,7 +132,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     (per token), or [NB, Hkv, S, D/2] uint8 MXFP4 with uint8 e8m0 scales
     [NB, Hkv, S, D/32].  block_tables int32 [B, W]; context_lens int32 [B].
     causal: query position i sees tokens < L - qlen + 1 + i.  sliding_window W > 0: query
-    position i sees only tokens > L - qlen + i - W.
+    position i sees only tokens > L - qlen + i - W.  trans_v: value_cache is [NB, Hkv, D, S]
+    (e4m3 bytes, per-tensor scale), with the key cache's block and head strides.
     """
     D = query.shape[-1]
     Hq = query.shape[-2]
@@ -171,11 +173,17 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     a.merge_in_decode = int(bool(merge_in_decode))
     a.causal = int(bool(causal))
     a.sliding_window = int(sliding_window)
+    a.trans_v = int(bool(trans_v))
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
     a.key_cache, a.value_cache = _ptr(key_cache), _ptr(value_cache)
-    if value_cache.stride() != key_cache.stride():
+    if trans_v:
+        if value_cache.stride()[:2] != key_cache.stride()[:2] or value_cache.stride(-1) != 1 \
+                or value_cache.stride(-2) != S:
+            raise ValueError("a transposed value cache is [NB, Hkv, D, S], dense pages, with "
+                             "the key cache's block and head strides")
+    elif value_cache.stride() != key_cache.stride():
         raise ValueError("key and value caches must share strides")
     a.kv_stride_block = key_cache.stride(0) * es
     a.kv_stride_head = key_cache.stride(1) * es
@@ -279,7 +287,8 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      softmax_scale=case.scale_qk(), max_partitions=max_partitions,
                      task_budget=task_budget, merge_in_decode=merge_in_decode,
                      causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False),
-                     sliding_window=getattr(case, "window", 0))
+                     sliding_window=getattr(case, "window", 0),
+                     trans_v=getattr(case, "trans_v", False))
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -29,16 +29,17 @@ def test_header_declarations_are_exported(lib):
     assert set(ops.EXPORTED) == set(names), names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.pa_decode_abi_version() == 3
+    assert lib.pa_decode_abi_version() == 4
 
 
 def test_args_struct_layout_matches_header():
     # 16 int32/float fields, then 19 pointers and int64s, then the causal flag and the
-    # sliding window
-    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 20 * 8
+    # sliding window, then trans_v (padded)
+    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 21 * 8
     assert ops.PaDecodeArgs.query.offset == 64
     assert ops.PaDecodeArgs.causal.offset == 64 + 19 * 8
     assert ops.PaDecodeArgs.sliding_window.offset == 64 + 19 * 8 + 4
+    assert ops.PaDecodeArgs.trans_v.offset == 64 + 20 * 8
 
 
 def _valid_args():
@@ -66,6 +67,9 @@ def test_valid_arguments_pass(lib):
     # head_dim 64 with 64-byte e4m3 rows
     a.head_dim, a.kv_stride_token, a.q_stride_head, a.out_stride_head = 64, 64, 64, 64
     assert ops.pa_decode_validate(a) == ops.PA_OK
+    # a transposed value cache with a per-tensor scale
+    a.kv_scale, a.trans_v = ops.PA_SCALE_PER_TENSOR, 1
+    assert ops.pa_decode_validate(a) == ops.PA_OK
 
 
 REFUSED = [
@@ -85,6 +89,11 @@ REFUSED = [
     ("unknown kv dtype", dict(kv_dtype=7), ops.PA_ERR_INVALID_ARG),
     ("merge flag not 0/1", dict(merge_in_decode=2), ops.PA_ERR_INVALID_ARG),
     ("negative sliding window", dict(sliding_window=-1), ops.PA_ERR_INVALID_ARG),
+    ("trans_v not 0/1", dict(trans_v=2), ops.PA_ERR_INVALID_ARG),
+    ("trans_v with per-token scales", dict(trans_v=1), ops.PA_ERR_UNSUPPORTED),
+    ("trans_v with bf16", dict(trans_v=1, kv_dtype=ops.PA_KV_BF16, kv_scale=ops.PA_SCALE_NONE,
+                               kv_stride_token=256, kv_stride_head=256 * 128,
+                               kv_stride_block=256 * 128), ops.PA_ERR_UNSUPPORTED),
     ("null query", dict(query=None), ops.PA_ERR_INVALID_ARG),
     ("null scales", dict(key_scale=None), ops.PA_ERR_INVALID_ARG),
     ("e4m3 query without scale", dict(q_dtype=ops.PA_Q_FP8_E4M3), ops.PA_ERR_INVALID_ARG),

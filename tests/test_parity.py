@@ -254,6 +254,50 @@ def test_head_dim_64_fused_merge_of_128_partitions(kv):
     util.assert_parity(split, util.oracle_decode(p), case.kv, case.name + " split")
 
 
+TRANS_V = [
+    # fp8 per-tensor with the value cache stored [NB, Hkv, D, S] (the first page's
+    # "trans_v"): K rows read in the order that matches the transposed V fragments
+    synth.Case("tv_d128_g8", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=6, qlen=1,
+               num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[1, 17, 255, 257, 1000, 5000], fill=synth.FILL_INF, seed=3101,
+               kv_std=20.0, trans_v=True),
+    synth.replace(synth.config2("b", batch=6, seed=3102), trans_v=True),
+    synth.Case("tv_d64_g4_q2_window", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=4,
+               qlen=2, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=128,
+               context_lens=[2, 130, 900, 3000], fill=synth.FILL_INF, seed=3103, kv_std=20.0,
+               causal=True, window=300, trans_v=True),
+    synth.Case("tv_d128_g16_q2", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=4,
+               qlen=2, num_kv_heads=1, num_q_heads=16, head_dim=128, page_size=32,
+               context_lens=[5, 33, 700, 2600], fill=synth.FILL_INF, seed=3104, kv_std=20.0,
+               trans_v=True),
+    synth.Case("tv_d256_g8_q2", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_E4M3, batch=3,
+               qlen=2, num_kv_heads=2, num_q_heads=16, head_dim=256, page_size=16,
+               context_lens=[9, 400, 1800], fill=synth.FILL_INF, seed=3105, kv_std=20.0,
+               trans_v=True),
+    synth.Case("tv_d64_g16_q2", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=3,
+               qlen=2, num_kv_heads=1, num_q_heads=16, head_dim=64, page_size=64,
+               context_lens=[64, 65, 2000], fill=synth.FILL_INF, seed=3106, kv_std=20.0,
+               trans_v=True),
+]
+
+
+@pytest.mark.parametrize("case", TRANS_V, ids=lambda c: c.name)
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_transposed_value_cache_matches_oracle(case, mode):
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name + " trans_v")
+
+
+def test_transposed_value_cache_agrees_with_plain():
+    case = TRANS_V[0]
+    p = synth.make(case)
+    plain = synth.make(synth.replace(case, trans_v=False))
+    a, b = run_gpu(p, task_budget=24), run_gpu(plain, task_budget=24)
+    assert util.rel_l2(a, b) < 2e-3
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
