@@ -330,34 +330,40 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   }
 }
 
-// Tokens per warp slice (the TMA box is min(S, this) rows high) and swizzle span of the
-// tile kernel that serves a format / head_dim / query-row count.
-void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub) {
+// Tokens per warp slice (the TMA box is min(S, this) rows high), swizzle span and head dims
+// per warp of the tile kernel that serves a format / head_dim / query-row count.
+template <class C>
+static void geometry_of(int* tw, int* sub, int* dw) {
+  *tw = C::TW;
+  *sub = C::SUB;
+  *dw = C::DW;
+}
+
+void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub, int* dw) {
+  const int m = rows <= 16 ? 1 : (rows <= 32 ? 2 : 4);
   if (kind == KIND_BF16) {
-    if (head_dim == 64) {
-      *tw = rows <= 16 ? CfgBf16D64M1::TW : CfgBf16D64M2::TW;
-      *sub = CfgBf16D64M1::SUB;
-    } else if (head_dim == 128) {
-      *tw = rows <= 16 ? CfgBf16D128M1::TW : CfgBf16D128M2::TW;
-      *sub = CfgBf16D128M1::SUB;
-    } else {
-      *tw = rows <= 16 ? CfgBf16D256M1::TW : CfgBf16D256M2::TW;
-      *sub = CfgBf16D256M1::SUB;
-    }
+    if (head_dim == 64)
+      m == 1 ? geometry_of<CfgBf16D64M1>(tw, sub, dw)
+             : (m == 2 ? geometry_of<CfgBf16D64M2>(tw, sub, dw) : geometry_of<CfgBf16D64M4>(tw, sub, dw));
+    else if (head_dim == 128)
+      m == 1 ? geometry_of<CfgBf16D128M1>(tw, sub, dw)
+             : (m == 2 ? geometry_of<CfgBf16D128M2>(tw, sub, dw) : geometry_of<CfgBf16D128M4>(tw, sub, dw));
+    else
+      m == 1 ? geometry_of<CfgBf16D256M1>(tw, sub, dw) : geometry_of<CfgBf16D256M2>(tw, sub, dw);
   } else if (kind == KIND_FP8) {
-    if (head_dim == 64) {
-      *tw = rows <= 16 ? CfgFp8D64M1<SK_TOKEN>::TW : CfgFp8D64M2<SK_TOKEN>::TW;
-      *sub = CfgFp8D64M1<SK_TOKEN>::SUB;
-    } else if (head_dim == 128) {
-      *tw = rows <= 16 ? CfgFp8D128M1<SK_TOKEN>::TW : CfgFp8D128M2<SK_TOKEN>::TW;
-      *sub = CfgFp8D128M1<SK_TOKEN>::SUB;
-    } else {
-      *tw = rows <= 16 ? CfgFp8D256M1<SK_TOKEN>::TW : CfgFp8D256M2<SK_TOKEN>::TW;
-      *sub = CfgFp8D256M1<SK_TOKEN>::SUB;
-    }
+    if (head_dim == 64)
+      m == 1 ? geometry_of<CfgFp8D64M1<SK_TOKEN>>(tw, sub, dw)
+             : (m == 2 ? geometry_of<CfgFp8D64M2<SK_TOKEN>>(tw, sub, dw)
+                       : geometry_of<CfgFp8D64M4<SK_TOKEN>>(tw, sub, dw));
+    else if (head_dim == 128)
+      m == 1 ? geometry_of<CfgFp8D128M1<SK_TOKEN>>(tw, sub, dw)
+             : (m == 2 ? geometry_of<CfgFp8D128M2<SK_TOKEN>>(tw, sub, dw)
+                       : geometry_of<CfgFp8D128M4<SK_TOKEN>>(tw, sub, dw));
+    else
+      m == 1 ? geometry_of<CfgFp8D256M1<SK_TOKEN>>(tw, sub, dw)
+             : geometry_of<CfgFp8D256M2<SK_TOKEN>>(tw, sub, dw);
   } else {
-    *tw = CfgFp4D128M1::TW;
-    *sub = CfgFp4D128M1::SUB;
+    geometry_of<CfgFp4D128M1>(tw, sub, dw);
   }
 }
 
@@ -370,7 +376,7 @@ namespace {
 
 using pa::WsLayout;
 
-constexpr int kMaxRows = 32;         // G * qlen served by the tile kernels
+constexpr int kMaxRows = 64;         // G * qlen served by the tile kernels (32 at head_dim 256)
 constexpr int kDefaultMaxParts = 128;
 constexpr int kMaxParts = 128;  // the in-decode merge keeps [rows, partitions] weights in smem
 
@@ -430,7 +436,7 @@ pa_status validate(const pa_decode_args* a) {
     return PA_ERR_UNSUPPORTED;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
-  if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
+  if (R > kMaxRows || (R > 32 && a->head_dim > 128)) return PA_ERR_UNSUPPORTED;
   if (a->kv_dtype == PA_KV_MXFP4 && (a->head_dim != 128 || a->qlen != 1 || G > 16)) return PA_ERR_UNSUPPORTED;
   if (a->batch == 0) return PA_OK;
   if (!a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->context_lens || !a->out)
@@ -669,19 +675,19 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   const int R = G * a->qlen;
   const int kind = a->kv_dtype == PA_KV_BF16 ? pa::KIND_BF16 : (a->kv_dtype == PA_KV_FP8_E4M3 ? pa::KIND_FP8 : pa::KIND_FP4);
   const bool use_tc = tc_kernel_applies(a, R);
-  int tc = 0, sub = 0;
+  int tc = 0, sub = 0, dims = a->head_dim;
   if (use_tc) {
     tc = 128;
     sub = kind == pa::KIND_FP4 ? 64 : 128;
   } else {
-    pa::tile_geometry(kind, a->head_dim, R, &tc, &sub);
+    pa::tile_geometry(kind, a->head_dim, R, &tc, &sub, &dims);
   }
   // transposed V is loaded in 16-token pieces, and K in boxes of the same height
   const int box = a->trans_v ? 16 : (a->page_size < tc ? a->page_size : tc);
   CUtensorMap tk, tv;
   if ((st = cache_map(a, a->key_cache, sub, box, &tk)) != PA_OK) return st;
   if (a->trans_v)
-    st = cache_map_vt(a, a->head_dim > 128 ? a->head_dim / 2 : a->head_dim, &tv);
+    st = cache_map_vt(a, dims, &tv);
   else
     st = cache_map(a, a->value_cache, sub, box, &tv);
   if (st != PA_OK) return st;

@@ -117,8 +117,10 @@ int launch_tc_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMa
 int launch_tc_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                     int grid, void* stream);
 
-// Tokens per warp slice and swizzle span (bytes) of the tile kernel chosen for a
-// format / head_dim / query-row count; the TMA box is min(S, slice tokens) rows high.
-void tile_geometry(int kind, int head_dim, int rows, int* slice_tokens, int* swizzle_bytes);
+// Tokens per warp slice, swizzle span (bytes) and head dims per warp of the tile kernel
+// chosen for a format / head_dim / query-row count; the TMA box is min(S, slice tokens)
+// rows high (16 with a transposed value cache, whose boxes are `dims_per_warp` high).
+void tile_geometry(int kind, int head_dim, int rows, int* slice_tokens, int* swizzle_bytes,
+                   int* dims_per_warp);
 
 }  // namespace pa

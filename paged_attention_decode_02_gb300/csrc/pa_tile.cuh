@@ -49,7 +49,8 @@ struct TileCfg {
   static constexpr int NKC = TW / 16;    // PV k-chunks per slice
   static constexpr int RPAD = MT * 16;
   static constexpr int ROW_BYTES = KIND == KIND_BF16 ? 2 * D : (KIND == KIND_FP8 ? D : D / 2);
-  static constexpr int SUB = ROW_BYTES >= 128 ? 128 : 64;  // swizzle span = sub-tile row
+  // swizzle span = sub-tile row: 128 bytes, or 64 where a warp's share of a row is 64 bytes
+  static constexpr int SUB = ROW_BYTES / NDW_ >= 128 ? 128 : 64;
   static constexpr int NSUB = ROW_BYTES / SUB;
   static constexpr int NSUBW = NSUB / NDW;  // sub-tiles one warp loads and reads
   static constexpr int WBYTES = ROW_BYTES / NDW;

@@ -7,11 +7,13 @@ template <int SKT, int TRV>
 static int launch_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                       int grid, void* stream) {
   if (p.D == 64)
-    return p.R <= 16 ? launch_tile<CfgFp8D64M1<SKT, TRV>>(p, tk, tv, grid, stream)
-                     : launch_tile<CfgFp8D64M2<SKT, TRV>>(p, tk, tv, grid, stream);
+    return p.R <= 16   ? launch_tile<CfgFp8D64M1<SKT, TRV>>(p, tk, tv, grid, stream)
+           : p.R <= 32 ? launch_tile<CfgFp8D64M2<SKT, TRV>>(p, tk, tv, grid, stream)
+                       : launch_tile<CfgFp8D64M4<SKT, TRV>>(p, tk, tv, grid, stream);
   if (p.D == 128)
-    return p.R <= 16 ? launch_tile<CfgFp8D128M1<SKT, TRV>>(p, tk, tv, grid, stream)
-                     : launch_tile<CfgFp8D128M2<SKT, TRV>>(p, tk, tv, grid, stream);
+    return p.R <= 16   ? launch_tile<CfgFp8D128M1<SKT, TRV>>(p, tk, tv, grid, stream)
+           : p.R <= 32 ? launch_tile<CfgFp8D128M2<SKT, TRV>>(p, tk, tv, grid, stream)
+                       : launch_tile<CfgFp8D128M4<SKT, TRV>>(p, tk, tv, grid, stream);
   return p.R <= 16 ? launch_tile<CfgFp8D256M1<SKT, TRV>>(p, tk, tv, grid, stream)
                    : launch_tile<CfgFp8D256M2<SKT, TRV>>(p, tk, tv, grid, stream);
 }

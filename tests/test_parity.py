@@ -298,6 +298,38 @@ def test_transposed_value_cache_agrees_with_plain():
     assert util.rel_l2(a, b) < 2e-3
 
 
+ROWS64 = [
+    # 33 to 64 query rows per KV head (four m-tiles): the first page's GQA 16 x qlen 4 and
+    # GQA 8 x qlen 7 / 8 cases (64 and 56 rows)
+    synth.Case("r64_bf16_d64", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3, qlen=4,
+               num_kv_heads=2, num_q_heads=32, head_dim=64, page_size=16,
+               context_lens=[4, 300, 2000], seed=3201),
+    synth.Case("r56_bf16_d128_q7_causal", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
+               batch=3, qlen=7, num_kv_heads=1, num_q_heads=8, head_dim=128, page_size=64,
+               context_lens=[3, 257, 1500], seed=3202, causal=True),
+    synth.Case("r64_fp8_token_d128_window", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16,
+               batch=3, qlen=4, num_kv_heads=1, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[17, 800, 4000], seed=3203, kv_std=20.0, window=1000),
+    synth.Case("r64_fp8_tensor_d64_trans_v", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16,
+               batch=3, qlen=4, num_kv_heads=2, num_q_heads=32, head_dim=64, page_size=32,
+               context_lens=[1, 500, 2500], fill=synth.FILL_INF, seed=3204, kv_std=20.0,
+               trans_v=True),
+    synth.Case("r64_fp8_tensor_d128_q8_trans_v", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_E4M3,
+               batch=3, qlen=8, num_kv_heads=1, num_q_heads=8, head_dim=128, page_size=128,
+               context_lens=[9, 700, 3000], fill=synth.FILL_INF, seed=3205, kv_std=20.0,
+               trans_v=True, causal=True),
+]
+
+
+@pytest.mark.parametrize("case", ROWS64, ids=lambda c: c.name)
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_up_to_64_query_rows_per_kv_head(case, mode):
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
