@@ -349,7 +349,8 @@ void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub, int* dw)
       m == 1 ? geometry_of<CfgBf16D128M1>(tw, sub, dw)
              : (m == 2 ? geometry_of<CfgBf16D128M2>(tw, sub, dw) : geometry_of<CfgBf16D128M4>(tw, sub, dw));
     else
-      m == 1 ? geometry_of<CfgBf16D256M1>(tw, sub, dw) : geometry_of<CfgBf16D256M2>(tw, sub, dw);
+      m == 1 ? geometry_of<CfgBf16D256M1>(tw, sub, dw)
+             : (m == 2 ? geometry_of<CfgBf16D256M2>(tw, sub, dw) : geometry_of<CfgBf16D256M4>(tw, sub, dw));
   } else if (kind == KIND_FP8) {
     if (head_dim == 64)
       m == 1 ? geometry_of<CfgFp8D64M1<SK_TOKEN>>(tw, sub, dw)
@@ -361,7 +362,8 @@ void tile_geometry(int kind, int head_dim, int rows, int* tw, int* sub, int* dw)
                        : geometry_of<CfgFp8D128M4<SK_TOKEN>>(tw, sub, dw));
     else
       m == 1 ? geometry_of<CfgFp8D256M1<SK_TOKEN>>(tw, sub, dw)
-             : geometry_of<CfgFp8D256M2<SK_TOKEN>>(tw, sub, dw);
+             : (m == 2 ? geometry_of<CfgFp8D256M2<SK_TOKEN>>(tw, sub, dw)
+                       : geometry_of<CfgFp8D256M4<SK_TOKEN>>(tw, sub, dw));
   } else {
     geometry_of<CfgFp4D128M1>(tw, sub, dw);
   }
@@ -376,7 +378,7 @@ namespace {
 
 using pa::WsLayout;
 
-constexpr int kMaxRows = 64;         // G * qlen served by the tile kernels (32 at head_dim 256)
+constexpr int kMaxRows = 64;         // G * qlen served by the tile kernels
 constexpr int kDefaultMaxParts = 128;
 constexpr int kMaxParts = 128;  // the in-decode merge keeps [rows, partitions] weights in smem
 
@@ -436,7 +438,7 @@ pa_status validate(const pa_decode_args* a) {
     return PA_ERR_UNSUPPORTED;
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
-  if (R > kMaxRows || (R > 32 && a->head_dim > 128)) return PA_ERR_UNSUPPORTED;
+  if (R > kMaxRows) return PA_ERR_UNSUPPORTED;
   if (a->kv_dtype == PA_KV_MXFP4 && (a->head_dim != 128 || a->qlen != 1 || G > 16)) return PA_ERR_UNSUPPORTED;
   if (a->batch == 0) return PA_OK;
   if (!a->query || !a->key_cache || !a->value_cache || !a->block_tables || !a->context_lens || !a->out)

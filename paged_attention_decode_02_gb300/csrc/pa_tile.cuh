@@ -75,7 +75,10 @@ struct TileCfg {
   static constexpr int OFF_CR = OFF_Q + RPAD * D * 2;
   static constexpr int OFF_X = OFF_CR + RPAD * 4;
   static constexpr int XW = MT * NT * 4 * 32;  // floats per warp per exchange buffer
-  static constexpr int X_BYTES = NDW == 2 ? NTG * 2 * 2 * XW * 4 : 0;
+  // partial-score exchange between the head-dim warps of a token group: double-buffered
+  // for two warps, one buffer (and a second barrier) for four
+  static constexpr int XBUFS = NDW > 2 ? 1 : 2;
+  static constexpr int X_BYTES = NDW > 1 ? NTG * XBUFS * NDW * XW * 4 : 0;
   static constexpr int OFF_OB = OFF_X + X_BYTES;
   // merged rows (RPAD x D floats), reused by the fused partition merge for its weights
   // (RPAD x up to 128 partitions)
@@ -641,28 +644,36 @@ __device__ __forceinline__ void stage_compute(
 #pragma unroll
       for (int j = 0; j < 4; ++j) sacc[0][nt][j] += sacc2[0][nt][j];
   }
-  // ---------------- combine the two head-dim halves ----------------
-  if constexpr (C::NDW == 2) {
+  // ---------------- combine the head-dim parts of the token group ----------------
+  // Every warp of the group adds the NDW partial scores in the same order (part 0 first),
+  // so all of them hold the same scores and run the same softmax.
+  if constexpr (C::NDW > 1) {
     float* xb = reinterpret_cast<float*>(smem + C::OFF_X);
-    float* mine = xb + ((tg * 2 + xbuf) * 2 + dw) * C::XW;
-    const float* other = xb + ((tg * 2 + xbuf) * 2 + (dw ^ 1)) * C::XW;
+    const float* parts = xb + (tg * C::XBUFS + xbuf) * C::NDW * C::XW;
+    float* mine = const_cast<float*>(parts) + dw * C::XW;
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) mine[((mt * C::NT + nt) * 4 + j) * 32 + lane] = sacc[mt][nt][j];
-    named_bar(1 + tg, 64);
+    named_bar(1 + tg, C::NDW * 32);
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
       for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float x = other[((mt * C::NT + nt) * 4 + j) * 32 + lane];
-          sacc[mt][nt][j] = dw == 0 ? sacc[mt][nt][j] + x : x + sacc[mt][nt][j];
+          const int e = ((mt * C::NT + nt) * 4 + j) * 32 + lane;
+          float x = dw == 0 ? sacc[mt][nt][j] : parts[e];
+#pragma unroll
+          for (int i = 1; i < C::NDW; ++i) x = x + (dw == i ? sacc[mt][nt][j] : parts[i * C::XW + e]);
+          sacc[mt][nt][j] = x;
         }
-    xbuf ^= 1;
+    if constexpr (C::XBUFS == 1)
+      named_bar(1 + tg, C::NDW * 32);  // one buffer: every part read before the next slice
+    else
+      xbuf ^= 1;
   }
   // ---------------- MXFP4 V references (lazy) and factor table ----------------
   if constexpr (C::KIND == KIND_FP4) {

@@ -13,8 +13,9 @@ int launch_tile_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtenso
     return p.R <= 16   ? launch_tile<CfgBf16D128M1>(p, tk, tv, grid, stream)
            : p.R <= 32 ? launch_tile<CfgBf16D128M2>(p, tk, tv, grid, stream)
                        : launch_tile<CfgBf16D128M4>(p, tk, tv, grid, stream);
-  return p.R <= 16 ? launch_tile<CfgBf16D256M1>(p, tk, tv, grid, stream)
-                   : launch_tile<CfgBf16D256M2>(p, tk, tv, grid, stream);
+  return p.R <= 16   ? launch_tile<CfgBf16D256M1>(p, tk, tv, grid, stream)
+         : p.R <= 32 ? launch_tile<CfgBf16D256M2>(p, tk, tv, grid, stream)
+                     : launch_tile<CfgBf16D256M4>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pa

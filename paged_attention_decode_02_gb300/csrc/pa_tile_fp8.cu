@@ -14,8 +14,9 @@ static int launch_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtens
     return p.R <= 16   ? launch_tile<CfgFp8D128M1<SKT, TRV>>(p, tk, tv, grid, stream)
            : p.R <= 32 ? launch_tile<CfgFp8D128M2<SKT, TRV>>(p, tk, tv, grid, stream)
                        : launch_tile<CfgFp8D128M4<SKT, TRV>>(p, tk, tv, grid, stream);
-  return p.R <= 16 ? launch_tile<CfgFp8D256M1<SKT, TRV>>(p, tk, tv, grid, stream)
-                   : launch_tile<CfgFp8D256M2<SKT, TRV>>(p, tk, tv, grid, stream);
+  return p.R <= 16   ? launch_tile<CfgFp8D256M1<SKT, TRV>>(p, tk, tv, grid, stream)
+         : p.R <= 32 ? launch_tile<CfgFp8D256M2<SKT, TRV>>(p, tk, tv, grid, stream)
+                     : launch_tile<CfgFp8D256M4<SKT, TRV>>(p, tk, tv, grid, stream);
 }
 
 int launch_tile_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

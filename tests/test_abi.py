@@ -81,11 +81,6 @@ REFUSED = [
     ("Hq not a multiple of Hkv", dict(num_q_heads=15, num_kv_heads=2), ops.PA_ERR_INVALID_ARG),
     ("qlen 0", dict(qlen=0), ops.PA_ERR_INVALID_ARG),
     ("G*qlen > 64", dict(qlen=5), ops.PA_ERR_UNSUPPORTED),
-    ("head_dim 256 with 48 rows", dict(qlen=3, head_dim=256, q_stride_head=256,
-                                       out_stride_head=256, q_stride_token=16 * 256,
-                                       out_stride_token=16 * 256, kv_stride_token=256,
-                                       kv_stride_head=256 * 128, kv_stride_block=256 * 128),
-     ops.PA_ERR_UNSUPPORTED),
     ("bf16 with scales", dict(kv_dtype=ops.PA_KV_BF16), ops.PA_ERR_UNSUPPORTED),
     ("fp8 with e8m0", dict(kv_scale=ops.PA_SCALE_E8M0_32), ops.PA_ERR_UNSUPPORTED),
     ("mxfp4 qlen 2", dict(kv_dtype=ops.PA_KV_MXFP4, kv_scale=ops.PA_SCALE_E8M0_32, qlen=2,

@@ -318,6 +318,17 @@ ROWS64 = [
                batch=3, qlen=8, num_kv_heads=1, num_q_heads=8, head_dim=128, page_size=128,
                context_lens=[9, 700, 3000], fill=synth.FILL_INF, seed=3205, kv_std=20.0,
                trans_v=True, causal=True),
+    # head_dim 256: four warps split the head dim of a token group
+    synth.Case("r64_bf16_d256_causal", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=3,
+               qlen=4, num_kv_heads=1, num_q_heads=16, head_dim=256, page_size=64,
+               context_lens=[1, 300, 1500], seed=3206, causal=True),
+    synth.Case("r64_fp8_token_d256_q8_window", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16,
+               batch=3, qlen=8, num_kv_heads=2, num_q_heads=16, head_dim=256, page_size=16,
+               context_lens=[9, 777, 3000], seed=3207, kv_std=20.0, window=900),
+    synth.Case("r64_fp8_tensor_d256_trans_v", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16,
+               batch=3, qlen=4, num_kv_heads=1, num_q_heads=16, head_dim=256, page_size=32,
+               context_lens=[2, 600, 2200], fill=synth.FILL_INF, seed=3208, kv_std=20.0,
+               trans_v=True),
 ]
 
 
