@@ -17,7 +17,9 @@ e2e    = the same metric through the C ABI with host buffers: per step the query
          double-buffered, overlapping the neighbouring steps' compute.
 per_config = every workload of the method, timed one call at a time through the C ABI
          (plan + tile + reduce, device buffers) with the 129 MB L2 flushed before each
-         call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak.
+         call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak; also
+         the same call replayed from a CUDA graph, and tile + reduce on a plan built
+         beforehand (us_per_call_planned).
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -149,7 +151,10 @@ def kernel_source_hash():
 
 
 def per_config(device, peak, calls=10, warmup=3):
-    """µs/call and GB/s of every workload of the method, one call at a time, L2 flushed."""
+    """µs/call and GB/s of every workload of the method, one call at a time, L2 flushed:
+    the whole call (plan, decode, reduce), the same call replayed from a CUDA graph, and
+    decode + reduce on a plan built beforehand (a model plans once per step and reuses the
+    plan in every layer; the pages' "planned" timings take the plan as an input too)."""
     cases = [synth.config1(), synth.config2("a"), synth.config2("b"), synth.config3(qlen=1),
              synth.config3(qlen=4)] + [synth.config4(batch=b) for b in (8, 64, 512, 4096)]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
@@ -177,10 +182,14 @@ def per_config(device, peak, calls=10, warmup=3):
                 ops.pa_decode_run(args, ws, gs)
         stream.wait_stream(gs)
         torch.cuda.synchronize()
-        ts, tg = [], []
+        def planned():
+            ops.pa_decode(args, ws, stream)
+            ops.pa_decode_reduce(args, ws, stream)
+
+        ts, tg, tp = [], [], []
         for _ in range(calls):
             for launch, acc in ((lambda: ops.pa_decode_run(args, ws, stream), ts),
-                                (graph.replay, tg)):
+                                (graph.replay, tg), (planned, tp)):
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -190,10 +199,11 @@ def per_config(device, peak, calls=10, warmup=3):
                 acc.append(e0.elapsed_time(e1))
         assert ops.pa_decode_read_status(ws) == 0, case.name
         nbytes = synth.algorithmic_bytes(case, p["context_lens"].cpu().tolist())
-        med, medg = statistics.median(ts), statistics.median(tg)
+        med, medg, medp = statistics.median(ts), statistics.median(tg), statistics.median(tp)
         name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
         res[name] = {"us_per_call": round(med * 1e3, 2),
-                     "us_per_call_graph": round(medg * 1e3, 2), "algorithmic_bytes": nbytes,
+                     "us_per_call_graph": round(medg * 1e3, 2),
+                     "us_per_call_planned": round(medp * 1e3, 2), "algorithmic_bytes": nbytes,
                      "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
                      "GBps_graph": round(nbytes / (medg * 1e-3) / 1e9, 1),
                      "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
