@@ -399,3 +399,63 @@ int orc_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ---- MXFP4 quantisation: the cache write whose pages the decode reads ------------
+ *
+ * "[FlyDSL] pa_decode: MXFP4 K/V ...", Dependencies: the MXFP4 pages come from a KV write
+ * kernel.  The pages name the format (e2m1 values, one e8m0 scale per 32 along head_dim,
+ * element 2j in the low nibble of byte j) but not the conversion into it; the conversion
+ * here is the OCP MX one.  Per block of 32 values: the shared scale is
+ * X = 2^(floor(log2 amax) - 2) (2 = the largest exponent of e2m1, whose largest value is
+ * 6 = 1.5 * 2^2), and each value becomes the e2m1 value nearest to x / X, ties to the code
+ * with an even mantissa bit, saturating at +-6, keeping the sign (a negative value that
+ * rounds to zero is the code of -0).  Where the format leaves a choice: an all-zero block
+ * takes scale byte 127 (X = 1); the exponent is clamped to [-126, 127], so scale bytes
+ * stay in 1..254 (the decode takes 0 and 255 as undefined in owned rows); a block holding
+ * a NaN or an infinity takes byte 255 (NaN) and zero codes.
+ */
+static uint8_t orc_e2m1_nearest(double y) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const double a = fabs(y);
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = fabs(a - mag[c]), db = fabs(a - mag[best]);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c; /* a tie goes to the even code */
+  }
+  return (uint8_t)(best | (signbit(y) ? 8 : 0));
+}
+
+/* Quantises n values (n a multiple of 32) into n/2 data bytes and n/32 scale bytes.
+ * Returns 0, or -1 if n is not a multiple of 32. */
+int orc_mxfp4_quantize(const float* x, int n, uint8_t* data, uint8_t* scales) {
+  if (n <= 0 || n % 32) return -1;
+  memset(data, 0, (size_t)n / 2);
+  for (int b = 0; b < n / 32; ++b) {
+    const float* v = x + 32 * b;
+    double amax = 0.0;
+    int finite = 1;
+    for (int i = 0; i < 32; ++i) {
+      if (!isfinite(v[i])) finite = 0;
+      else if (fabs((double)v[i]) > amax) amax = fabs((double)v[i]);
+    }
+    uint8_t sb = 127;
+    double X = 1.0;
+    if (!finite) {
+      sb = 255;
+    } else if (amax > 0.0) {
+      int e;
+      (void)frexp(amax, &e); /* amax = f * 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+      int E = (e - 1) - 2;
+      E = E < -126 ? -126 : (E > 127 ? 127 : E);
+      sb = (uint8_t)(E + 127);
+      X = ldexp(1.0, E);
+    }
+    scales[b] = sb;
+    for (int i = 0; i < 32; ++i) {
+      const uint8_t code = finite ? orc_e2m1_nearest((double)v[i] / X) : 0;
+      const int j = 32 * b + i;
+      data[j / 2] |= (uint8_t)(j % 2 == 0 ? code : code << 4);
+    }
+  }
+  return 0;
+}

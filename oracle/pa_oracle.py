@@ -98,6 +98,9 @@ def lib():
             L.orc_e4m3_round.argtypes = [ctypes.c_float]
             L.orc_e4m3_round.restype = ctypes.c_double
             L.orc_max_threads.restype = ctypes.c_int
+            L.orc_mxfp4_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.c_void_p]
+            L.orc_mxfp4_quantize.restype = ctypes.c_int
             _lib = L
         return _lib
 
@@ -210,3 +213,19 @@ def decode_bf16(bits: int) -> float:
 
 def max_threads() -> int:
     return lib().orc_max_threads()
+
+
+def mxfp4_quantize(x: np.ndarray):
+    """The oracle's MXFP4 conversion of float32 values [..., D] (D a multiple of 32):
+    returns (data uint8 [..., D/2], e8m0 scales uint8 [..., D/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    D = x.shape[-1]
+    rows = x.reshape(-1, D)
+    data = np.zeros((rows.shape[0], D // 2), np.uint8)
+    scales = np.zeros((rows.shape[0], D // 32), np.uint8)
+    for r in range(rows.shape[0]):
+        rc = lib().orc_mxfp4_quantize(rows[r].ctypes.data, D, data[r].ctypes.data,
+                                      scales[r].ctypes.data)
+        if rc != 0:
+            raise ValueError("head_dim must be a multiple of 32")
+    return data.reshape(*x.shape[:-1], D // 2), scales.reshape(*x.shape[:-1], D // 32)
