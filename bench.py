@@ -209,9 +209,46 @@ def per_config(device, peak, calls=10, warmup=3):
                      "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
         del graph
         del p, out, ws
+    res.update(kv_write_config(device, peak, calls))
     del flush
     torch.cuda.empty_cache()
     return res
+
+
+def kv_write_config(device, peak, calls):
+    """The MXFP4 KV-cache write (include/pa_kv_write.h): 65536 new tokens x 8 KV heads x
+    head_dim 128, K and V, scattered over the slots of a paged cache; bytes = bf16 rows read
+    + e2m1 data and e8m0 scales written + the slot map.  The 268 MB of rows read are twice
+    the L2, so calls run back to back without a flush (a flush by writing would leave L2
+    full of dirty lines, whose write-back this write-heavy kernel would pay for)."""
+    T, Hkv, D, S = 65536, 8, 128, 128
+    NB = T // S + 1
+    g = torch.Generator().manual_seed(4242)
+    key = torch.randn((T, Hkv, D), generator=g).to(torch.bfloat16).to(device)
+    value = torch.randn((T, Hkv, D), generator=g).to(torch.bfloat16).to(device)
+    slots = (torch.randperm(T, generator=g) + S).to(torch.int64).to(device)  # block 0 unused
+    kc = torch.zeros((NB, Hkv, S, D // 2), dtype=torch.uint8, device=device)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((NB, Hkv, S, D // 32), dtype=torch.uint8, device=device)
+    vs = torch.zeros_like(ks)
+    args = ops.mxfp4_write_args(key, value, slots, kc, vc, ks, vs)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        ops.mxfp4_kv_write(args, stream)
+    ts = []
+    for _ in range(calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ops.mxfp4_kv_write(args, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    med = statistics.median(ts)
+    nbytes = 2 * T * Hkv * (2 * D + D // 2 + D // 32) + 8 * T
+    return {"mxfp4_kv_write_t65536_h8_d128": {
+        "us_per_call": round(med * 1e3, 2), "algorithmic_bytes": nbytes,
+        "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
+        "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}}
 
 
 def make_variant(kv, device, batch=None):

@@ -9,8 +9,9 @@
  *     x_t = softmax_scale * q_scale * <q[s,i,h,:], k_t>,
  *
  * where token t of sequence s lives in page block_tables[s, t / page_size], slot
- * t mod page_size, and L_s = context_lens[s].  Queries are not causally masked
- * (every query position sees all L_s tokens).  References: "[FlyDSL] pa_decode:
+ * t mod page_size, and L_s = context_lens[s].  By default queries are not causally
+ * masked (every query position sees all L_s tokens); `causal` and `sliding_window` in
+ * pa_decode_args restrict what each query position sees.  References: "[FlyDSL] pa_decode:
  * zero V rows past the context before PV" (Root cause, Fix) and "[FlyDSL]
  * pa_decode: MXFP4 K/V in the shared PA tile kernel" (Summary, Self-Review).
  *
@@ -53,10 +54,10 @@
  *   (round to nearest), y rounded to the nearest e4m3 (ties to even, saturating at
  *   448), used as e4m3(y) * s; q_scale is not read.
  *
- * Supported shapes (others return PA_ERR_UNSUPPORTED): head_dim 128 or 256
- * (MXFP4: 128); page_size 16, 32, 64, 128 or 256; G * qlen <= 32 (MXFP4: <= 16,
+ * Supported shapes (others return PA_ERR_UNSUPPORTED): head_dim 64, 128 or 256
+ * (MXFP4: 128); page_size 16, 32, 64, 128 or 256; G * qlen <= 64 (MXFP4: <= 16,
  * qlen 1); kv_stride_token == row_bytes; 16-byte aligned cache, scale and
- * stride values.
+ * stride values.  fp8 per-tensor caches may store V transposed (`trans_v`).
  */
 #ifndef PA_DECODE_H_
 #define PA_DECODE_H_

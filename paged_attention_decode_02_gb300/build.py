@@ -16,7 +16,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_decode.so")
 SOURCES = ["pa_decode.cu", "pa_tile_bf16.cu", "pa_tile_fp8.cu", "pa_tile_mxfp4.cu",
-           "pa_tc_bf16.cu", "pa_tc_fp8.cu", "pa_tc_mxfp4.cu", "pa_decode_static.cu"]
+           "pa_tc_bf16.cu", "pa_tc_fp8.cu", "pa_tc_mxfp4.cu", "pa_decode_static.cu",
+           "pa_kv_write.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

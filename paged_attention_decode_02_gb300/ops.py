@@ -26,7 +26,8 @@ PA_DEVICE_WAIT_TIMEOUT, PA_DEVICE_CONTEXT_CLAMPED = 1, 2
 
 EXPORTED = ["pa_decode_abi_version", "pa_decode_workspace_size", "pa_decode_validate",
             "pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run",
-            "pa_decode_read_status", "pa_status_string", "pa_decode_run_static"]
+            "pa_decode_read_status", "pa_status_string", "pa_decode_run_static",
+            "pa_mxfp4_kv_write"]
 STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -92,6 +93,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         L.pa_decode_read_status.restype = ctypes.c_int32
         L.pa_status_string.argtypes = [ctypes.c_int32]
         L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_mxfp4_kv_write.argtypes = [ctypes.POINTER(Mxfp4WriteArgs), ctypes.c_void_p]
+        L.pa_mxfp4_kv_write.restype = ctypes.c_int32
         if path is None:
             _lib = L
         return L
@@ -293,3 +296,48 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)
     return out, args, workspace
+
+
+class Mxfp4WriteArgs(ctypes.Structure):
+    """Mirror of ``pa_mxfp4_write_args`` (include/pa_kv_write.h)."""
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32), ("key", ctypes.c_void_p), ("value", ctypes.c_void_p),
+        ("src_stride_token", ctypes.c_int64), ("src_stride_head", ctypes.c_int64),
+        ("slot_mapping", ctypes.c_void_p), ("key_cache", ctypes.c_void_p),
+        ("value_cache", ctypes.c_void_p), ("cache_stride_block", ctypes.c_int64),
+        ("cache_stride_head", ctypes.c_int64), ("key_scale", ctypes.c_void_p),
+        ("value_scale", ctypes.c_void_p), ("scale_stride_block", ctypes.c_int64),
+        ("scale_stride_head", ctypes.c_int64),
+    ]
+
+
+def mxfp4_write_args(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+                     key_cache: torch.Tensor, value_cache: torch.Tensor,
+                     key_scale: torch.Tensor, value_scale: torch.Tensor) -> Mxfp4WriteArgs:
+    """key / value bf16 [T, Hkv, D]; slot_mapping int64 [T]; caches uint8 [NB, Hkv, S, D/2]
+    and e8m0 scales uint8 [NB, Hkv, S, D/32] (token rows dense)."""
+    if key.stride() != value.stride() or key.dtype != torch.bfloat16 or value.dtype != torch.bfloat16:
+        raise ValueError("key and value: bf16 [T, Hkv, D] with the same strides")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if key_cache.stride() != value_cache.stride() or key_scale.stride() != value_scale.stride():
+        raise ValueError("key and value caches (and scale caches) must share strides")
+    a = Mxfp4WriteArgs()
+    a.num_tokens, a.num_kv_heads, a.head_dim = key.shape[0], key.shape[1], key.shape[2]
+    a.num_blocks, a.page_size = key_cache.shape[0], key_cache.shape[2]
+    a.key, a.value = _ptr(key), _ptr(value)
+    a.src_stride_token, a.src_stride_head = key.stride(0), key.stride(1)
+    a.slot_mapping = _ptr(slot_mapping)
+    a.key_cache, a.value_cache = _ptr(key_cache), _ptr(value_cache)
+    a.cache_stride_block, a.cache_stride_head = key_cache.stride(0), key_cache.stride(1)
+    a.key_scale, a.value_scale = _ptr(key_scale), _ptr(value_scale)
+    a.scale_stride_block, a.scale_stride_head = key_scale.stride(0), key_scale.stride(1)
+    return a
+
+
+def mxfp4_kv_write(args: Mxfp4WriteArgs, stream=None):
+    """Quantise and write the rows described by ``args`` (see include/pa_kv_write.h)."""
+    _check(load_library().pa_mxfp4_kv_write(ctypes.byref(args), _stream_handle(stream)),
+           "pa_mxfp4_kv_write")

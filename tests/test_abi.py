@@ -1,6 +1,7 @@
-"""The C ABI: the library loads, exports what include/pa_decode.h declares, and refuses
-malformed or unsupported arguments on the host (no GPU work)."""
+"""The C ABI: the library loads, exports what include/*.h declare, and refuses malformed
+or unsupported arguments on the host (no GPU work)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -8,8 +9,7 @@ import pytest
 
 from paged_attention_decode_02_gb300 import build, ops
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
-                      "pa_decode.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +19,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in glob.glob(os.path.join(INCLUDE, "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declarations_are_exported(lib):
@@ -145,3 +147,50 @@ def test_workspace_grows_with_budget_and_rows(lib):
 def test_status_strings(lib):
     for s in (0, -1, -2, -3, -4):
         assert lib.pa_status_string(s)
+
+
+def test_write_args_layout_matches_header():
+    # 5 int32 (padded to 24 bytes), then 13 pointers and int64s
+    assert ops.Mxfp4WriteArgs.key.offset == 24
+    assert ops.Mxfp4WriteArgs.scale_stride_head.offset == 24 + 12 * 8
+    assert ctypes.sizeof(ops.Mxfp4WriteArgs) == 24 + 13 * 8
+
+
+def _valid_write_args():
+    a = ops.Mxfp4WriteArgs()
+    a.num_tokens, a.num_kv_heads, a.head_dim, a.page_size, a.num_blocks = 4, 2, 128, 128, 8
+    fake = 1 << 20
+    a.key, a.value, a.slot_mapping = fake, fake * 2, fake * 3
+    a.src_stride_token, a.src_stride_head = 2 * 128, 128
+    a.key_cache, a.value_cache = fake * 4, fake * 5
+    a.cache_stride_head, a.cache_stride_block = 128 * 64, 2 * 128 * 64
+    a.key_scale, a.value_scale = fake * 6, fake * 7
+    a.scale_stride_head, a.scale_stride_block = 128 * 4, 2 * 128 * 4
+    return a
+
+
+WRITE_REFUSED = [
+    ("head_dim 96", dict(head_dim=96), ops.PA_ERR_UNSUPPORTED),
+    ("page 48", dict(page_size=48), ops.PA_ERR_UNSUPPORTED),
+    ("no key", dict(key=None), ops.PA_ERR_INVALID_ARG),
+    ("no slot mapping", dict(slot_mapping=None), ops.PA_ERR_INVALID_ARG),
+    ("negative tokens", dict(num_tokens=-1), ops.PA_ERR_INVALID_ARG),
+    ("overlapping source heads", dict(src_stride_head=64), ops.PA_ERR_INVALID_ARG),
+    ("overlapping cache heads", dict(cache_stride_head=64), ops.PA_ERR_INVALID_ARG),
+    ("short scale head stride", dict(scale_stride_head=8), ops.PA_ERR_INVALID_ARG),
+    ("unaligned key", dict(key=(1 << 20) + 2), ops.PA_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("what,changes,status", WRITE_REFUSED, ids=[r[0] for r in WRITE_REFUSED])
+def test_write_refused_arguments(lib, what, changes, status):
+    a = _valid_write_args()
+    for k, v in changes.items():
+        setattr(a, k, v)
+    assert lib.pa_mxfp4_kv_write(ctypes.byref(a), None) == status
+
+
+def test_write_with_no_tokens_launches_nothing(lib):
+    a = _valid_write_args()
+    a.num_tokens = 0
+    assert lib.pa_mxfp4_kv_write(ctypes.byref(a), None) == ops.PA_OK

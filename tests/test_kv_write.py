@@ -155,3 +155,123 @@ def test_planted_mistakes_are_caught():
     # scales one binade off (floor(log2 amax) - 1: the largest values would exceed 6)
     q = _dequant(d, (s.astype(np.int64) + 1).astype(np.uint8))
     assert np.abs(q - x).max() > 0
+
+
+# ---- GPU: the write kernel through the C ABI ---------------------------------------
+
+def _gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_attention_decode_02_gb300 import build, ops
+    build.build()
+    ops.load_library()
+    return ops
+
+
+def _gpu_write(ops, key, value, slots, NB, S):
+    T, Hkv, D = key.shape
+    kc = torch.full((NB, Hkv, S, D // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    vc = torch.full_like(kc, 0xAB)
+    ks = torch.full((NB, Hkv, S, D // 32), 0xAB, dtype=torch.uint8, device="cuda")
+    vs = torch.full_like(ks, 0xAB)
+    args = ops.mxfp4_write_args(key.cuda(), value.cuda(), slots.cuda(), kc, vc, ks, vs)
+    ops.mxfp4_kv_write(args)
+    torch.cuda.synchronize()
+    return kc.cpu().numpy(), vc.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_write_kernel_matches_oracle(D):
+    ops = _gpu_lib()
+    rng = np.random.default_rng(80 + D)
+    T, Hkv, NB, S = 300, 3, 12, 32
+    key = torch.from_numpy(_mixed_rows(rng, T * Hkv, D).reshape(T, Hkv, D)).to(torch.bfloat16)
+    value = torch.from_numpy(_mixed_rows(rng, T * Hkv, D).reshape(T, Hkv, D)).to(torch.bfloat16)
+    slots = torch.from_numpy(rng.permutation(NB * S)[:T].astype(np.int64))
+    slots[5] = -1          # skipped
+    slots[6] = NB * S + 3  # past the cache: skipped too
+    kc, vc, ks, vs = _gpu_write(ops, key, value, slots, NB, S)
+    for src, cache, sc in ((key, kc, ks), (value, vc, vs)):
+        d_ref, s_ref = orc.mxfp4_quantize(src.float().numpy())
+        written = np.zeros((NB, S), bool)
+        for t in range(T):
+            sl = int(slots[t])
+            if sl < 0 or sl >= NB * S:
+                continue
+            b, o = divmod(sl, S)
+            written[b, o] = True
+            assert np.array_equal(sc[b, :, o], s_ref[t]), t
+            assert np.array_equal(_zero_sign(cache[b, :, o]), _zero_sign(d_ref[t])), t
+        # slots no token maps to keep their bytes ([NB, S, Hkv, ...] view for the mask)
+        assert np.all(np.moveaxis(cache, 2, 1)[~written] == 0xAB)
+        assert np.all(np.moveaxis(sc, 2, 1)[~written] == 0xAB)
+
+
+@pytest.mark.gpu
+def test_write_kernel_special_blocks():
+    ops = _gpu_lib()
+    x = np.zeros((4, 1, 128), np.float32)
+    x[0, 0, 32] = np.nan
+    x[0, 0, 64] = -np.inf
+    x[1, 0, :32] = 1e-39          # subnormal bf16 values
+    x[2, 0, :] = 3.0e38           # near the bf16 maximum
+    x[3, 0, ::2] = -1e-6          # tiny negatives next to zeros
+    key = torch.from_numpy(x).to(torch.bfloat16)
+    slots = torch.arange(4, dtype=torch.int64)
+    kc, _, ks, _ = _gpu_write(ops, key, key.clone(), slots, 1, 16)
+    d_ref, s_ref = orc.mxfp4_quantize(key.float().numpy())
+    assert np.array_equal(ks[0, 0, :4], s_ref[:, 0])
+    assert np.array_equal(_zero_sign(kc[0, 0, :4]), _zero_sign(d_ref[:, 0]))
+
+
+@pytest.mark.gpu
+def test_written_cache_decodes_like_the_oracle():
+    # bf16 K/V -> the GPU write -> the GPU decode, against the oracle decode of the same
+    # rows quantised by the oracle (no oracle input comes from the CUDA path)
+    ops = _gpu_lib()
+    from paged_attention_decode_02_gb300 import synth
+    from tests import util
+    rng = np.random.default_rng(90)
+    B, Hkv, G, D, S = 3, 2, 8, 128, 128
+    lens = [300, 1000, 2049]
+    pages = [(L + S - 1) // S for L in lens]
+    NB = 1 + sum(pages)
+    perm = rng.permutation(np.arange(1, NB))
+    bt = np.zeros((B, max(pages) + 2), np.int32)
+    pos = 0
+    slots = []
+    for s, (L, n) in enumerate(zip(lens, pages)):
+        bt[s, :n] = perm[pos:pos + n]
+        pos += n
+        slots += [int(bt[s, t // S]) * S + t % S for t in range(L)]
+    T = len(slots)
+    kx = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 3).to(torch.bfloat16)
+    vx = torch.from_numpy(rng.standard_normal((T, Hkv, D)) * 3).to(torch.bfloat16)
+    kc, vc, ks, vs = _gpu_write(ops, kx, vx, torch.tensor(slots, dtype=torch.int64), NB, S)
+    # the oracle's cache: the same rows, quantised by the oracle, unwritten rows zero
+    okc, ovc = np.zeros_like(kc), np.zeros_like(vc)
+    oks, ovs = np.full_like(ks, 127), np.full_like(vs, 127)
+    for src, c, sc in ((kx, okc, oks), (vx, ovc, ovs)):
+        d, e = orc.mxfp4_quantize(src.float().numpy())
+        for t, sl in enumerate(slots):
+            c[sl // S, :, sl % S] = d[t]
+            sc[sl // S, :, sl % S] = e[t]
+    q = torch.randn((B, 1, Hkv * G, D), generator=torch.Generator().manual_seed(91)).to(torch.bfloat16)
+    case = synth.Case("written", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_BF16, batch=B, qlen=1,
+                      num_kv_heads=Hkv, num_q_heads=Hkv * G, head_dim=D, page_size=S,
+                      context_lens=lens)
+    ctx = torch.tensor(lens, dtype=torch.int32)
+    ref = util.oracle_decode({"case": case, "query": q, "q_scale": None,
+                              "key_cache": torch.from_numpy(okc), "value_cache": torch.from_numpy(ovc),
+                              "key_scale": torch.from_numpy(oks), "value_scale": torch.from_numpy(ovs),
+                              "block_tables": torch.from_numpy(bt), "context_lens": ctx,
+                              "num_blocks": NB})
+    dev = {"case": case, "query": q.cuda(), "q_scale": None,
+           "key_cache": torch.from_numpy(kc).cuda(), "value_cache": torch.from_numpy(vc).cuda(),
+           "key_scale": torch.from_numpy(ks).cuda(), "value_scale": torch.from_numpy(vs).cuda(),
+           "block_tables": torch.from_numpy(bt).cuda(), "context_lens": ctx.cuda(), "num_blocks": NB}
+    out = torch.full(tuple(q.shape), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out, _, ws = ops.decode(dev, out)
+    torch.cuda.synchronize()
+    util.assert_parity(out.float().cpu().numpy(), ref, case.kv, "written cache")
