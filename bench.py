@@ -561,7 +561,14 @@ def main():
                     help="skip the per-workload µs/call table")
     ap.add_argument("--kernel", default=None, choices=["mma", "tc"],
                     help="decode kernel: mma.sync (default) or the tcgen05 kernel")
+    ap.add_argument("--kv-write", action="store_true",
+                    help="time only the MXFP4 KV-cache write (--steps calls after 3 warm-up) "
+                         "and print its line")
     a = ap.parse_args()
+    if a.kv_write:
+        ops.load_library()
+        print(json.dumps(kv_write_config("cuda", peaks()[0], a.steps)))
+        return
     if a.kernel is not None:
         os.environ["PA_DECODE_KERNEL"] = a.kernel
     if a.warmup < 3 and a.impl == "ours":
