@@ -18,8 +18,9 @@ e2e    = the same metric through the C ABI with host buffers: per step the query
 per_config = every workload of the method, timed one call at a time through the C ABI
          (plan + tile + reduce, device buffers) with the 129 MB L2 flushed before each
          call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak; also
-         the same call replayed from a CUDA graph, and tile + reduce on a plan built
-         beforehand (us_per_call_planned).
+         the same call replayed from a CUDA graph, tile + reduce on a plan built
+         beforehand (us_per_call_planned), and the one-launch plan-free call with one
+         partition per unit (us_per_call_plan_free).
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -170,8 +171,15 @@ def per_config(device, peak, calls=10, warmup=3):
                              out, key_scale=p["key_scale"], value_scale=p["value_scale"],
                              q_scale=p["q_scale"], softmax_scale=case.scale_qk())
         ws = ops.alloc_workspace(args, device)
+        # one partition per unit: pa_decode_run runs the tile kernel alone, without a plan
+        args1 = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"],
+                              p["context_lens"], out, key_scale=p["key_scale"],
+                              value_scale=p["value_scale"], q_scale=p["q_scale"],
+                              softmax_scale=case.scale_qk(), max_partitions=1)
+        ws1 = ops.alloc_workspace(args1, device)
         for _ in range(warmup):
             ops.pa_decode_run(args, ws, stream)
+            ops.pa_decode_run(args1, ws1, stream)
         # the same call captured once in a CUDA graph (how a serving loop issues it)
         gs = torch.cuda.Stream(device)
         gs.wait_stream(stream)
@@ -186,10 +194,11 @@ def per_config(device, peak, calls=10, warmup=3):
             ops.pa_decode(args, ws, stream)
             ops.pa_decode_reduce(args, ws, stream)
 
-        ts, tg, tp = [], [], []
+        ts, tg, tp, tf = [], [], [], []
         for _ in range(calls):
             for launch, acc in ((lambda: ops.pa_decode_run(args, ws, stream), ts),
-                                (graph.replay, tg), (planned, tp)):
+                                (graph.replay, tg), (planned, tp),
+                                (lambda: ops.pa_decode_run(args1, ws1, stream), tf)):
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -197,18 +206,20 @@ def per_config(device, peak, calls=10, warmup=3):
                 e1.record(stream)
                 torch.cuda.synchronize()
                 acc.append(e0.elapsed_time(e1))
-        assert ops.pa_decode_read_status(ws) == 0, case.name
+        assert ops.pa_decode_read_status(ws) == 0 and ops.pa_decode_read_status(ws1) == 0, case.name
         nbytes = synth.algorithmic_bytes(case, p["context_lens"].cpu().tolist())
         med, medg, medp = statistics.median(ts), statistics.median(tg), statistics.median(tp)
+        medf = statistics.median(tf)
         name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
         res[name] = {"us_per_call": round(med * 1e3, 2),
                      "us_per_call_graph": round(medg * 1e3, 2),
-                     "us_per_call_planned": round(medp * 1e3, 2), "algorithmic_bytes": nbytes,
+                     "us_per_call_planned": round(medp * 1e3, 2),
+                     "us_per_call_plan_free": round(medf * 1e3, 2), "algorithmic_bytes": nbytes,
                      "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
                      "GBps_graph": round(nbytes / (medg * 1e-3) / 1e9, 1),
                      "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
         del graph
-        del p, out, ws
+        del p, out, ws, ws1
     res.update(kv_write_config(device, peak, calls))
     del flush
     torch.cuda.empty_cache()

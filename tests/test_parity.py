@@ -341,6 +341,37 @@ def test_up_to_64_query_rows_per_kv_head(case, mode):
     util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
 
 
+PLAN_FREE = [synth.config1(), synth.config4(batch=8),
+             synth.config4(batch=5, context_lens=[2048, 1, 129, 0, 3000], seed=2005),
+             synth.config3(qlen=4, batch=3, context_lens=(200, 900), seed=2004),
+             WINDOW[1], TRANS_V[0], CAUSAL[0], ROWS64[2]]
+
+
+@pytest.mark.parametrize("case", PLAN_FREE, ids=lambda c: f"{c.name}-b{c.batch}")
+def test_plan_free_equals_one_partition_plan(case):
+    # pa_decode_run with max_partitions 1 runs no plan and no reduce; plan + decode + reduce
+    # with max_partitions 1 must give the same bits (the pages' plan-free mode)
+    p = synth.make(case)
+    dev = synth.to_device(p, "cuda")
+    free = run_gpu(p, max_partitions=1, task_budget=7)
+    out = torch.full(tuple(p["query"].shape), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q = dev["query"].view(torch.float8_e4m3fn) if dev["query"].dtype == torch.uint8 else dev["query"]
+    args = ops.make_args(q, dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                         dev["context_lens"], out, key_scale=dev["key_scale"],
+                         value_scale=dev["value_scale"], q_scale=dev["q_scale"],
+                         softmax_scale=case.scale_qk(), max_partitions=1, task_budget=7,
+                         causal=case.causal, q_quant=case.q_quant, sliding_window=case.window,
+                         trans_v=case.trans_v)
+    ws = ops.alloc_workspace(args)
+    ops.pa_decode_plan(args, ws)
+    ops.pa_decode(args, ws)
+    ops.pa_decode_reduce(args, ws)
+    torch.cuda.synchronize()
+    assert ops.pa_decode_read_status(ws) == 0
+    assert np.array_equal(free, out.float().cpu().numpy(), equal_nan=False)
+    util.assert_parity(free, util.oracle_decode(p), case.kv, case.name + " plan-free")
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
