@@ -29,6 +29,11 @@
  *   whose own place in the context is p = L - qlen + i, sees only the tokens t > p - W:
  *   the W tokens ending at itself, cut further by causal masking when that is set.
  *   Tokens before every position's window (t < L - qlen - W + 1) are never read.
+ *   With sinks (one fp32 logit per query head, in the units of the softmax-scaled scores;
+ *   the pages list "sinks" beside sliding window among what the MXFP4 path refuses,
+ *   without defining them), every row's softmax takes one more term with a zero value:
+ *   out = sum_t exp(x_t - M) v_t / (sum_t exp(x_t - M) + exp(s_h - M)),
+ *   M = max(max_t x_t, s_h); a row that sees no token gives zeros.
  *   With trans_v set, the value cache stores each page head-dim major: [NB, Hkv, D, S],
  *   the S tokens of one head dim contiguous (the first page's probe covers fp8
  *   per-tensor caches with "trans_v" and with plain V, without defining the layout; this
@@ -91,6 +96,7 @@ typedef struct {
   int32_t causal;
   int32_t window; /* sliding window W (0: none) */
   int32_t trans_v; /* value cache [NB, Hkv, D, S] (bf16 / e4m3 only) */
+  const float* sinks; /* [Hq] or NULL */
 } orc_args;
 
 /* ---- format decoders ---------------------------------------------------- */
@@ -357,7 +363,14 @@ int orc_pa_decode(const orc_args* a, double* out, int nthreads) {
         for (int r = 0; r < R; ++r) {
           int i = r / G, h = hkv * G + r % G;
           double* dst = out + ((((int64_t)s * a->qlen + i) * a->num_q_heads + h) * D);
-          for (int d = 0; d < D; ++d) dst[d] = o[(int64_t)r * D + d];
+          double f = 1.0; /* o = sum_t exp(x_t - m) v_t / l; with a sink the denominator grows */
+          if (a->sinks && l[r] > 0.0) {
+            const double sk = (double)a->sinks[h];
+            const double Mp = m[r] > sk ? m[r] : sk; /* M = max(max_t x_t, s_h) */
+            const double num = l[r] * exp(m[r] - Mp);
+            f = num / (num + exp(sk - Mp));
+          }
+          for (int d = 0; d < D; ++d) dst[d] = o[(int64_t)r * D + d] * f;
         }
       }
     }

@@ -53,6 +53,7 @@ class OrcArgs(ctypes.Structure):
         ("causal", ctypes.c_int32),
         ("window", ctypes.c_int32),
         ("trans_v", ctypes.c_int32),
+        ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -140,7 +141,7 @@ class Problem:
                  num_blocks, kv_format, scale_kind, q_format, softmax_scale, query,
                  key_cache, value_cache, block_tables, context_lens, key_scale=None,
                  value_scale=None, q_scale=None, causal=False, window=0,
-                 trans_v=False):
+                 trans_v=False, sinks=None):
         self.keep = []
         a = OrcArgs()
         a.batch, a.qlen, a.num_q_heads, a.num_kv_heads = batch, qlen, num_q_heads, num_kv_heads
@@ -153,6 +154,9 @@ class Problem:
         a.causal = int(bool(causal))
         a.window = int(window)
         a.trans_v = int(bool(trans_v))
+        sk = _np(sinks, np.float32) if sinks is not None else None
+        a.sinks = _ptr(sk)
+        self.keep.append(sk)
         q = _np(query)
         kc, vc = _np(key_cache), _np(value_cache)
         ks = _np(key_scale)

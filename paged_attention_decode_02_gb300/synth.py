@@ -57,6 +57,9 @@ class Case:
     window: int = 0
     # value cache stored head-dim major per page, [NB, Hkv, D, S] (bf16 / fp8 only)
     trans_v: bool = False
+    # attention sinks: one fp32 logit per query head (in the units of the softmax-scaled
+    # scores), drawn N(sink_mean, 1); None: no sinks
+    sink_mean: Optional[float] = None
     pad_columns: int = 2
     extra_blocks: int = 0
     # > 0: magnitudes grow along each sequence by 2^(ramp * position / length) -- bf16 K and
@@ -254,6 +257,9 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
     unowned = ~own4
     _fill(case, caches, key_scale, value_scale, unowned, g)
 
+    sinks = None
+    if case.sink_mean is not None:
+        sinks = case.sink_mean + torch.randn((case.num_q_heads,), generator=g, dtype=torch.float32)
     vcache = caches[1].view(torch.bfloat16) if case.kv == KV_BF16 else caches[1]
     if case.trans_v:
         assert case.kv != KV_MXFP4, "trans_v is a bf16 / fp8 layout"
@@ -268,6 +274,7 @@ def make(case: Case, device: str | torch.device = "cpu") -> dict:
         "value_scale": value_scale,
         "block_tables": bt,
         "context_lens": lens,
+        "sinks": sinks,
         "owned": owned,
         "num_blocks": NB,
     }

@@ -137,6 +137,7 @@ def brute_force(p: dict, head_map=None, window=None) -> np.ndarray:
     B, qlen, Hq, D = Q.shape
     G = case.gqa
     S = case.page_size
+    sinks = p.get("sinks")
     out = torch.zeros((B, qlen, Hq, D), dtype=torch.float64)
     for s in range(B):
         L = int(p["context_lens"][s])
@@ -159,7 +160,11 @@ def brute_force(p: dict, head_map=None, window=None) -> np.ndarray:
                     continue
                 # unseen rows may hold NaN: select, never multiply
                 x = torch.where(seen, x, torch.tensor(-math.inf, dtype=x.dtype))
-                w = torch.softmax(x, dim=0)
+                if sinks is not None:  # the sink: one more softmax column, with a zero value
+                    xs = torch.cat([x, sinks[h].to(torch.float64).reshape(1)])
+                    w = torch.softmax(xs, dim=0)[:-1]
+                else:
+                    w = torch.softmax(x, dim=0)
                 out[s, i, h] = torch.where(seen[:, None], v, torch.zeros_like(v)).mul(w[:, None]).sum(0)
     return out.numpy()
 
@@ -201,6 +206,14 @@ def _tiny_cases():
         synth.Case("t_bf16_trans_v_window", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
                    batch=2, qlen=1, num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=32,
                    context_lens=[40, 90], fill=synth.FILL_NAN, seed=26, trans_v=True, window=33),
+        synth.Case("t_fp8_sinks", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=3,
+                   qlen=2, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+                   context_lens=[1, 20, 60], fill=synth.FILL_NAN, seed=27, kv_std=20.0,
+                   sink_mean=2.0),
+        synth.Case("t_bf16_sinks_causal_window", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
+                   batch=3, qlen=3, num_kv_heads=1, num_q_heads=4, head_dim=64, page_size=16,
+                   context_lens=[2, 9, 50], fill=synth.FILL_NAN, seed=28, causal=True,
+                   window=6, sink_mean=0.0),
         synth.Case("t_mxfp4_window", synth.KV_MXFP4, synth.SCALE_E8M0, synth.Q_E4M3, batch=2,
                    qlen=1, num_kv_heads=1, num_q_heads=4, head_dim=128, page_size=16,
                    context_lens=[20, 45], fill=synth.FILL_RANDOM, seed=24, window=17),
@@ -386,6 +399,50 @@ def test_transposed_value_cache_gives_the_same_result(kv):
     wrong["case"] = synth.replace(case, trans_v=False)
     wrong["value_cache"] = pt["value_cache"].reshape(p["value_cache"].shape)
     assert util.rel_l2(util.oracle_decode(wrong), util.oracle_decode(p)) > 1e-2
+
+
+def test_sinks_at_minus_infinity_change_nothing():
+    case = synth.Case("sk0", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=3, qlen=2,
+                      num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=16,
+                      context_lens=[1, 30, 70], seed=65, kv_std=20.0)
+    p = synth.make(case)
+    ps = dict(p)
+    ps["sinks"] = torch.full((8,), -1e30)
+    assert np.array_equal(util.oracle_decode(ps), util.oracle_decode(p))
+
+
+def test_sinks_with_identical_keys_closed_form():
+    # every score equals c: out = mean(V) * L e^c / (L e^c + e^s)
+    case = synth.Case("skc", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=1, qlen=1,
+                      num_kv_heads=1, num_q_heads=3, head_dim=64, page_size=16,
+                      context_lens=[37], seed=66)
+    p = synth.make(case)
+    kc = p["key_cache"].clone()
+    row = kc[int(p["block_tables"][0, 0]), 0, 0].clone()
+    for t in range(37):
+        kc[int(p["block_tables"][0, t // 16]), 0, t % 16] = row
+    p["key_cache"] = kc
+    p["sinks"] = torch.tensor([-1.0, 0.5, 4.0])
+    got = util.oracle_decode(p)
+    V = _dequant_dense(p, "v")
+    t = torch.arange(37)
+    mean = V[p["block_tables"][0].long()[t // 16], 0, t % 16].mean(dim=0).numpy()
+    Q = _query_dense(p)
+    for h in range(3):
+        c = float(row.to(torch.float64) @ Q[0, 0, h]) * case.scale_qk()
+        s_h = float(p["sinks"][h])
+        want = mean * (37 * math.exp(c)) / (37 * math.exp(c) + math.exp(s_h))
+        np.testing.assert_allclose(got[0, 0, h], want, rtol=1e-12, atol=1e-13)
+
+
+def test_a_dominant_sink_drives_the_output_to_zero():
+    case = synth.Case("skz", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16, batch=2, qlen=1,
+                      num_kv_heads=1, num_q_heads=2, head_dim=64, page_size=16,
+                      context_lens=[5, 40], seed=67)
+    p = synth.make(case)
+    p["sinks"] = torch.tensor([600.0, 600.0])
+    got = util.oracle_decode(p)
+    assert np.all(np.isfinite(got)) and np.abs(got).max() < 1e-200
 
 
 def test_e4m3_rounding_matches_torch():

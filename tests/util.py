@@ -37,7 +37,7 @@ def oracle_problem(p: dict, seqs=None) -> orc.Problem:
         key_cache=cpu(p["key_cache"]), value_cache=cpu(p["value_cache"]),
         key_scale=cpu(p["key_scale"]), value_scale=cpu(p["value_scale"]), q_scale=qs,
         block_tables=bt, context_lens=cl, causal=case.causal, window=case.window,
-        trans_v=case.trans_v)
+        trans_v=case.trans_v, sinks=cpu(p.get("sinks")))
 
 
 def oracle_decode(p: dict, seqs=None, nthreads: int = 0) -> np.ndarray:
