@@ -158,10 +158,17 @@ typedef struct pa_decode_args {
    * layout; this is the plain transposed reading.  fp8 with a per-tensor scale only
    * (PA_ERR_UNSUPPORTED otherwise); the tcgen05 kernel does not take it. */
   int32_t trans_v;
+  /* Attention sinks: fp32 [Hq], one logit per query head in the units of the
+   * softmax-scaled scores, or NULL.  Every row of query head h then takes one more softmax
+   * term with a zero value: out = sum_t e^(x_t - M) v_t / (sum_t e^(x_t - M) + e^(s_h - M)),
+   * M = max(max_t x_t, s_h); a row that sees no token stays zero.  The pages list sinks
+   * beside sliding window among what the MXFP4 path refuses, without defining them; this
+   * is the plain reading.  Every format; the tcgen05 kernel does not take them. */
+  const float* sinks;
 } pa_decode_args;
 
 /* ABI version of this header; a mismatched library refuses nothing but reports it here. */
-#define PA_DECODE_ABI_VERSION 4
+#define PA_DECODE_ABI_VERSION 5
 int32_t pa_decode_abi_version(void);
 
 /* Bytes of workspace the three calls need for these shapes (plan, partition scratch,

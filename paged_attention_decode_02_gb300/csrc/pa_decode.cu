@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(256) pa_reduce_kernel(const ReduceParams rp) {
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  if (rp.sinks != nullptr && W > 0.f) W += fast_exp2(rp.sinks[h] * kLog2e - mb);  // the sink's term
   const float inv = W > 0.f ? 1.f / W : 0.f;
   __syncwarp();
   for (int q = lane; q < P; q += 32) w[q] *= inv;
@@ -492,14 +493,14 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
 // and pages of at least 8 tokens, with the separate reduce, not causal, without a sliding
-// window and with token-major V.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
+// window or sinks, and with token-major V.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
 // each call); otherwise every shape runs the mma.sync kernel, the faster of the two on
 // the long-context workloads.
 bool tc_kernel_applies(const pa_decode_args* a, int rows) {
   const char* e = getenv("PA_DECODE_KERNEL");
   const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
   return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
-         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && !a->trans_v &&
+         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && !a->trans_v && !a->sinks &&
          a->q_dtype != PA_Q_BF16_TO_E4M3;
 }
 
@@ -708,6 +709,7 @@ pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* s
   p.causal = a->causal && a->qlen > 1;
   p.window = a->sliding_window;
   p.trans_v = a->trans_v;
+  p.sinks = a->sinks;
   p.Hq = a->num_q_heads;
   p.Hkv = a->num_kv_heads;
   p.G = G;
@@ -797,6 +799,7 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
   uint8_t* w = static_cast<uint8_t*>(ws);
   pa::ReduceParams rp;
   rp.B = a->batch;
+  rp.sinks = a->sinks;
   rp.qlen = a->qlen;
   rp.Hq = a->num_q_heads;
   rp.Hkv = a->num_kv_heads;

@@ -13,6 +13,7 @@ constexpr int kTileTokens = 256;  // the plan's work unit: ceil(L / 256) tiles p
 // cost (query load, first-slice latency, masked tail, merge and store) measured at about
 // two tiles' worth of streaming on the long-context workloads.
 constexpr int kUnitCostTiles = 2;
+constexpr float kLog2e = 1.4426950408889634f;  // sinks are natural-log logits; scores are log2
 
 // One task = a run of consecutive 256-token tiles of one (sequence, KV head) unit.
 struct PlanTask {
@@ -49,6 +50,7 @@ struct DecodeParams {
   int causal;  // qlen > 1: query position i sees tokens < L - qlen + 1 + i
   int window;  // > 0: query position i sees tokens > L - qlen + i - window
   int trans_v;  // value cache [NB, Hkv, D, S] (fp8 per-tensor)
+  const float* sinks;  // [Hq] logits joining every row's softmax with a zero value, or null
   int q_quant;  // bf16 query quantised per head row to e4m3 (scale amax / 448)
   int drop_first_slice;  // test hook: warp 0 of each CTA never loads its first slice
   const void* q;
@@ -91,6 +93,7 @@ struct PlanParams {
 
 struct ReduceParams {
   int B, qlen, Hq, Hkv, G, R, D;
+  const float* sinks;  // [Hq] or null
   const int* nparts;
   const int* part_base;
   const float* part_ml;

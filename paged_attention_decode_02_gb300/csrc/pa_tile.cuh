@@ -1201,7 +1201,11 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int row = 16 * mt + g + 8 * hr;
-          fin[row] = Lrow[mt][hr] > 0.f ? 1.f / Lrow[mt][hr] : 0.f;
+          float den = Lrow[mt][hr];
+          // a row written here (one partition) takes its query head's sink in the sum
+          if (p.sinks != nullptr && nparts <= 1 && den > 0.f && row < p.R)
+            den += fast_exp2(p.sinks[hkv * p.G + row % p.G] * kLog2e - Mrow[mt][hr]);
+          fin[row] = den > 0.f ? 1.f / den : 0.f;
           if (nparts > 1 && row < p.R)
             reinterpret_cast<float2*>(p.part_ml)[slot * p.R + row] =
                 make_float2(Mrow[mt][hr], Lrow[mt][hr]);
@@ -1302,6 +1306,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
           }
 #pragma unroll
           for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+          if (p.sinks != nullptr && W > 0.f) W += fast_exp2(p.sinks[hkv * p.G + r % p.G] * kLog2e - mb);
           const float inv = W > 0.f ? 1.f / W : 0.f;
           __syncwarp();
           for (int q = lane; q < nparts; q += 32) wts[r * nparts + q] *= inv;

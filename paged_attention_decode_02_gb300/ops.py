@@ -53,6 +53,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
         ("out_stride_head", ctypes.c_int64), ("causal", ctypes.c_int32),
         ("sliding_window", ctypes.c_int32), ("trans_v", ctypes.c_int32),
+        ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -125,7 +126,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               max_partitions: int = 0, task_budget: int = 0,
               merge_in_decode: bool = False, causal: bool = False,
               q_quant: bool = False, sliding_window: int = 0,
-              trans_v: bool = False) -> PaDecodeArgs:
+              trans_v: bool = False, sinks: Optional[torch.Tensor] = None) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -137,6 +138,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     causal: query position i sees tokens < L - qlen + 1 + i.  sliding_window W > 0: query
     position i sees only tokens > L - qlen + i - W.  trans_v: value_cache is [NB, Hkv, D, S]
     (e4m3 bytes, per-tensor scale), with the key cache's block and head strides.
+    sinks: fp32 [Hq], one softmax logit per query head with a zero value, or None.
     """
     D = query.shape[-1]
     Hq = query.shape[-2]
@@ -177,6 +179,9 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     a.causal = int(bool(causal))
     a.sliding_window = int(sliding_window)
     a.trans_v = int(bool(trans_v))
+    if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() != Hq):
+        raise ValueError("sinks: fp32, one per query head")
+    a.sinks = _ptr(sinks)
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
@@ -291,7 +296,7 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      task_budget=task_budget, merge_in_decode=merge_in_decode,
                      causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False),
                      sliding_window=getattr(case, "window", 0),
-                     trans_v=getattr(case, "trans_v", False))
+                     trans_v=getattr(case, "trans_v", False), sinks=problem.get("sinks"))
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -31,17 +31,18 @@ def test_header_declarations_are_exported(lib):
     assert set(ops.EXPORTED) == set(names), names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.pa_decode_abi_version() == 4
+    assert lib.pa_decode_abi_version() == 5
 
 
 def test_args_struct_layout_matches_header():
     # 16 int32/float fields, then 19 pointers and int64s, then the causal flag and the
-    # sliding window, then trans_v (padded)
-    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 21 * 8
+    # sliding window, then trans_v (padded), then the sinks pointer
+    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 22 * 8
     assert ops.PaDecodeArgs.query.offset == 64
     assert ops.PaDecodeArgs.causal.offset == 64 + 19 * 8
     assert ops.PaDecodeArgs.sliding_window.offset == 64 + 19 * 8 + 4
     assert ops.PaDecodeArgs.trans_v.offset == 64 + 20 * 8
+    assert ops.PaDecodeArgs.sinks.offset == 64 + 21 * 8
 
 
 def _valid_args():

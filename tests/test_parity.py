@@ -341,6 +341,43 @@ def test_up_to_64_query_rows_per_kv_head(case, mode):
     util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
 
 
+SINKS = [
+    synth.Case("sinks_fp8_token", synth.KV_FP8, synth.SCALE_TOKEN, synth.Q_BF16, batch=4,
+               qlen=1, num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
+               context_lens=[1, 100, 1000, 4000], seed=3301, kv_std=20.0, sink_mean=2.0),
+    synth.Case("sinks_bf16_q4_causal_window", synth.KV_BF16, synth.SCALE_NONE, synth.Q_BF16,
+               batch=3, qlen=4, num_kv_heads=1, num_q_heads=8, head_dim=256, page_size=64,
+               context_lens=[3, 300, 2000], seed=3302, causal=True, window=200, sink_mean=1.0),
+    synth.replace(synth.config4(batch=8, seed=3303), sink_mean=40.0),
+    synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=3304),
+                  sink_mean=45.0),
+    synth.replace(TRANS_V[0], sink_mean=2.0, seed=3305),
+]
+
+
+@pytest.mark.parametrize("case", SINKS, ids=lambda c: c.name)
+@pytest.mark.parametrize("mode", ["split", "direct", "fused"])
+def test_attention_sinks_match_oracle(case, mode):
+    p = synth.make(case)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=24,
+                  merge_in_decode=mode == "fused")
+    util.assert_parity(got, util.oracle_decode(p), case.kv, case.name + " sinks")
+
+
+def test_sink_limits():
+    # a sink at -1e30 weighs nothing: the bits of the call without sinks; a dominant sink
+    # takes all the weight: zero rows
+    case = SINKS[0]
+    p = synth.make(synth.replace(case, sink_mean=None))
+    for maxp in (0, 1):  # split partitions with the reduce; one partition written directly
+        plain = run_gpu(p, max_partitions=maxp, task_budget=24)
+        q = dict(p)
+        q["sinks"] = torch.full((case.num_q_heads,), -1e30)
+        assert np.array_equal(run_gpu(q, max_partitions=maxp, task_budget=24), plain), maxp
+        q["sinks"] = torch.full((case.num_q_heads,), 600.0)
+        assert np.all(run_gpu(q, max_partitions=maxp, task_budget=24) == 0.0), maxp
+
+
 PLAN_FREE = [synth.config1(), synth.config4(batch=8),
              synth.config4(batch=5, context_lens=[2048, 1, 129, 0, 3000], seed=2005),
              synth.config3(qlen=4, batch=3, context_lens=(200, 900), seed=2004),
