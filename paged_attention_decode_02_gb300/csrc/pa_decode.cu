@@ -752,10 +752,8 @@ pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* s
   p.part_o = reinterpret_cast<float*>(w + L.part_o);
   p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
   int grid = L.budget;
-  if (plan_free) {
-    p.tasks = nullptr;
-    p.nparts = nullptr;
-    p.part_base = nullptr;
+  p.plan_free = plan_free;
+  if (plan_free) {  // the kernel writes the task records and partition counts itself
     p.chunk_first = nullptr;
     p.counters = nullptr;
     const long long units = (long long)a->batch * a->num_kv_heads;

@@ -352,24 +352,8 @@ struct SliceIt {
   int bx0, bcur, bnxt;  // blocks of this warp's boxes bx0 + lane and bx0 + 32 + lane in the task
 };
 
-// Task i: the plan's record, or without a plan (p.tasks == nullptr: "[FlyDSL] pa_decode:
-// MXFP4 K/V ...", Summary: work_plan=None runs one task per sequence and writes the row
-// directly) the whole of unit i = (sequence i / Hkv, KV head i mod Hkv), from the tile of
-// the first token any sliding window holds.
-__device__ __forceinline__ PlanTask get_task(const DecodeParams& p, int i) {
-  if (p.tasks != nullptr) return p.tasks[i];
-  PlanTask tk;
-  tk.seq = i / p.Hkv;
-  tk.hkv_part = i - tk.seq * p.Hkv;
-  const int L = clamped_context(p, tk.seq);
-  const int lo = p.window > 0 ? L - p.qlen - p.window + 1 : 0;
-  tk.tile_begin = (lo > 0 ? lo : 0) / kTileTokens;
-  tk.tile_end = (L + kTileTokens - 1) / kTileTokens;
-  return tk;
-}
-
 __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p) {
-  const PlanTask tk = get_task(p, it.task);
+  const PlanTask tk = p.tasks[it.task];
   it.s = tk.seq;
   it.hkv = tk.hkv_part & 0xFFFF;
   it.L = clamped_context(p, it.s);
@@ -994,7 +978,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   QRaw<C> qn;  // query words of the next task to start
   if constexpr (C::Q_EARLY) {
     if (t_begin < t_end) {
-      const PlanTask tk0 = get_task(p, t_begin);
+      const PlanTask tk0 = p.tasks[t_begin];
       load_q_issue<C>(p, tk0.seq, tk0.hkv_part & 0xFFFF, cw, lane, qn);
     }
   }
@@ -1032,14 +1016,14 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   const int wcap = p.window > 0 ? p.window : 0x7FFFFFFF;
 
   for (int task = t_begin; task < t_end; ++task) {
-    const PlanTask tk = get_task(p, task);
+    const PlanTask tk = p.tasks[task];
     const int s = tk.seq, hkv = tk.hkv_part & 0xFFFF, part = tk.hkv_part >> 16;
     const int L = clamped_context(p, s);
     const int t0 = tk.tile_begin * kTileTokens;
     int t1 = tk.tile_end * kTileTokens;
     t1 = t1 < L ? t1 : L;
     const int unit = s * p.Hkv + hkv;
-    const int nparts = p.nparts != nullptr ? p.nparts[unit] : 1;  // plan-free: one task a unit
+    const int nparts = p.nparts[unit];
     const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
 
     if constexpr (!C::Q_EARLY) load_q_issue<C>(p, s, hkv, cw, lane, qn);
@@ -1047,16 +1031,9 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
     named_bar(BAR_CONSUMERS, C::NCW * 32);
     // The next task's record, read at this task's merge, copied without waiting for it.
     if (C::Q_EARLY && task + 1 < t_end && cw == 0 && lane == 0) {
-      if (p.tasks != nullptr) {
-        cp_async16(smem + C::OFF_NXT, p.tasks + task + 1);
-        cp_async_commit();
-      } else {  // read after the barrier that follows the merge's (max, sum) writes
-        *reinterpret_cast<PlanTask*>(smem + C::OFF_NXT) = get_task(p, task + 1);
-      }
+      cp_async16(smem + C::OFF_NXT, p.tasks + task + 1);
+      cp_async_commit();
     }
-    // without a plan, the context clamp is reported here (the plan reports it otherwise)
-    if (p.tasks == nullptr && cw == 0 && lane == 0 && p.ctx[s] > p.W * p.S)
-      atomicOr(p.status, ST_CLAMPED);
     // Touch this task's output rows now, so that their address translation is not first
     // needed by the stores at the end of the task, with the memory system under load.
     if (cw == 0 && lane == 0) {
@@ -1375,14 +1352,35 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
   pdl_launch_dependents();  // the reduce kernel may launch (after the plan completed); it
                             // waits for this grid's results
   int t_begin, t_end;
-  if (p.tasks != nullptr) {  // the plan's chunk
+  if (!p.plan_free) {  // the plan's chunk
     t_begin = p.chunk_first[blockIdx.x];
     t_end = p.chunk_first[blockIdx.x + 1];
-  } else {  // without a plan: a contiguous run of units per CTA
+  } else {
+    // Without a plan ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary: work_plan=None runs one
+    // task per sequence and writes the row directly): a contiguous run of (sequence, KV
+    // head) units per CTA, one task per unit over its whole context (from the tile of the
+    // first token any sliding window holds).  The CTA writes its own records and partition
+    // counts into the plan's regions of the workspace (task index = unit index) and runs
+    // them as planned tasks; it also reports a clamped context, as the plan would.
     const int units = p.B * p.Hkv;
     const int k = (units + (int)gridDim.x - 1) / (int)gridDim.x;
     t_begin = min(units, (int)blockIdx.x * k);
     t_end = min(units, t_begin + k);
+    PlanTask* tasks = const_cast<PlanTask*>(p.tasks);
+    int* nparts = const_cast<int*>(p.nparts);
+    for (int u = t_begin + (int)threadIdx.x; u < t_end; u += (int)blockDim.x) {
+      PlanTask tk;
+      tk.seq = u / p.Hkv;
+      tk.hkv_part = u - tk.seq * p.Hkv;
+      const int L = clamped_context(p, tk.seq);
+      const int lo = p.window > 0 ? L - p.qlen - p.window + 1 : 0;
+      tk.tile_begin = (lo > 0 ? lo : 0) / kTileTokens;
+      tk.tile_end = (L + kTileTokens - 1) / kTileTokens;
+      tasks[u] = tk;
+      nparts[u] = 1;
+      if (p.ctx[tk.seq] > p.W * p.S) atomicOr(p.status, ST_CLAMPED);
+    }
+    __syncthreads();  // the records are read by every warp of this CTA only
   }
   warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, t_begin, t_end, threadIdx.x >> 5,
                threadIdx.x & 31);
