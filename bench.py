@@ -19,8 +19,8 @@ per_config = every workload of the method, timed one call at a time through the 
          (plan + tile + reduce, device buffers) with the 129 MB L2 flushed before each
          call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak; also
          the same call replayed from a CUDA graph, tile + reduce on a plan built
-         beforehand (us_per_call_planned), and the one-launch plan-free call with one
-         partition per unit (us_per_call_plan_free).
+         beforehand (us_per_call_planned), and the whole call with one partition per
+         unit, rows written directly and no reduce (us_per_call_one_partition).
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -171,7 +171,7 @@ def per_config(device, peak, calls=10, warmup=3):
                              out, key_scale=p["key_scale"], value_scale=p["value_scale"],
                              q_scale=p["q_scale"], softmax_scale=case.scale_qk())
         ws = ops.alloc_workspace(args, device)
-        # one partition per unit: pa_decode_run runs the tile kernel alone, without a plan
+        # one partition per unit (the pages' plan-free mode): rows written directly, no reduce
         args1 = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"],
                               p["context_lens"], out, key_scale=p["key_scale"],
                               value_scale=p["value_scale"], q_scale=p["q_scale"],
@@ -214,7 +214,7 @@ def per_config(device, peak, calls=10, warmup=3):
         res[name] = {"us_per_call": round(med * 1e3, 2),
                      "us_per_call_graph": round(medg * 1e3, 2),
                      "us_per_call_planned": round(medp * 1e3, 2),
-                     "us_per_call_plan_free": round(medf * 1e3, 2), "algorithmic_bytes": nbytes,
+                     "us_per_call_one_partition": round(medf * 1e3, 2), "algorithmic_bytes": nbytes,
                      "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
                      "GBps_graph": round(nbytes / (medg * 1e-3) / 1e9, 1),
                      "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}

@@ -211,13 +211,12 @@ pa_status pa_decode(const pa_decode_args* args, void* workspace, size_t workspac
 pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
                            size_t workspace_bytes, void* stream);
 
-/* plan + decode + reduce in one call, on one stream.  With max_partitions == 1 (and the
- * mma.sync kernel) it is one launch without a plan: each CTA takes a contiguous run of
- * (sequence, KV head) units, one task per unit covering its whole context, and writes the
- * rows directly; the workspace's status word is cleared by a memset first.  The result is
- * bitwise the same as plan + decode with max_partitions == 1 ("[FlyDSL] pa_decode: MXFP4
- * K/V ...", Summary: work_plan=None runs one task per sequence and writes the row directly,
- * and a plan with max_partitions == 1 is served the same way). */
+/* plan + decode + reduce in one call, on one stream.  With max_partitions == 1 every
+ * (sequence, KV head) unit is one task whose rows the decode writes directly, and the
+ * reduce launches nothing: the pages' plan-free mode ("[FlyDSL] pa_decode: MXFP4 K/V ...",
+ * Summary: work_plan=None runs one task per sequence and writes the row directly, and a
+ * plan with max_partitions == 1 is served the same way) with the plan still built, in a
+ * few microseconds, by pa_decode_plan. */
 pa_status pa_decode_run(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);
 

@@ -668,14 +668,7 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-}  // extern "C"
-
-namespace {
-
-// Launches the decode kernel: on the plan in the workspace, or without one (plan_free:
-// one task per (sequence, KV head) unit, rows written directly; the tile kernel only).
-pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* stream,
-                        bool plan_free) {
+pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
   pa_status st = validate(a);
   if (st != PA_OK) return st;
   WsLayout L;
@@ -684,7 +677,7 @@ pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* s
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   const int kind = a->kv_dtype == PA_KV_BF16 ? pa::KIND_BF16 : (a->kv_dtype == PA_KV_FP8_E4M3 ? pa::KIND_FP8 : pa::KIND_FP4);
-  const bool use_tc = !plan_free && tc_kernel_applies(a, R);
+  const bool use_tc = tc_kernel_applies(a, R);
   int tc = 0, sub = 0, dims = a->head_dim;
   if (use_tc) {
     tc = 128;
@@ -751,18 +744,7 @@ pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* s
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_o = reinterpret_cast<float*>(w + L.part_o);
   p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
-  int grid = L.budget;
-  p.plan_free = plan_free;
-  if (plan_free) {  // the kernel writes the task records and partition counts itself
-    p.chunk_first = nullptr;
-    p.counters = nullptr;
-    const long long units = (long long)a->batch * a->num_kv_heads;
-    grid = units < L.budget ? (int)units : L.budget;
-    // the plan kernel is what clears the status word otherwise
-    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-  }
+  const int grid = L.budget;
   int rc;
   if (use_tc) {
     if (kind == pa::KIND_BF16)
@@ -778,14 +760,6 @@ pa_status launch_decode(const pa_decode_args* a, void* ws, size_t bytes, void* s
   else
     rc = pa::launch_tile_mxfp4(p, tk, tv, grid, stream);
   return rc == 0 ? PA_OK : PA_ERR_CUDA;
-}
-
-}  // namespace
-
-extern "C" {
-
-pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
-  return launch_decode(a, ws, bytes, stream, false);
 }
 
 pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
@@ -827,14 +801,6 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
 }
 
 pa_status pa_decode_run(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
-  // one partition per unit: no plan and no reduce, one launch ("[FlyDSL] pa_decode: MXFP4
-  // K/V ...", Summary: a plan with max_partitions == 1 is served as work_plan=None)
-  if (a && a->max_partitions == 1) {
-    pa_status st = validate(a);
-    if (st != PA_OK) return st;
-    const int R = a->qlen * (a->num_q_heads / a->num_kv_heads);
-    if (!tc_kernel_applies(a, R)) return launch_decode(a, ws, bytes, stream, true);
-  }
   pa_status st = pa_decode_plan(a, ws, bytes, stream);
   if (st != PA_OK) return st;
   if ((st = pa_decode(a, ws, bytes, stream)) != PA_OK) return st;

@@ -51,7 +51,6 @@ struct DecodeParams {
   int window;  // > 0: query position i sees tokens > L - qlen + i - window
   int trans_v;  // value cache [NB, Hkv, D, S] (fp8 per-tensor)
   const float* sinks;  // [Hq] logits joining every row's softmax with a zero value, or null
-  int plan_free;  // no plan: each CTA writes and runs one task per unit of its run of units
   int q_quant;  // bf16 query quantised per head row to e4m3 (scale amax / 448)
   int drop_first_slice;  // test hook: warp 0 of each CTA never loads its first slice
   const void* q;

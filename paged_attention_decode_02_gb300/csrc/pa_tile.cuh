@@ -1351,37 +1351,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
   pdl_wait_prior();         // the plan's task list is complete and visible from here on
   pdl_launch_dependents();  // the reduce kernel may launch (after the plan completed); it
                             // waits for this grid's results
-  int t_begin, t_end;
-  if (!p.plan_free) {  // the plan's chunk
-    t_begin = p.chunk_first[blockIdx.x];
-    t_end = p.chunk_first[blockIdx.x + 1];
-  } else {
-    // Without a plan ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary: work_plan=None runs one
-    // task per sequence and writes the row directly): a contiguous run of (sequence, KV
-    // head) units per CTA, one task per unit over its whole context (from the tile of the
-    // first token any sliding window holds).  The CTA writes its own records and partition
-    // counts into the plan's regions of the workspace (task index = unit index) and runs
-    // them as planned tasks; it also reports a clamped context, as the plan would.
-    const int units = p.B * p.Hkv;
-    const int k = (units + (int)gridDim.x - 1) / (int)gridDim.x;
-    t_begin = min(units, (int)blockIdx.x * k);
-    t_end = min(units, t_begin + k);
-    PlanTask* tasks = const_cast<PlanTask*>(p.tasks);
-    int* nparts = const_cast<int*>(p.nparts);
-    for (int u = t_begin + (int)threadIdx.x; u < t_end; u += (int)blockDim.x) {
-      PlanTask tk;
-      tk.seq = u / p.Hkv;
-      tk.hkv_part = u - tk.seq * p.Hkv;
-      const int L = clamped_context(p, tk.seq);
-      const int lo = p.window > 0 ? L - p.qlen - p.window + 1 : 0;
-      tk.tile_begin = (lo > 0 ? lo : 0) / kTileTokens;
-      tk.tile_end = (L + kTileTokens - 1) / kTileTokens;
-      tasks[u] = tk;
-      nparts[u] = 1;
-      if (p.ctx[tk.seq] > p.W * p.S) atomicOr(p.status, ST_CLAMPED);
-    }
-    __syncthreads();  // the records are read by every warp of this CTA only
-  }
+  const int t_begin = p.chunk_first[blockIdx.x], t_end = p.chunk_first[blockIdx.x + 1];
   warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, t_begin, t_end, threadIdx.x >> 5,
                threadIdx.x & 31);
 }

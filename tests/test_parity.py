@@ -385,9 +385,9 @@ PLAN_FREE = [synth.config1(), synth.config4(batch=8),
 
 
 @pytest.mark.parametrize("case", PLAN_FREE, ids=lambda c: f"{c.name}-b{c.batch}")
-def test_plan_free_equals_one_partition_plan(case):
-    # pa_decode_run with max_partitions 1 runs no plan and no reduce; plan + decode + reduce
-    # with max_partitions 1 must give the same bits (the pages' plan-free mode)
+def test_one_partition_run_equals_its_steps(case):
+    # one partition per unit (the pages' plan-free mode: each unit one task, rows written
+    # directly, no reduce): pa_decode_run and plan + decode + reduce give the same bits
     p = synth.make(case)
     dev = synth.to_device(p, "cuda")
     free = run_gpu(p, max_partitions=1, task_budget=7)
@@ -406,7 +406,7 @@ def test_plan_free_equals_one_partition_plan(case):
     torch.cuda.synchronize()
     assert ops.pa_decode_read_status(ws) == 0
     assert np.array_equal(free, out.float().cpu().numpy(), equal_nan=False)
-    util.assert_parity(free, util.oracle_decode(p), case.kv, case.name + " plan-free")
+    util.assert_parity(free, util.oracle_decode(p), case.kv, case.name + " one partition")
 
 
 QQUANT = [
