@@ -141,13 +141,39 @@ def traffic_from_profile():
         return None
 
 
-def kernel_source_hash():
+def _code_only(text: str) -> str:
+    """C / CUDA source without comments, trailing blanks or empty lines: what the compiler
+    sees, so that an edit of comments alone does not change the hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in "\"'":  # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln)
+
+
+def kernel_source_hash(csrc=None):
+    """sha256 (first 16 hex) over the kernel sources, comments removed."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_attention_decode_02_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_attention_decode_02_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

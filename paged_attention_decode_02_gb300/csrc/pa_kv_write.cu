@@ -33,7 +33,8 @@ struct WriteParams {
 
 // e8m0 byte of a finite block whose largest magnitude is amax, and 2^-E:
 // E = floor(log2 amax) - 2 clamped to [-126, 127] (read from the exponent field; a
-// subnormal amax lies below the clamp); an all-zero block takes byte 127 (X = 1).
+// subnormal amax lies below the clamp, and a finite bf16 amax puts E at most at 125, so
+// 2^-E stays a normal fp32); an all-zero block takes byte 127 (X = 1).
 __device__ __forceinline__ uint32_t block_scale(float amax, float* inv) {
   if (amax == 0.f) {
     *inv = 1.f;

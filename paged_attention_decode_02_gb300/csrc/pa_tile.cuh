@@ -8,13 +8,16 @@
 // ahead of the one it computes, so no warp ever waits for another inside a task.
 // Softmax state and the output accumulators are warp-private; QK^T and PV run on
 // mma.sync (m16n8k16, fp32 accumulate) with fp8 / fp4 operands widened to f16 in
-// registers.  Only a slice holding tokens at or past the context length runs the masked
+// registers.  Only a slice holding tokens at or past the context length (or past a
+// query position's causal limit, or before a sliding window's start) runs the masked
 // path: scores there become -inf, and V values and per-token scales become 0 by select,
 // so unowned rows never reach the output whatever bytes they hold ("[FlyDSL] pa_decode:
 // zero V rows past the context before PV", Fix).  At the end of a task the warps merge
 // their (max, sum, output) in a fixed order and store either the final bf16 row (units
-// with one partition) or a partial for the reduce kernel ("[FlyDSL] pa_decode: MXFP4
-// K/V ...", direct output commit).
+// with one partition; an attention sink joins the row's sum here) or a partial for the
+// reduce kernel ("[FlyDSL] pa_decode: MXFP4 K/V ...", direct output commit).  A
+// transposed value cache (fp8) arrives in 16-token pieces, one 16-byte row per head dim,
+// and the score columns take tokens in the order its fragments need (kv_token).
 #pragma once
 
 #include "pa_params.h"
