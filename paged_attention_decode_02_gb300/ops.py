@@ -279,6 +279,41 @@ def pa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
     return int(host.item())
 
 
+def paged_attention_decode(query: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                           key_scale: Optional[torch.Tensor] = None,
+                           value_scale: Optional[torch.Tensor] = None,
+                           q_scale: Optional[torch.Tensor] = None,
+                           softmax_scale: Optional[float] = None, max_partitions: int = 0,
+                           causal: bool = False, sliding_window: int = 0, trans_v: bool = False,
+                           sinks: Optional[torch.Tensor] = None, q_quant: bool = False,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode call on tensors: plan + decode + reduce on ``stream`` (default: the current
+    stream), returning ``out`` (bf16, the query's shape; allocated when not given).  The
+    arguments are those of make_args; ``workspace`` (from alloc_workspace) is allocated per
+    call when not given.  Every tensor must be on one CUDA device; a refused call raises
+    PaDecodeError.  Nothing here computes: the library does the work."""
+    tensors = [t for t in (query, key_cache, value_cache, block_tables, context_lens, out,
+                           key_scale, value_scale, q_scale, sinks, workspace) if t is not None]
+    devs = {t.device for t in tensors}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError(f"paged_attention_decode: every tensor must be on one CUDA device, got {devs}")
+    if query.dtype == torch.uint8:
+        query = query.view(torch.float8_e4m3fn)
+    if out is None:
+        out = torch.empty(query.shape, dtype=torch.bfloat16, device=query.device)
+    args = make_args(query, key_cache, value_cache, block_tables, context_lens, out,
+                     key_scale=key_scale, value_scale=value_scale, q_scale=q_scale,
+                     softmax_scale=softmax_scale, max_partitions=max_partitions, causal=causal,
+                     q_quant=q_quant, sliding_window=sliding_window, trans_v=trans_v,
+                     sinks=sinks)
+    if workspace is None:
+        workspace = alloc_workspace(args, query.device)
+    pa_decode_run(args, workspace, stream)
+    return out
+
+
 def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions: int = 0,
            task_budget: int = 0, workspace: Optional[torch.Tensor] = None,
            merge_in_decode: bool = False):

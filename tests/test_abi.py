@@ -195,3 +195,14 @@ def test_write_with_no_tokens_launches_nothing(lib):
     a = _valid_write_args()
     a.num_tokens = 0
     assert lib.pa_mxfp4_kv_write(ctypes.byref(a), None) == ops.PA_OK
+
+
+def test_tensor_wrapper_refuses_host_tensors():
+    # the one-call wrapper needs every tensor on one CUDA device (checked before any call)
+    import torch
+    q = torch.zeros(2, 1, 8, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 1, 16, 128, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    ctx = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="one CUDA device"):
+        ops.paged_attention_decode(q, kc, kc, bt, ctx)

@@ -409,6 +409,24 @@ def test_one_partition_run_equals_its_steps(case):
     util.assert_parity(free, util.oracle_decode(p), case.kv, case.name + " one partition")
 
 
+@pytest.mark.parametrize("case", [SINKS[0], synth.config4(batch=5, seed=3401), WINDOW[1]],
+                         ids=lambda c: c.name)
+def test_one_call_tensor_wrapper(case):
+    # ops.paged_attention_decode: tensors in, output out, on the current stream
+    p = synth.make(case)
+    dev = synth.to_device(p, "cuda")
+    out = ops.paged_attention_decode(
+        dev["query"], dev["key_cache"], dev["value_cache"], dev["block_tables"],
+        dev["context_lens"], key_scale=dev["key_scale"], value_scale=dev["value_scale"],
+        q_scale=dev["q_scale"], softmax_scale=case.scale_qk(), causal=case.causal,
+        sliding_window=case.window, trans_v=case.trans_v, sinks=dev.get("sinks"),
+        q_quant=case.q_quant)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == tuple(p["query"].shape)
+    util.assert_parity(out.float().cpu().numpy(), util.oracle_decode(p), case.kv,
+                       case.name + " wrapper")
+
+
 QQUANT = [
     synth.replace(synth.config4(batch=6, seed=2801), q=synth.Q_BF16, q_quant=True),
     synth.replace(synth.config5(synth.KV_MXFP4, batch=3, context_lens=(3000, 9000), seed=2802),
