@@ -478,6 +478,36 @@ def test_ragged_edges(lens):
         util.assert_parity(got, ref, case.kv, "edges")
 
 
+def _bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("kv,scale", [(synth.KV_BF16, synth.SCALE_NONE),
+                                      (synth.KV_FP8, synth.SCALE_TENSOR),
+                                      (synth.KV_FP8, synth.SCALE_TOKEN),
+                                      (synth.KV_MXFP4, synth.SCALE_E8M0)],
+                         ids=["bf16", "fp8_tensor", "fp8_token", "mxfp4"])
+def test_context_one_gives_that_v_row(kv, scale):
+    # one token: its softmax weight is exactly 1, so the output is that token's V row --
+    # bitwise for bf16 KV, within one bf16 ulp of the dequantised row otherwise
+    D = 128
+    case = synth.Case("ctx1", kv, scale, synth.Q_BF16, batch=3, qlen=1, num_kv_heads=2,
+                      num_q_heads=16, head_dim=D, page_size=16 if kv != synth.KV_MXFP4 else 128,
+                      context_lens=[1, 1, 1], seed=3501, kv_std=20.0)
+    p = synth.make(case)
+    got = run_gpu(p, task_budget=8)
+    ref = util.oracle_decode(p)  # the dequantised V row of token 0 (closed form, pinned on CPU)
+    if kv == synth.KV_BF16:
+        vc = p["value_cache"]
+        for s in range(3):
+            blk = int(p["block_tables"][s, 0])
+            for h in range(16):
+                assert np.array_equal(got[s, 0, h], vc[blk, h // 8, 0].float().numpy()), (s, h)
+    else:
+        assert np.all(np.abs(got - ref) <= _bf16_ulp(ref)), float(np.abs(got - ref).max())
+
+
 @pytest.mark.parametrize("kv", [synth.KV_MXFP4, synth.KV_FP8], ids=["5a_mxfp4", "5b_fp8_token"])
 def test_long_context_full_size_sampled(kv):
     # the launch configuration bench.py times: default split, separate reduce
