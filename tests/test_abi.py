@@ -206,3 +206,31 @@ def test_tensor_wrapper_refuses_host_tensors():
     ctx = torch.ones(2, dtype=torch.int32)
     with pytest.raises(ValueError, match="one CUDA device"):
         ops.paged_attention_decode(q, kc, kc, bt, ctx)
+
+
+def test_make_args_fills_the_variant_fields():
+    # host tensors are enough: make_args reads shapes, strides and pointers only
+    import torch
+    B, qlen, Hq, Hkv, D, S, NB = 2, 3, 8, 2, 128, 16, 6
+    q = torch.zeros(B, qlen, Hq, D, dtype=torch.bfloat16)
+    kc = torch.zeros(NB, Hkv, S, D, dtype=torch.uint8)
+    vt = torch.zeros(NB, Hkv, D, S, dtype=torch.uint8)  # transposed value cache
+    bt = torch.zeros(B, 4, dtype=torch.int32)
+    ctx = torch.ones(B, dtype=torch.int32)
+    out = torch.empty(B, qlen, Hq, D, dtype=torch.bfloat16)
+    sc = torch.tensor([0.05], dtype=torch.float32)
+    sinks = torch.zeros(Hq, dtype=torch.float32)
+    a = ops.make_args(q, kc, vt, bt, ctx, out, key_scale=sc, value_scale=sc, causal=True,
+                      sliding_window=100, trans_v=True, sinks=sinks)
+    assert (a.causal, a.sliding_window, a.trans_v) == (1, 100, 1)
+    assert a.sinks == sinks.data_ptr() and a.kv_dtype == ops.PA_KV_FP8_E4M3
+    assert a.kv_scale == ops.PA_SCALE_PER_TENSOR and a.qlen == qlen
+    # a token-major value cache with trans_v, and sinks of the wrong size or type, are refused
+    with pytest.raises(ValueError):
+        ops.make_args(q, kc, kc, bt, ctx, out, key_scale=sc, value_scale=sc, trans_v=True)
+    with pytest.raises(ValueError):
+        ops.make_args(q, kc, kc, bt, ctx, out, key_scale=sc, value_scale=sc,
+                      sinks=torch.zeros(Hq - 1))
+    with pytest.raises(ValueError):
+        ops.make_args(q, kc, kc, bt, ctx, out, key_scale=sc, value_scale=sc,
+                      sinks=torch.zeros(Hq, dtype=torch.float64))
