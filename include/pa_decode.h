@@ -154,8 +154,8 @@ typedef struct pa_decode_args {
   /* 0 or 1.  With 1 the value cache stores each page head-dim major: value_cache is
    * [NB, Hkv, D, S] e4m3 bytes, the S tokens of one head dim contiguous, with the key
    * cache's block and head strides (the key cache keeps [NB, Hkv, S, D]).  The first page's
-   * probe covers fp8 per-tensor caches "with trans_v and plain V" without defining the
-   * layout; this is the plain transposed reading.  fp8 with a per-tensor scale only
+   * probe runs fp8 per-tensor caches in a trans_v layout as well as with plain V, and does
+   * not define that layout; this is the plain transposed reading.  fp8 with a per-tensor scale only
    * (PA_ERR_UNSUPPORTED otherwise); the tcgen05 kernel does not take it. */
   int32_t trans_v;
   /* Attention sinks: fp32 [Hq], one logit per query head in the units of the

@@ -36,7 +36,7 @@
  *   M = max(max_t x_t, s_h); a row that sees no token gives zeros.
  *   With trans_v set, the value cache stores each page head-dim major: [NB, Hkv, D, S],
  *   the S tokens of one head dim contiguous (the first page's probe covers fp8
- *   per-tensor caches with "trans_v" and with plain V, without defining the layout; this
+ *   per-tensor caches in a trans_v layout as well as with plain V, without defining it; this
  *   is the plain transposed reading, and the layout of vLLM's classic value cache).
  *
  * Storage formats are decoded from their definitions:

@@ -256,7 +256,7 @@ def test_head_dim_64_fused_merge_of_128_partitions(kv):
 
 TRANS_V = [
     # fp8 per-tensor with the value cache stored [NB, Hkv, D, S] (the first page's
-    # "trans_v"): K rows read in the order that matches the transposed V fragments
+    # trans_v layout): K rows read in the order that matches the transposed V fragments
     synth.Case("tv_d128_g8", synth.KV_FP8, synth.SCALE_TENSOR, synth.Q_BF16, batch=6, qlen=1,
                num_kv_heads=2, num_q_heads=16, head_dim=128, page_size=16,
                context_lens=[1, 17, 255, 257, 1000, 5000], fill=synth.FILL_INF, seed=3101,
