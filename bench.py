@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +46,7 @@ METRIC = "pa_decode µs/call and achieved KV GB/s (fraction of GB300 HBM peak)"
 WORKLOAD = ("long-context decode: MXFP4 and fp8-per-token KV, batch 16, 1 KV head, GQA 16, "
             "head_dim 128, page 128, qlen 1, context_lens U[120000, 131072]")
 FALLBACK_HBM_GBS = 6800.0
+KERNEL = None  # decode kernel choice passed to every call (--kernel)
 
 
 def dist_env():
@@ -73,11 +75,11 @@ class Clocks:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="pa_bench_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                                           "-i", str(self.idx), "-lms", "200"], stdout=self.f,
@@ -116,6 +118,11 @@ class Clocks:
                         reasons.add(n)
         except OSError:
             return None
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
@@ -195,13 +202,13 @@ def per_config(device, peak, calls=10, warmup=3):
         out = torch.empty(tuple(p["query"].shape), dtype=torch.bfloat16, device=device)
         args = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"], p["context_lens"],
                              out, key_scale=p["key_scale"], value_scale=p["value_scale"],
-                             q_scale=p["q_scale"], softmax_scale=case.scale_qk())
+                             q_scale=p["q_scale"], softmax_scale=case.scale_qk(), kernel=KERNEL)
         ws = ops.alloc_workspace(args, device)
         # one partition per unit (the pages' plan-free mode): rows written directly, no reduce
         args1 = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"],
                               p["context_lens"], out, key_scale=p["key_scale"],
                               value_scale=p["value_scale"], q_scale=p["q_scale"],
-                              softmax_scale=case.scale_qk(), max_partitions=1)
+                              softmax_scale=case.scale_qk(), max_partitions=1, kernel=KERNEL)
         ws1 = ops.alloc_workspace(args1, device)
         for _ in range(warmup):
             ops.pa_decode_run(args, ws, stream)
@@ -295,7 +302,7 @@ def make_variant(kv, device, batch=None):
     out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=device)
     args = ops.make_args(q, p["key_cache"], p["value_cache"], p["block_tables"], p["context_lens"], out,
                          key_scale=p["key_scale"], value_scale=p["value_scale"], q_scale=p["q_scale"],
-                         softmax_scale=case.scale_qk())
+                         softmax_scale=case.scale_qk(), kernel=KERNEL)
     ws = ops.alloc_workspace(args, device)
     lens = p["context_lens"].cpu().tolist()
     return {"case": case, "p": p, "out": out, "args": args, "ws": ws,
@@ -399,7 +406,8 @@ def run_ours(a):
         out2 = torch.empty_like(v["out"])
         args2 = ops.make_args(q2, p["key_cache"], p["value_cache"], bt2, cl2, out2,
                               key_scale=p["key_scale"], value_scale=p["value_scale"],
-                              q_scale=p["q_scale"], softmax_scale=v["case"].scale_qk())
+                              q_scale=p["q_scale"], softmax_scale=v["case"].scale_qk(),
+                              kernel=KERNEL)
         two.append({"q": q2, "bt": bt2, "cl": cl2, "out": out2, "args": args2,
                     "ws": ops.alloc_workspace(args2, dev)})
         sets.append(two)
@@ -479,7 +487,7 @@ def run_ours(a):
                    "global_batch": 16 * ws_n, "seq_len": "120000-131072",
                    "parallelism": f"replicas x{ws_n}",
                    "l2": "no flush: each call streams more than the 129 MB L2",
-                   "mma": ("tcgen05.mma (TMEM accumulators)" if os.environ.get("PA_DECODE_KERNEL") == "tc"
+                   "mma": ("tcgen05.mma (TMEM accumulators)" if KERNEL == "tc"
                            else "mma.sync m16n8k16 f16 x f16 -> f32"),
                    "merge": "separate pa_decode_reduce launch"},
         "per_variant": per,
@@ -493,8 +501,8 @@ def run_ours(a):
     }
     if a.batch is not None or a.variant != "both":
         line["config"]["note"] = "profiling subset, not the benchmark workload"
-    if os.environ.get("PA_DECODE_KERNEL") == "tc":
-        line["config"]["kernel"] = "tcgen05 (PA_DECODE_KERNEL=tc)"
+    if KERNEL == "tc":
+        line["config"]["kernel"] = "tcgen05 (--kernel tc)"
     if not a.no_per_config and a.batch is None and a.variant == "both":
         line["per_config"] = per_config(dev, peak)
     if rank == 0:
@@ -606,8 +614,8 @@ def main():
         ops.load_library()
         print(json.dumps(kv_write_config("cuda", peaks()[0], a.steps)))
         return
-    if a.kernel is not None:
-        os.environ["PA_DECODE_KERNEL"] = a.kernel
+    global KERNEL
+    KERNEL = a.kernel
     if a.warmup < 3 and a.impl == "ours":
         a.warmup = 3
     if a.impl == "reference":

@@ -165,10 +165,22 @@ typedef struct pa_decode_args {
    * beside sliding window among what the MXFP4 path refuses, without defining them; this
    * is the plain reading.  Every format; the tcgen05 kernel does not take them. */
   const float* sinks;
+  /* Which decode kernel serves the call (PA_KERNEL_*): the library's choice (0), the
+   * mma.sync tile kernel, or the tcgen05 kernel where it covers the shape (head_dim 128, at
+   * most 32 query rows, pages of 8 tokens or more, separate reduce, no causal mask, window,
+   * sinks, transposed V or in-kernel query quantisation; other shapes run the tile kernel).
+   * Every choice computes the same function within the stated tolerances.  Other values:
+   * PA_ERR_INVALID_ARG. */
+  int32_t kernel;
 } pa_decode_args;
 
-/* ABI version of this header; a mismatched library refuses nothing but reports it here. */
-#define PA_DECODE_ABI_VERSION 5
+#define PA_KERNEL_DEFAULT 0
+#define PA_KERNEL_MMA 1
+#define PA_KERNEL_TCGEN05 2
+
+/* ABI version of this header; a mismatched library refuses nothing but reports it here.
+ * Version 6 appended `kernel`; earlier fields keep their offsets. */
+#define PA_DECODE_ABI_VERSION 6
 int32_t pa_decode_abi_version(void);
 
 /* Bytes of workspace the three calls need for these shapes (plan, partition scratch,
@@ -211,12 +223,11 @@ pa_status pa_decode(const pa_decode_args* args, void* workspace, size_t workspac
 pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
                            size_t workspace_bytes, void* stream);
 
-/* plan + decode + reduce in one call, on one stream.  With max_partitions == 1 every
- * (sequence, KV head) unit is one task whose rows the decode writes directly, and the
- * reduce launches nothing: the pages' plan-free mode ("[FlyDSL] pa_decode: MXFP4 K/V ...",
- * Summary: work_plan=None runs one task per sequence and writes the row directly, and a
- * plan with max_partitions == 1 is served the same way) with the plan still built, in a
- * few microseconds, by pa_decode_plan. */
+/* plan + decode + reduce in one call, on one stream.  With max_partitions == 1 each
+ * (sequence, KV head) unit is a single task, the decode stores its bf16 rows itself and
+ * the reduce has nothing to do; this is how the pages' plan-free mode is served here
+ * ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary), except that pa_decode_plan still builds
+ * the task list first. */
 pa_status pa_decode_run(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);
 
@@ -239,6 +250,13 @@ pa_status pa_decode_run_static(const pa_decode_args* args, void* stream);
 /* Enqueues a copy of the device status word (PA_DEVICE_*) into *host_status; the caller
  * synchronises the stream before reading it. host_status should be pinned memory. */
 pa_status pa_decode_read_status(const void* workspace, int32_t* host_status, void* stream);
+
+/* No counterpart in the source pages.  The device status word of the last
+ * pa_decode_run_static call on the current device (the word lives in the library-owned
+ * array, whose address callers never see): enqueues its copy into *host_status on
+ * `stream`, which must belong to the current device (PA_ERR_INVALID_ARG otherwise); the
+ * caller synchronises the stream before reading it.  Allocates nothing. */
+pa_status pa_decode_read_status_static(int32_t* host_status, void* stream);
 
 /* Static description of a status code. */
 const char* pa_status_string(pa_status status);

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_decode.so")
 SOURCES = ["pa_decode.cu", "pa_tile_bf16.cu", "pa_tile_fp8.cu", "pa_tile_mxfp4.cu",
-           "pa_tc_bf16.cu", "pa_tc_fp8.cu", "pa_tc_mxfp4.cu", "pa_decode_static.cu",
+           "pa_tc_bf16.cu", "pa_tc_fp8.cu", "pa_tc_mxfp4.cu", "pa_mx.cu", "pa_decode_static.cu",
            "pa_kv_write.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -37,7 +37,7 @@ def cuda_lib_dir() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "pa_decode.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
 
@@ -71,7 +71,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     tmp = LIB + f".tmp{os.getpid()}"
     libdir = cuda_lib_dir()
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + [
-        "-cudart", "shared", "-L", libdir, "-Xlinker", f"-rpath={libdir}", "-lcuda" if False else "-lcudart"]
+        "-cudart", "shared", "-L", libdir, "-Xlinker", f"-rpath={libdir}", "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa_configs.cuh"
@@ -232,6 +233,28 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   if (tid == 0) *pp.ntasks = carry_tasks;
   // chunks past the last task hold none
   for (int c = carry_chunk + 1 + tid; c <= pp.budget; c += blockDim.x) pp.chunk_first[c] = carry_tasks;
+  __syncthreads();
+  // Each chunk's first task: its query rows and first 64 block-table entries into L2 now,
+  // while the memory system is quiet (the decode kernel reads them before its first copies).
+  if (pp.q != nullptr) {
+    for (int c = tid; c < pp.budget; c += blockDim.x) {
+      const int t = pp.chunk_first[c];
+      if (t >= carry_tasks) continue;
+      const PlanTask tk = pp.tasks[t];
+      const int hkv = tk.hkv_part & 0xFFFF;
+      const char* bt = reinterpret_cast<const char*>(pp.bt + (int64_t)tk.seq * pp.bt_stride +
+                                                     (int64_t)tk.tile_begin * kTileTokens / pp.S);
+      prefetch_l2(bt);
+      prefetch_l2(bt + 128);
+      const int row_bytes = pp.D * pp.q_bytes;
+      for (int i = 0; i < pp.qlen; ++i)
+        for (int r = 0; r < pp.G; ++r) {
+          const char* q = reinterpret_cast<const char*>(pp.q) +
+                          (((int64_t)tk.seq * pp.qlen + i) * pp.q_st + (int64_t)(hkv * pp.G + r) * pp.q_sh) * pp.q_bytes;
+          for (int b = 0; b < row_bytes; b += 128) prefetch_l2(q + b);
+        }
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -435,6 +458,7 @@ pa_status validate(const pa_decode_args* a) {
   if (a->causal != 0 && a->causal != 1) return PA_ERR_INVALID_ARG;
   if (a->sliding_window < 0) return PA_ERR_INVALID_ARG;
   if (a->trans_v != 0 && a->trans_v != 1) return PA_ERR_INVALID_ARG;
+  if (a->kernel < PA_KERNEL_DEFAULT || a->kernel > PA_KERNEL_TCGEN05) return PA_ERR_INVALID_ARG;
   if (a->trans_v && !(a->kv_dtype == PA_KV_FP8_E4M3 && a->kv_scale == PA_SCALE_PER_TENSOR))
     return PA_ERR_UNSUPPORTED;
   const int G = a->num_q_heads / a->num_kv_heads;
@@ -493,15 +517,33 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The tensor-core (tcgen05) kernel covers head_dim 128, up to 32 query rows per KV head
 // and pages of at least 8 tokens, with the separate reduce, not causal, without a sliding
-// window or sinks, and with token-major V.  It runs when PA_DECODE_KERNEL=tc is set in the environment (read at
-// each call); otherwise every shape runs the mma.sync kernel, the faster of the two on
-// the long-context workloads.
+// window or sinks, and with token-major V.  It runs when the caller asks for it
+// (kernel = PA_KERNEL_TCGEN05) and covers the shape; otherwise the mma.sync tile kernel
+// runs, the faster of the two on the long-context workloads.
 bool tc_kernel_applies(const pa_decode_args* a, int rows) {
-  const char* e = getenv("PA_DECODE_KERNEL");
-  const bool want_tc = e != nullptr && strcmp(e, "tc") == 0;
-  return want_tc && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 && !a->merge_in_decode &&
-         !(a->causal && a->qlen > 1) && a->sliding_window == 0 && !a->trans_v && !a->sinks &&
-         a->q_dtype != PA_Q_BF16_TO_E4M3;
+  return a->kernel == PA_KERNEL_TCGEN05 && a->head_dim == 128 && rows <= 32 && a->page_size >= 8 &&
+         !a->merge_in_decode && !(a->causal && a->qlen > 1) && a->sliding_window == 0 &&
+         !a->trans_v && !a->sinks && a->q_dtype != PA_Q_BF16_TO_E4M3;
+}
+
+// The MXFP4 kernel with block-scaled tcgen05 QK serves MXFP4 caches by default: any page
+// size and sliding window, without the in-decode merge (that runs on the tile kernel).
+bool mx_kernel_applies(const pa_decode_args* a) {
+  return a->kv_dtype == PA_KV_MXFP4 && a->kernel == PA_KERNEL_DEFAULT && !a->merge_in_decode;
+}
+
+// Test hook, read once per process: when the environment holds PA_DECODE_TEST_DROP_SLICE=1
+// at the library's first decode call, that one call (and no later one) has the first warp
+// of every CTA leave its first ring slot unloaded, so that wait runs out and the status
+// word reports it; the next call shows that the context is still usable.
+bool drop_first_slice_hook() {
+  static std::once_flag once;
+  static std::atomic<bool> armed{false};
+  std::call_once(once, [] {
+    const char* d = getenv("PA_DECODE_TEST_DROP_SLICE");
+    armed.store(d != nullptr && strcmp(d, "1") == 0);
+  });
+  return armed.load(std::memory_order_relaxed) && armed.exchange(false);
 }
 
 pa_status make_layout(const pa_decode_args* a, WsLayout* L) {
@@ -586,6 +628,23 @@ pa_status cache_map(const pa_decode_args* a, const void* base, int sub, int box_
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
+// A cache as a 4-D byte tensor {row bytes, page slots, KV heads, blocks} with unswizzled
+// boxes of whole rows by `box_rows` slots (rows land back to back in shared memory).
+pa_status cache_map_rows(const pa_decode_args* a, const void* base, int box_rows, CUtensorMap* m) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)row_bytes(a), (cuuint64_t)a->page_size, (cuuint64_t)a->num_kv_heads,
+                        (cuuint64_t)a->num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)a->kv_stride_token, (cuuint64_t)a->kv_stride_head,
+                           (cuuint64_t)a->kv_stride_block};
+  cuuint32_t box[4] = {(cuuint32_t)row_bytes(a), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 // Tensor map of a transposed e4m3 value cache [NB, Hkv, D, S]: boxes of 16 tokens (16
 // bytes) by `dims` head dims, unswizzled (rows of 16 bytes are read conflict-free).
 pa_status cache_map_vt(const pa_decode_args* a, int dims, CUtensorMap* m) {
@@ -653,6 +712,14 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
   pp.task_chunk = reinterpret_cast<int*>(w + L.task_chunk);
   pp.chunk_first = reinterpret_cast<int*>(w + L.chunk_first);
+  pp.q = a->query;
+  pp.q_st = a->q_stride_token;
+  pp.q_sh = a->q_stride_head;
+  pp.q_bytes = a->q_dtype == PA_Q_FP8_E4M3 ? 1 : 2;
+  pp.G = a->num_q_heads / a->num_kv_heads;
+  pp.D = a->head_dim;
+  pp.bt = a->block_tables;
+  pp.bt_stride = a->bt_stride;
   int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
   cudaLaunchConfig_t cfg = {};
@@ -678,8 +745,12 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   const int R = G * a->qlen;
   const int kind = a->kv_dtype == PA_KV_BF16 ? pa::KIND_BF16 : (a->kv_dtype == PA_KV_FP8_E4M3 ? pa::KIND_FP8 : pa::KIND_FP4);
   const bool use_tc = tc_kernel_applies(a, R);
+  const bool use_mx = !use_tc && mx_kernel_applies(a);
   int tc = 0, sub = 0, dims = a->head_dim;
-  if (use_tc) {
+  if (use_mx) {
+    tc = 128;
+    sub = 64;
+  } else if (use_tc) {
     tc = 128;
     sub = kind == pa::KIND_FP4 ? 64 : 128;
   } else {
@@ -688,7 +759,11 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   // transposed V is loaded in 16-token pieces, and K in boxes of the same height
   const int box = a->trans_v ? 16 : (a->page_size < tc ? a->page_size : tc);
   CUtensorMap tk, tv;
-  if ((st = cache_map(a, a->key_cache, sub, box, &tk)) != PA_OK) return st;
+  if (use_mx)
+    st = cache_map_rows(a, a->key_cache, box, &tk);
+  else
+    st = cache_map(a, a->key_cache, sub, box, &tk);
+  if (st != PA_OK) return st;
   if (a->trans_v)
     st = cache_map_vt(a, dims, &tv);
   else
@@ -716,10 +791,7 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.scale_log2 = sc * 1.4426950408889634f;
   p.q_fp8 = a->q_dtype == PA_Q_FP8_E4M3;
   p.q_quant = a->q_dtype == PA_Q_BF16_TO_E4M3;
-  {  // test hook (environment, read at each call): make one pipeline wait run out
-    const char* d = getenv("PA_DECODE_TEST_DROP_SLICE");
-    p.drop_first_slice = d != nullptr && strcmp(d, "1") == 0;
-  }
+  p.drop_first_slice = drop_first_slice_hook();
   p.q_scale_per_row = a->q_scale_per_row != 0;
   p.scale_kind = a->kv_scale;
   p.q = a->query;
@@ -746,7 +818,9 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
   const int grid = L.budget;
   int rc;
-  if (use_tc) {
+  if (use_mx) {
+    rc = pa::launch_mx_mxfp4(p, tk, tv, grid, stream);
+  } else if (use_tc) {
     if (kind == pa::KIND_BF16)
       rc = pa::launch_tc_bf16(p, tk, tv, L.budget, stream);
     else if (kind == pa::KIND_FP8)

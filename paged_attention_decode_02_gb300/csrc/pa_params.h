@@ -81,6 +81,15 @@ struct PlanParams {
   int max_partitions;
   int budget;
   const int32_t* ctx;
+  // for the L2 prefetch of each chunk's first task (its query rows and first block-table
+  // entries), so that the decode kernel's first dependent loads do not wait behind the copies
+  // that every other CTA starts at once
+  const void* q;
+  int64_t q_st, q_sh;  // elements
+  int q_bytes;         // bytes per query element
+  int G, D;
+  const int32_t* bt;
+  int64_t bt_stride;
   int* status;
   int* ntasks;
   int* nparts;
@@ -118,6 +127,12 @@ int launch_tc_bf16(const DecodeParams& p, const CUtensorMap& tk, const CUtensorM
 int launch_tc_fp8(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                   int grid, void* stream);
 int launch_tc_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                    int grid, void* stream);
+
+// MXFP4 kernel with block-scaled tcgen05 QK and mma.sync PV (head_dim 128, up to 16 query
+// rows); `tk` maps the key cache as unswizzled 64-byte rows, `tv` the value cache as
+// 64-byte-swizzled rows, both in boxes of min(page size, 128) tokens.
+int launch_mx_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                     int grid, void* stream);
 
 // Tokens per warp slice, swizzle span (bytes) and head dims per warp of the tile kernel

@@ -286,3 +286,52 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 }  // namespace pa
+
+namespace pa {
+
+// ---- tcgen05: block-scaled MMA, scale-factor copies, TMEM loads in fragment order ----------
+// D[tmem] (+)= (A * 2^(sfa - 127)) (B * 2^(sfb - 127))^T per 32-element k block: A and B from
+// shared memory (descriptors), e8m0 scale factors of A and B in tensor memory; the k block's
+// byte of each 32-bit scale cell is selected by the instruction descriptor.
+__device__ __forceinline__ void umma_mxf8f6f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+               "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+               : "memory");
+}
+// Instruction descriptor of a block-scaled MMA with e8m0 scales: operand formats (e4m3 0,
+// e2m1 5), both K-major, N, M, and the byte of the A / B scale cells this MMA reads.
+__host__ __device__ constexpr uint32_t umma_idesc_mx(uint32_t afmt, uint32_t bfmt, uint32_t n, uint32_t m,
+                                                     uint32_t sfa_byte, uint32_t sfb_byte) {
+  return (sfb_byte << 4) | (afmt << 7) | (bfmt << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) |
+         (sfa_byte << 29);
+}
+// Shared-memory descriptor of an unswizzled K-major matrix of 16-byte rows (8-row core
+// matrices `sbo` bytes apart).
+__device__ __forceinline__ uint64_t umma_desc_noswz(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(16 >> 4) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
+// Copies a 32-row x 16-byte shared-memory matrix into lanes 0..31 of every TMEM lane
+// quarter, four 32-bit columns from `taddr`.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// 16 TMEM lanes x 8 columns, mma-accumulator order: thread i holds (lane i/4, columns 2(i%4),
+// 2(i%4)+1) and (lane 8 + i/4, the same columns).
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+// Transpose of an 8x8 b16 matrix held in mma fragment order (thread i: row i/4, columns 2(i%4),
+// 2(i%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+}  // namespace pa

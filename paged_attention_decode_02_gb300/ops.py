@@ -23,11 +23,14 @@ PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_MXFP4 = 0, 1, 2
 PA_SCALE_NONE, PA_SCALE_PER_TENSOR, PA_SCALE_PER_TOKEN, PA_SCALE_E8M0_32 = 0, 1, 2, 3
 PA_Q_BF16, PA_Q_FP8_E4M3, PA_Q_BF16_TO_E4M3 = 0, 1, 2
 PA_DEVICE_WAIT_TIMEOUT, PA_DEVICE_CONTEXT_CLAMPED = 1, 2
+PA_KERNEL_DEFAULT, PA_KERNEL_MMA, PA_KERNEL_TCGEN05 = 0, 1, 2
+_KERNELS = {None: PA_KERNEL_DEFAULT, "default": PA_KERNEL_DEFAULT, "mma": PA_KERNEL_MMA,
+            "tc": PA_KERNEL_TCGEN05, "tcgen05": PA_KERNEL_TCGEN05}
 
 EXPORTED = ["pa_decode_abi_version", "pa_decode_workspace_size", "pa_decode_validate",
             "pa_decode_plan", "pa_decode", "pa_decode_reduce", "pa_decode_run",
             "pa_decode_read_status", "pa_status_string", "pa_decode_run_static",
-            "pa_mxfp4_kv_write"]
+            "pa_decode_read_status_static", "pa_mxfp4_kv_write"]
 STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -53,7 +56,7 @@ class PaDecodeArgs(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
         ("out_stride_head", ctypes.c_int64), ("causal", ctypes.c_int32),
         ("sliding_window", ctypes.c_int32), ("trans_v", ctypes.c_int32),
-        ("sinks", ctypes.c_void_p),
+        ("sinks", ctypes.c_void_p), ("kernel", ctypes.c_int32),
     ]
 
 
@@ -92,6 +95,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         L.pa_decode_run_static.restype = ctypes.c_int32
         L.pa_decode_read_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.pa_decode_read_status.restype = ctypes.c_int32
+        L.pa_decode_read_status_static.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        L.pa_decode_read_status_static.restype = ctypes.c_int32
         L.pa_status_string.argtypes = [ctypes.c_int32]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_mxfp4_kv_write.argtypes = [ctypes.POINTER(Mxfp4WriteArgs), ctypes.c_void_p]
@@ -119,6 +124,28 @@ def _stream_handle(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def call_device(tensors, stream=None) -> torch.device:
+    """The one CUDA device a call's tensors live on; raises ValueError when they are spread
+    over several devices, are not CUDA tensors, or when ``stream`` (a torch stream) belongs to
+    another device.  The library launches on the current device and stream, so callers make
+    this device current for the call."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError(f"every tensor must be on one CUDA device, got {devs}")
+    dev = next(iter(devs))
+    sdev = getattr(stream, "device", None)
+    if sdev is not None and torch.device(sdev) != dev:
+        raise ValueError(f"stream is on {sdev}, the tensors on {dev}")
+    return dev
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtypes, *, contiguous_last=True):
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+    if contiguous_last and t.dim() > 0 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last axis must be contiguous (stride 1)")
+
+
 def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
               block_tables: torch.Tensor, context_lens: torch.Tensor, out: torch.Tensor, *,
               key_scale: Optional[torch.Tensor] = None, value_scale: Optional[torch.Tensor] = None,
@@ -126,7 +153,8 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
               max_partitions: int = 0, task_budget: int = 0,
               merge_in_decode: bool = False, causal: bool = False,
               q_quant: bool = False, sliding_window: int = 0,
-              trans_v: bool = False, sinks: Optional[torch.Tensor] = None) -> PaDecodeArgs:
+              trans_v: bool = False, sinks: Optional[torch.Tensor] = None,
+              kernel=None) -> PaDecodeArgs:
     """Describe one decode call.
 
     query / out: [B, qlen, Hq, D] (or [B*qlen, Hq, D]); query bf16 or e4m3
@@ -139,7 +167,36 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     position i sees only tokens > L - qlen + i - W.  trans_v: value_cache is [NB, Hkv, D, S]
     (e4m3 bytes, per-tensor scale), with the key cache's block and head strides.
     sinks: fp32 [Hq], one softmax logit per query head with a zero value, or None.
+    kernel: None / "default" (the library's choice), "mma" (the mma.sync tile kernel) or
+    "tc" (the tcgen05 kernel where it covers the shape).
+    Malformed tensors (wrong dtype, shape, batch or layout) raise ValueError here, before
+    any pointer reaches the library.
     """
+    _check_tensor(query, "query", (torch.bfloat16, torch.float8_e4m3fn, torch.uint8))
+    _check_tensor(out, "out", (torch.bfloat16,))
+    if tuple(out.shape) != tuple(query.shape):
+        raise ValueError(f"out {tuple(out.shape)} must have the query's shape {tuple(query.shape)}")
+    if query.dim() not in (3, 4):
+        raise ValueError("query: [B, qlen, Hq, D] or [B*qlen, Hq, D]")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name}: contiguous int32 expected, got {t.dtype}")
+    if block_tables.dim() != 2 or context_lens.dim() != 1:
+        raise ValueError("block_tables [B, W] and context_lens [B]")
+    B_ = block_tables.shape[0]
+    if context_lens.shape[0] != B_:
+        raise ValueError(f"context_lens has {context_lens.shape[0]} entries for {B_} sequences")
+    if query.dim() == 4 and query.shape[0] != B_:
+        raise ValueError(f"query batch {query.shape[0]} != block_tables batch {B_}")
+    if query.dim() == 3 and (B_ == 0 or query.shape[0] % B_):
+        raise ValueError("query rows must be batch x qlen")
+    if key_cache.dtype != value_cache.dtype:
+        raise ValueError(f"key cache {key_cache.dtype} and value cache {value_cache.dtype} differ")
+    _check_tensor(key_cache, "key_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    if key_cache.dim() != 4 or value_cache.dim() != 4:
+        raise ValueError("caches: 4-D [NB, Hkv, S, row]")
+    if kernel not in _KERNELS:
+        raise ValueError(f"kernel: one of {sorted(k for k in _KERNELS if k)} or None")
     D = query.shape[-1]
     Hq = query.shape[-2]
     if query.dim() == 4:
@@ -163,15 +220,34 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
         a.kv_dtype = PA_KV_FP8_E4M3
         if key_scale is None or value_scale is None:
             raise ValueError("fp8 KV needs key_scale and value_scale")
+        for t, name in ((key_scale, "key_scale"), (value_scale, "value_scale")):
+            if t.dtype != torch.float32:
+                raise ValueError(f"{name}: fp32 expected for an e4m3 cache, got {t.dtype}")
+        if key_scale.numel() != value_scale.numel():
+            raise ValueError("key_scale and value_scale must have the same shape")
         a.kv_scale = PA_SCALE_PER_TENSOR if key_scale.numel() == 1 else PA_SCALE_PER_TOKEN
+        if a.kv_scale == PA_SCALE_PER_TOKEN and (tuple(key_scale.shape) != (NB, Hkv, S)
+                                                 or key_scale.stride(-1) != 1):
+            raise ValueError(f"per-token scales: fp32 [NB, Hkv, S] = {(NB, Hkv, S)}, token axis dense")
     elif key_cache.shape[-1] * 2 == D:
         a.kv_dtype, a.kv_scale = PA_KV_MXFP4, PA_SCALE_E8M0_32
+        if key_scale is None or value_scale is None:
+            raise ValueError("MXFP4 KV needs e8m0 key_scale and value_scale")
+        for t, name in ((key_scale, "key_scale"), (value_scale, "value_scale")):
+            if t.dtype != torch.uint8 or tuple(t.shape) != (NB, Hkv, S, D // 32) \
+                    or t.stride(-1) != 1 or t.stride(-2) != D // 32:
+                raise ValueError(f"{name}: uint8 e8m0 [NB, Hkv, S, D/32] = {(NB, Hkv, S, D // 32)}, "
+                                 "token rows dense")
     else:
         raise ValueError(f"cannot infer the KV format from {tuple(key_cache.shape)} and D={D}")
     if query.dtype == torch.bfloat16:
         a.q_dtype = PA_Q_BF16_TO_E4M3 if q_quant else PA_Q_BF16
     else:
         a.q_dtype = PA_Q_FP8_E4M3
+        if q_scale is None or q_scale.dtype != torch.float32:
+            raise ValueError("an e4m3 query needs an fp32 q_scale ([1] or [B, qlen, Hq])")
+    if a.kv_dtype == PA_KV_BF16 and (key_scale is not None or value_scale is not None):
+        raise ValueError("bf16 KV takes no scales")
     a.q_scale_per_row = int(q_scale is not None and q_scale.numel() > 1)
     a.softmax_scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)
     a.max_partitions, a.task_budget = int(max_partitions), int(task_budget)
@@ -182,6 +258,7 @@ def make_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.T
     if sinks is not None and (sinks.dtype != torch.float32 or sinks.numel() != Hq):
         raise ValueError("sinks: fp32, one per query head")
     a.sinks = _ptr(sinks)
+    a.kernel = _KERNELS[kernel]
     a.query, a.q_stride_token, a.q_stride_head = _ptr(query), q_st, q_sh
     a.q_scale = _ptr(q_scale)
     es = key_cache.element_size()
@@ -269,6 +346,16 @@ def pa_decode_run_static(args: PaDecodeArgs, stream=None):
     _check(status, "pa_decode_run_static")
 
 
+def pa_decode_read_status_static(stream=None) -> int:
+    """Device status word of the last pa_decode_run_static call on the current device;
+    synchronises the stream."""
+    host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    _check(load_library().pa_decode_read_status_static(host.data_ptr(), _stream_handle(stream)),
+           "pa_decode_read_status_static")
+    (stream or torch.cuda.current_stream()).synchronize()
+    return int(host.item())
+
+
 def pa_decode_read_status(workspace: torch.Tensor, stream=None) -> int:
     """Device status word (PA_DEVICE_* bits); synchronises the stream."""
     host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
@@ -288,35 +375,38 @@ def paged_attention_decode(query: torch.Tensor, key_cache: torch.Tensor,
                            softmax_scale: Optional[float] = None, max_partitions: int = 0,
                            causal: bool = False, sliding_window: int = 0, trans_v: bool = False,
                            sinks: Optional[torch.Tensor] = None, q_quant: bool = False,
-                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """One decode call on tensors: plan + decode + reduce on ``stream`` (default: the current
-    stream), returning ``out`` (bf16, the query's shape; allocated when not given).  The
-    arguments are those of make_args; ``workspace`` (from alloc_workspace) is allocated per
-    call when not given.  Every tensor must be on one CUDA device; a refused call raises
-    PaDecodeError.  Nothing here computes: the library does the work."""
-    tensors = [t for t in (query, key_cache, value_cache, block_tables, context_lens, out,
-                           key_scale, value_scale, q_scale, sinks, workspace) if t is not None]
-    devs = {t.device for t in tensors}
-    if len(devs) != 1 or next(iter(devs)).type != "cuda":
-        raise ValueError(f"paged_attention_decode: every tensor must be on one CUDA device, got {devs}")
-    if query.dtype == torch.uint8:
-        query = query.view(torch.float8_e4m3fn)
-    if out is None:
-        out = torch.empty(query.shape, dtype=torch.bfloat16, device=query.device)
-    args = make_args(query, key_cache, value_cache, block_tables, context_lens, out,
-                     key_scale=key_scale, value_scale=value_scale, q_scale=q_scale,
-                     softmax_scale=softmax_scale, max_partitions=max_partitions, causal=causal,
-                     q_quant=q_quant, sliding_window=sliding_window, trans_v=trans_v,
-                     sinks=sinks)
-    if workspace is None:
-        workspace = alloc_workspace(args, query.device)
-    pa_decode_run(args, workspace, stream)
+                           kernel=None, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """One decode call on tensors: plan + decode + reduce on ``stream`` (default: the
+    current stream of the tensors' device), returning ``out`` (bf16, the query's shape;
+    allocated when not given).  The arguments are those of make_args; ``workspace`` (from
+    alloc_workspace) is allocated per call when not given.  Every tensor must be on one
+    CUDA device, which is made current for the call, and an explicit stream must belong
+    to it (ValueError otherwise); a refused call raises PaDecodeError.  Nothing here
+    computes: the library does the work."""
+    dev = call_device([query, key_cache, value_cache, block_tables, context_lens, out,
+                       key_scale, value_scale, q_scale, sinks, workspace], stream)
+    with torch.cuda.device(dev):
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        if query.dtype == torch.uint8:
+            query = query.view(torch.float8_e4m3fn)
+        if out is None:
+            out = torch.empty(query.shape, dtype=torch.bfloat16, device=dev)
+        args = make_args(query, key_cache, value_cache, block_tables, context_lens, out,
+                         key_scale=key_scale, value_scale=value_scale, q_scale=q_scale,
+                         softmax_scale=softmax_scale, max_partitions=max_partitions,
+                         causal=causal, q_quant=q_quant, sliding_window=sliding_window,
+                         trans_v=trans_v, sinks=sinks, kernel=kernel)
+        if workspace is None:
+            workspace = alloc_workspace(args, dev)
+        pa_decode_run(args, workspace, stream)
     return out
 
 
 def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions: int = 0,
            task_budget: int = 0, workspace: Optional[torch.Tensor] = None,
-           merge_in_decode: bool = False):
+           merge_in_decode: bool = False, kernel=None):
     """plan + decode + reduce on a synthetic-workload dict (device tensors)."""
     case = problem["case"]
     q = problem["query"]
@@ -331,7 +421,8 @@ def decode(problem: dict, out: Optional[torch.Tensor] = None, *, max_partitions:
                      task_budget=task_budget, merge_in_decode=merge_in_decode,
                      causal=getattr(case, "causal", False), q_quant=getattr(case, "q_quant", False),
                      sliding_window=getattr(case, "window", 0),
-                     trans_v=getattr(case, "trans_v", False), sinks=problem.get("sinks"))
+                     trans_v=getattr(case, "trans_v", False), sinks=problem.get("sinks"),
+                     kernel=kernel)
     if workspace is None:
         workspace = alloc_workspace(args, q.device)
     pa_decode_run(args, workspace)

@@ -31,13 +31,15 @@ def test_header_declarations_are_exported(lib):
     assert set(ops.EXPORTED) == set(names), names
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.pa_decode_abi_version() == 5
+    assert lib.pa_decode_abi_version() == 6
 
 
 def test_args_struct_layout_matches_header():
     # 16 int32/float fields, then 19 pointers and int64s, then the causal flag and the
-    # sliding window, then trans_v (padded), then the sinks pointer
-    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 22 * 8
+    # sliding window, then trans_v (padded), then the sinks pointer, then the kernel choice
+    # (padded)
+    assert ctypes.sizeof(ops.PaDecodeArgs) == 64 + 23 * 8
+    assert ops.PaDecodeArgs.kernel.offset == 64 + 22 * 8
     assert ops.PaDecodeArgs.query.offset == 64
     assert ops.PaDecodeArgs.causal.offset == 64 + 19 * 8
     assert ops.PaDecodeArgs.sliding_window.offset == 64 + 19 * 8 + 4
@@ -93,6 +95,8 @@ REFUSED = [
     ("merge flag not 0/1", dict(merge_in_decode=2), ops.PA_ERR_INVALID_ARG),
     ("negative sliding window", dict(sliding_window=-1), ops.PA_ERR_INVALID_ARG),
     ("trans_v not 0/1", dict(trans_v=2), ops.PA_ERR_INVALID_ARG),
+    ("unknown kernel choice", dict(kernel=3), ops.PA_ERR_INVALID_ARG),
+    ("negative kernel choice", dict(kernel=-1), ops.PA_ERR_INVALID_ARG),
     ("trans_v with per-token scales", dict(trans_v=1), ops.PA_ERR_UNSUPPORTED),
     ("trans_v with bf16", dict(trans_v=1, kv_dtype=ops.PA_KV_BF16, kv_scale=ops.PA_SCALE_NONE,
                                kv_stride_token=256, kv_stride_head=256 * 128,
@@ -234,3 +238,84 @@ def test_make_args_fills_the_variant_fields():
     with pytest.raises(ValueError):
         ops.make_args(q, kc, kc, bt, ctx, out, key_scale=sc, value_scale=sc,
                       sinks=torch.zeros(Hq, dtype=torch.float64))
+
+
+def _host_call(**over):
+    """Host tensors of a small fp8 per-token call (make_args reads shapes and strides only)."""
+    import torch
+    B, qlen, Hq, Hkv, D, S, NB = 2, 1, 16, 1, 128, 16, 6
+    t = dict(query=torch.zeros(B, qlen, Hq, D, dtype=torch.bfloat16),
+             key_cache=torch.zeros(NB, Hkv, S, D, dtype=torch.uint8),
+             value_cache=torch.zeros(NB, Hkv, S, D, dtype=torch.uint8),
+             block_tables=torch.zeros(B, 4, dtype=torch.int32),
+             context_lens=torch.ones(B, dtype=torch.int32),
+             out=torch.empty(B, qlen, Hq, D, dtype=torch.bfloat16),
+             key_scale=torch.ones(NB, Hkv, S, dtype=torch.float32),
+             value_scale=torch.ones(NB, Hkv, S, dtype=torch.float32))
+    t.update(over)
+    return t
+
+
+def _make(t, **kw):
+    return ops.make_args(t["query"], t["key_cache"], t["value_cache"], t["block_tables"],
+                         t["context_lens"], t["out"], key_scale=t["key_scale"],
+                         value_scale=t["value_scale"], **kw)
+
+
+def _bad_calls():
+    import torch
+    B, Hq, D, S, NB = 2, 16, 128, 16, 6
+    return [
+        ("out smaller than query", dict(out=torch.empty(B, 1, Hq, D // 2, dtype=torch.bfloat16))),
+        ("out not bf16", dict(out=torch.empty(B, 1, Hq, D, dtype=torch.float32))),
+        ("strided query head dim", dict(query=torch.zeros(B, 1, Hq, 2 * D, dtype=torch.bfloat16)[..., ::2])),
+        ("strided out head dim", dict(out=torch.empty(B, 1, Hq, 2 * D, dtype=torch.bfloat16)[..., ::2])),
+        ("int64 context lengths", dict(context_lens=torch.ones(B, dtype=torch.int64))),
+        ("int64 block tables", dict(block_tables=torch.zeros(B, 4, dtype=torch.int64))),
+        ("non-contiguous block tables", dict(block_tables=torch.zeros(4, B, dtype=torch.int32).t())),
+        ("context lengths of another batch", dict(context_lens=torch.ones(B + 1, dtype=torch.int32))),
+        ("block tables of another batch", dict(block_tables=torch.zeros(B + 1, 4, dtype=torch.int32))),
+        ("key and value caches of different types",
+         dict(value_cache=torch.zeros(NB, 1, S, D // 2, dtype=torch.bfloat16))),
+        ("fp64 per-token scales", dict(key_scale=torch.ones(NB, 1, S, dtype=torch.float64),
+                                        value_scale=torch.ones(NB, 1, S, dtype=torch.float64))),
+        ("per-token scales of the wrong shape", dict(key_scale=torch.ones(NB, 1, S + 1),
+                                                     value_scale=torch.ones(NB, 1, S + 1))),
+        ("mxfp4 scales not uint8", dict(key_cache=torch.zeros(NB, 1, 128, D // 2, dtype=torch.uint8),
+                                         value_cache=torch.zeros(NB, 1, 128, D // 2, dtype=torch.uint8),
+                                         key_scale=torch.ones(NB, 1, 128, 4),
+                                         value_scale=torch.ones(NB, 1, 128, 4))),
+    ]
+
+
+@pytest.mark.parametrize("what,over", _bad_calls(), ids=[c[0] for c in _bad_calls()])
+def test_make_args_refuses_malformed_tensors(what, over):
+    # each of these, passed on, would read or write out of bounds or read the wrong bytes
+    with pytest.raises(ValueError):
+        _make(_host_call(**over))
+
+
+def test_make_args_kernel_choice():
+    t = _host_call()
+    assert _make(t).kernel == ops.PA_KERNEL_DEFAULT
+    assert _make(t, kernel="mma").kernel == ops.PA_KERNEL_MMA
+    assert _make(t, kernel="tc").kernel == ops.PA_KERNEL_TCGEN05
+    with pytest.raises(ValueError):
+        _make(t, kernel="triton")
+
+
+def test_call_device_guard():
+    # the one-call wrapper makes the tensors' device current; tensors spread over two devices,
+    # or an explicit stream of another device, are refused before any launch (fakes carrying a
+    # .device stand in for CUDA tensors and streams on this host)
+    import types
+
+    import torch
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    a, b = types.SimpleNamespace(device=d0), types.SimpleNamespace(device=d1)
+    assert ops.call_device([a, None, a]) == d0
+    assert ops.call_device([a], types.SimpleNamespace(device=d0)) == d0
+    with pytest.raises(ValueError, match="one CUDA device"):
+        ops.call_device([a, b])
+    with pytest.raises(ValueError, match="stream is on"):
+        ops.call_device([a, a], types.SimpleNamespace(device=d1))

@@ -65,16 +65,18 @@ RAMP = [
 ]
 
 
+KERNELS = [None, "mma", "tc"]  # the library's choice, the mma.sync tile kernel, tcgen05 (f16 / f8f6f4)
+
+
 @pytest.mark.parametrize("case", RAMP, ids=lambda c: f"{c.name}-ramp")
 @pytest.mark.parametrize("mode", ["split", "direct"])
-@pytest.mark.parametrize("kernel", ["mma", "tc"])
-def test_rising_magnitudes_match_oracle(case, mode, kernel, monkeypatch):
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: k or "default")
+def test_rising_magnitudes_match_oracle(case, mode, kernel):
     # scores and V scales keep growing along each sequence: the running max and the V
     # references rise again and again, and every rise rescales the accumulated output
-    monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
     p = synth.make(case)
     ref = util.oracle_decode(p)
-    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16, kernel=kernel)
     util.assert_parity(got, ref, case.kv, f"{case.name} {kernel}")
 
 
@@ -87,12 +89,12 @@ TC_CASES = [c for c in SMALL if c.head_dim == 128] + [
 
 @pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"{c.name}-q{c.qlen}-s{c.seed}")
 @pytest.mark.parametrize("mode", ["split", "direct"])
-def test_tensor_core_kernel_matches_oracle(case, mode, monkeypatch):
-    # the tcgen05 kernel (PA_DECODE_KERNEL=tc) on every head_dim-128 shape: bf16, fp8 per
-    # tensor and per token, MXFP4; 8 to 32 query rows per KV head; pages of 16 to 128
-    monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+def test_tensor_core_kernel_matches_oracle(case, mode):
+    # the tcgen05 kernel (kernel="tc") on every head_dim-128 shape: bf16, fp8 per tensor
+    # and per token, MXFP4; 8 to 32 query rows per KV head; pages of 16 to 128
     p = synth.make(case)
-    util.assert_parity(run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=64),
+    util.assert_parity(run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=64,
+                               kernel="tc"),
                        util.oracle_decode(p), case.kv, case.name + " tcgen05")
 
 
@@ -105,13 +107,12 @@ HUGE_K = [
 
 @pytest.mark.parametrize("case", HUGE_K, ids=lambda c: f"{c.name}-b{c.batch}")
 @pytest.mark.parametrize("mode", ["split", "direct"])
-@pytest.mark.parametrize("kernel", ["mma", "tc"])
-def test_mxfp4_huge_k_exponents(case, mode, kernel, monkeypatch):
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: k or "default")
+def test_mxfp4_huge_k_exponents(case, mode, kernel):
     # K block exponents up to byte 249 (P2: logits went to inf there): scores near 2^122
     # must stay finite, and the one-hot softmax must pick the oracle's token
-    monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
     p = synth.make(case)
-    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16)
+    got = run_gpu(p, max_partitions=1 if mode == "direct" else 0, task_budget=16, kernel=kernel)
     assert np.all(np.isfinite(got))
     util.assert_parity(got, util.oracle_decode(p), case.kv, f"{case.name} huge K {kernel}")
 
@@ -139,11 +140,11 @@ def test_causal_matches_oracle(case, mode):
     util.assert_parity(got, util.oracle_decode(p), case.kv, case.name)
 
 
-def test_causal_runs_on_the_mma_kernel_when_tcgen05_is_requested(monkeypatch):
-    monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+def test_causal_runs_on_the_mma_kernel_when_tcgen05_is_requested():
     case = CAUSAL[0]
     p = synth.make(case)
-    util.assert_parity(run_gpu(p, task_budget=24), util.oracle_decode(p), case.kv, case.name)
+    util.assert_parity(run_gpu(p, task_budget=24, kernel="tc"), util.oracle_decode(p), case.kv,
+                       case.name)
 
 
 WINDOW = [

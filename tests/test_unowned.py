@@ -58,13 +58,14 @@ def _cases():
 
 @pytest.mark.parametrize("case", _cases(), ids=lambda c: c.name)
 @pytest.mark.parametrize("mode", ["split", "direct", "fused", "split-tc", "direct-tc"])
-def test_unowned_fill_is_bit_identical(case, mode, monkeypatch):
+def test_unowned_fill_is_bit_identical(case, mode):
     # "-tc": the tcgen05 kernel (head_dim 128 shapes; others fall back to mma.sync)
+    kernel = None
     if mode.endswith("-tc"):
-        monkeypatch.setenv("PA_DECODE_KERNEL", "tc")
+        kernel = "tc"
         mode = mode[:-3]
     kw = dict(max_partitions=1 if mode == "direct" else 0, task_budget=16,
-              merge_in_decode=mode == "fused")
+              merge_in_decode=mode == "fused", kernel=kernel)
     p = synth.make(case)
     base = gpu_bits(synth.refill(p, synth.FILL_ZERO), **kw)
     assert np.isfinite(_f32(base)).all()

@@ -1,8 +1,12 @@
 """pa_decode_run_static: the entry point for callers that cannot allocate device memory
 (code inside another runtime's memory budget, or loops where an allocation may
-synchronise the device).  It must give the same output as pa_decode_run with a
-caller-allocated workspace, call after call, and refuse problems whose workspace would
-exceed its fixed maximum.  Kept in a file of its own that pytest collects last."""
+synchronise the device).  With the same arguments it runs the same plan and the same
+kernels as pa_decode_run with a caller-allocated workspace, so the two outputs must agree
+bit for bit, call after call; the output must also match the oracle, the status word of
+the fixed array must read back as 0 after each call, and problems whose workspace would
+exceed the fixed maximum must be refused.  Kept in a file of its own that pytest collects
+last."""
+import numpy as np
 import pytest
 import torch
 
@@ -38,21 +42,26 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
 def test_static_workspace_matches_allocated_workspace(case):
-    p = synth.to_device(synth.make(case), "cuda")
+    host = synth.make(case)
+    ref = util.oracle_decode(host)
+    p = synth.to_device(host, "cuda")
     shape = tuple(p["query"].shape)
-    ref_out = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    args = _args(p, ref_out, task_budget=48)
+    alloc_out = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    args = _args(p, alloc_out, task_budget=48)
     ws = ops.alloc_workspace(args)
     ops.pa_decode_run(args, ws)
     torch.cuda.synchronize()
-    ref = ref_out.float().cpu().numpy()
+    assert ops.pa_decode_read_status(ws) == 0
+    alloc_bits = alloc_out.view(torch.int16).cpu().numpy()
     for _ in range(2):  # two calls in a row share the fixed array
         out = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
         sargs = _args(p, out, task_budget=48)
         ops.pa_decode_run_static(sargs)
         torch.cuda.synchronize()
-        got = out.float().cpu().numpy()
-        util.assert_parity(got, ref, case.kv, "static vs allocated workspace")
+        assert ops.pa_decode_read_status_static() == 0
+        assert np.array_equal(out.view(torch.int16).cpu().numpy(), alloc_bits), \
+            "static vs allocated workspace: same plan, same kernels, different bits"
+        util.assert_parity(out.float().cpu().numpy(), ref, case.kv, "static workspace vs oracle")
 
 
 def test_static_workspace_refuses_oversized_problem():
@@ -63,3 +72,12 @@ def test_static_workspace_refuses_oversized_problem():
     with pytest.raises(ops.PaDecodeError) as e:
         ops.pa_decode_run_static(args)
     assert e.value.status == ops.PA_ERR_WORKSPACE
+
+
+def test_static_status_reports_a_wait_that_ran_out():
+    # a child process whose first decode call leaves one ring slot per CTA unloaded: the
+    # timeout must be readable through the static status word, and the next static call on
+    # the same context must be correct with a clean status
+    from tests.test_wait_timeout import run_child
+    res = run_child("static")
+    assert res["status"] == [ops.PA_DEVICE_WAIT_TIMEOUT, 0], res
