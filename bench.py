@@ -19,8 +19,12 @@ per_config = every workload of the method, timed one call at a time through the 
          (plan + tile + reduce, device buffers) with the 129 MB L2 flushed before each
          call: µs/call, GB/s of algorithmic bytes and the fraction of the HBM peak; also
          the same call replayed from a CUDA graph, tile + reduce on a plan built
-         beforehand (us_per_call_planned), and the whole call with one partition per
-         unit, rows written directly and no reduce (us_per_call_one_partition).
+         beforehand (us_planned), and the whole call with one partition per
+         unit, rows written directly and no reduce (us_one_partition).
+roofline = the tile kernel with the largest share of the step, against the measured HBM
+         peak; roofline.variants gives, per long-context variant, its tile kernel and its
+         whole call (plan + tile + reduce) in µs and as a fraction of the peak.  The
+         roofline object closes the line.
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -43,8 +47,8 @@ import torch  # noqa: E402
 from paged_attention_decode_02_gb300 import ops, replicas, synth  # noqa: E402
 
 METRIC = "pa_decode µs/call and achieved KV GB/s (fraction of GB300 HBM peak)"
-WORKLOAD = ("long-context decode: MXFP4 and fp8-per-token KV, batch 16, 1 KV head, GQA 16, "
-            "head_dim 128, page 128, qlen 1, context_lens U[120000, 131072]")
+WORKLOAD = ("long-context decode, MXFP4 + fp8/token KV, B16 Hkv1 G16 D128 page128 qlen1 "
+                  "L~U[120000,131072]")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL = None  # decode kernel choice passed to every call (--kernel)
 
@@ -129,10 +133,20 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def traffic_from_profile():
-    """dram bytes per launch of the fp8 per-token tile kernel from the committed ncu summary,
-    or None when the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+def tile_kernel_name(case) -> str:
+    """The decode kernel a call of this workload launches (the library's own choice)."""
+    if KERNEL == "tc":
+        return "pa_tc_kernel"
+    if case.kv == synth.KV_MXFP4 and KERNEL is None:
+        return "pa_mx_kernel"
+    return "pa_tile_kernel"
+
+
+def traffic_from_profile(kernel: str):
+    """dram bytes per launch of this kernel on the long-context workload, from the committed
+    ncu summary profiles/ncu_traffic_<kernel>.txt, or None when there is none or the kernel
+    sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"ncu_traffic_{kernel}.txt")
     if not os.path.exists(path):
         return None
     kv = {}
@@ -244,13 +258,10 @@ def per_config(device, peak, calls=10, warmup=3):
         med, medg, medp = statistics.median(ts), statistics.median(tg), statistics.median(tp)
         medf = statistics.median(tf)
         name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
-        res[name] = {"us_per_call": round(med * 1e3, 2),
-                     "us_per_call_graph": round(medg * 1e3, 2),
-                     "us_per_call_planned": round(medp * 1e3, 2),
-                     "us_per_call_one_partition": round(medf * 1e3, 2), "algorithmic_bytes": nbytes,
-                     "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
-                     "GBps_graph": round(nbytes / (medg * 1e-3) / 1e9, 1),
-                     "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
+        res[name] = {"us": round(med * 1e3, 2), "us_graph": round(medg * 1e3, 2),
+                     "us_planned": round(medp * 1e3, 2), "us_one_partition": round(medf * 1e3, 2),
+                     "bytes": nbytes, "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
+                     "frac": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
         del graph
         del p, out, ws, ws1
     res.update(kv_write_config(device, peak, calls))
@@ -290,9 +301,9 @@ def kv_write_config(device, peak, calls):
     med = statistics.median(ts)
     nbytes = 2 * T * Hkv * (2 * D + D // 2 + D // 32) + 8 * T
     return {"mxfp4_kv_write_t65536_h8_d128": {
-        "us_per_call": round(med * 1e3, 2), "algorithmic_bytes": nbytes,
+        "us": round(med * 1e3, 2), "bytes": nbytes,
         "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
-        "frac_of_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}}
+        "frac": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}}
 
 
 def make_variant(kv, device, batch=None):
@@ -326,21 +337,27 @@ def run_ours(a):
     peak, peak_kind = peaks()
 
     def step(ev=None):
+        """One step; with ev, events before the plan, around the tile kernel and after
+        the reduce of each variant (its whole-call time and its tile kernel's time)."""
         for k, v in enumerate(variants):
-            ops.pa_decode_plan(v["args"], v["ws"], stream)
             if ev is not None:
                 ev[k][0].record(stream)
-            ops.pa_decode(v["args"], v["ws"], stream)
+            ops.pa_decode_plan(v["args"], v["ws"], stream)
             if ev is not None:
                 ev[k][1].record(stream)
+            ops.pa_decode(v["args"], v["ws"], stream)
+            if ev is not None:
+                ev[k][2].record(stream)
             ops.pa_decode_reduce(v["args"], v["ws"], stream)
+            if ev is not None:
+                ev[k][3].record(stream)
 
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
     for v in variants:
         assert ops.pa_decode_read_status(v["ws"]) == 0, "device status"
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in variants]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in variants]
            for _ in range(a.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws_n > 1:
@@ -353,7 +370,7 @@ def run_ours(a):
             step()
         end.record(stream)
         torch.cuda.synchronize()
-        # the same steps again with events around each tile kernel (its roofline)
+        # the same steps again with events around each call and each tile kernel
         for i in range(a.steps):
             step(evs[i])
         torch.cuda.synchronize()
@@ -373,7 +390,9 @@ def run_ours(a):
     if ws_n > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(end)
-    tile_ms = [[evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(a.steps)]
+    tile_ms = [[evs[i][k][1].elapsed_time(evs[i][k][2]) for i in range(a.steps)]
+               for k in range(len(variants))]
+    call_ms = [[evs[i][k][0].elapsed_time(evs[i][k][3]) for i in range(a.steps)]
                for k in range(len(variants))]
     total_ms = replicas.max_over_ranks(total_ms, dev)
     ms_step = total_ms / a.steps
@@ -458,58 +477,56 @@ def run_ours(a):
         e2e_ms = replicas.max_over_ranks(t0.elapsed_time(t1) / a.steps, dev)
         e2e_val = replicas.job_throughput(step_bytes, e2e_ms, ws_n)
         e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "overlap": "double-buffered: step i+1's inputs load and step i's output "
-                          "reads back on a copy stream while step i computes"}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    per = {}
+    # per variant: the tile kernel alone and the whole call (plan + tile + reduce), each
+    # as µs and as a fraction of the HBM peak; the roofline kernel is the one with the
+    # largest share of the step
+    var = {}
     for k, v in enumerate(variants):
-        med = statistics.median(tile_ms[k])
+        tile, call = statistics.median(tile_ms[k]), statistics.median(call_ms[k])
         med_b2b = statistics.median(b2b[k])
-        per[v["case"].name] = {
-            "tile_kernel_us": round(med * 1e3, 2),
-            "tile_kernel_us_back_to_back": round(med_b2b * 1e3, 2),
-            "frac_of_peak_back_to_back": round(v["bytes"] / (med_b2b * 1e-3) / 1e9 / peak, 4),
-            "algorithmic_bytes": v["bytes"],
-            "tile_kernel_GBps": round(v["bytes"] / (med * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(v["bytes"] / (med * 1e-3) / 1e9 / peak, 4),
-        }
-    dom = variants[-1]
-    dom_ms = statistics.mean(tile_ms[-1])
-    achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
+        frac = lambda ms: round(v["bytes"] / (ms * 1e-3) / 1e9 / peak, 4)
+        var[v["case"].name] = {
+            "tile_kernel": tile_kernel_name(v["case"]),
+            "tile_us": round(tile * 1e3, 2), "tile_frac": frac(tile),
+            "tile_us_back_to_back": round(med_b2b * 1e3, 2), "tile_frac_back_to_back": frac(med_b2b),
+            "call_us": round(call * 1e3, 2), "call_frac": frac(call),
+            "share_of_step": round(tile / ms_step, 3), "algorithmic_bytes": v["bytes"]}
+    dk = max(range(len(variants)), key=lambda k: statistics.mean(tile_ms[k]))
+    dom = variants[dk]
+    achieved = dom["bytes"] / (statistics.mean(tile_ms[dk]) * 1e-3) / 1e9
+    kname = tile_kernel_name(dom["case"])
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws_n,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 4),
-        "us_per_call": round(ms_step * 1e3 / len(variants), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic (seeded; shapes and value distributions of the workload)",
-        "config": {"workload": WORKLOAD, "kv": ["mxfp4 e2m1+e8m0/32", "fp8 e4m3 per-token"],
-                   "global_batch": 16 * ws_n, "seq_len": "120000-131072",
-                   "parallelism": f"replicas x{ws_n}",
-                   "l2": "no flush: each call streams more than the 129 MB L2",
-                   "mma": ("tcgen05.mma (TMEM accumulators)" if KERNEL == "tc"
-                           else "mma.sync m16n8k16 f16 x f16 -> f32"),
-                   "merge": "separate pa_decode_reduce launch"},
-        "per_variant": per,
-        "roofline": {"bound": "hbm", "kernel": f"pa_tile_kernel ({dom['case'].name})",
-                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic_from_profile()},
-        "e2e": e2e,
-        "gpu_launches": 3 * len(variants) * a.steps,  # plan, tile, reduce per variant
-        "clocks": clk.summary(),
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "global_batch": 16 * ws_n,
+                   "seq_len": "120000-131072", "parallelism": f"replicas x{ws_n}",
+                   "l2": "no flush: each call streams more than the 129 MB L2"},
     }
     if a.batch is not None or a.variant != "both":
         line["config"]["note"] = "profiling subset, not the benchmark workload"
-    if KERNEL == "tc":
-        line["config"]["kernel"] = "tcgen05 (--kernel tc)"
+    if KERNEL is not None:
+        line["config"]["kernel"] = KERNEL
     if not a.no_per_config and a.batch is None and a.variant == "both":
         line["per_config"] = per_config(dev, peak)
+    line["gpu_launches"] = 3 * len(variants) * a.steps  # plan, tile, reduce per variant
+    line["clocks"] = clk.summary()
+    line["e2e"] = e2e
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(variants) if not a.no_cpu_baseline else None
+    # last on the line, so that a tail of the output keeps it whole
+    line["roofline"] = {"bound": "hbm", "kernel": f"{kname} ({dom['case'].name})",
+                        "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
+                        "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": traffic_from_profile(kname), "variants": var}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         torch.distributed.destroy_process_group()
+
 
 
 def _oracle_problem(v, seqs):
@@ -543,8 +560,8 @@ def cpu_baseline(variants, nseq=None):
         prob.decode()
         total_s += time.perf_counter() - t
         lens = [v["lens"][s] for s in seqs]
-        total_bytes += synth.algorithmic_bytes(v["case"], lens) * 0 + \
-            sum(lens) * v["case"].num_kv_heads * synth.kv_bytes_per_token(v["case"])
+        # the sample's owned-token KV and scale bytes (its Q, O and table bytes are < 0.01 %)
+        total_bytes += sum(lens) * v["case"].num_kv_heads * synth.kv_bytes_per_token(v["case"])
         lens_used += sum(lens)
     return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
@@ -582,7 +599,9 @@ def run_reference(a):
             "n_gpus": ws_n, "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(el * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": WORKLOAD, "sample": f"first {nseq} sequences of each KV variant"},
+            "config": {"workload": WORKLOAD, "global_batch": 16 * ws_n,
+                       "seq_len": "120000-131072", "parallelism": f"replicas x{ws_n}",
+                       "l2": "no flush: each call streams more than the 129 MB L2"},
             "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"first {nseq} of 16 sequences of each KV variant per step"},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -50,11 +50,19 @@ struct MxCfg {
   static constexpr int NCONS = 4 * NGRP;
   static constexpr int WPROD = NCONS, WMMA = NCONS + 1, WUNP = NCONS + 2;  // WUNP, WUNP + 1
   static constexpr int NTHREADS = 32 * (NCONS + 4);
+  static_assert(NCONS % 4 == 0, "consumer and helper warps form whole warpgroups");
   static constexpr int MAXREG = (65536 / NTHREADS) / 8 * 8;  // one CTA per SM
-  static constexpr int NSB = 3;  // S buffers in tensor memory (32 columns each)
+  // Registers per thread after the split: the helper warpgroup (producer, MMA, unpack) gives
+  // up what its loops do not need and the consumer warpgroups take it; the two shares add
+  // up to the launch's MAXREG * NTHREADS.
+  static constexpr int REG_HELP = 56;
+  static constexpr int REG_CONS = ((MAXREG * NTHREADS - REG_HELP * 128) / (NCONS * 32)) / 8 * 8;
+  static_assert(REG_HELP <= MAXREG && REG_CONS >= MAXREG && REG_CONS <= 255, "register split");
+  static_assert(REG_HELP * 128 + REG_CONS * NCONS * 32 <= MAXREG * NTHREADS, "register split");
+  static constexpr int NSB = 5;  // S buffers in tensor memory (16 columns each)
   static constexpr int NSF = 3;  // K-scale buffers in tensor memory (4 columns each)
   static constexpr int NKU = 3;  // unpacked K tiles (the MMA's A operand)
-  static constexpr int NQB = 4;  // query buffers (task ordinal mod NQB); > NSB, see mx_mma
+  static constexpr int NQB = 6;  // query buffers (task ordinal mod NQB); > NSB, see mx_mma
   static constexpr int MAXT = 32;  // task records staged in shared memory (more: global reads)
   // ring slot: K packed [128 tokens][64 B], V [128][64 B] (64-byte swizzle), K and V e8m0
   // words [128][4 B]
@@ -63,7 +71,8 @@ struct MxCfg {
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_KU = OFF_RING + NS * SLOT;     // [NKU][128 tokens][128 B], 128-byte swizzle
   static constexpr int OFF_Q = OFF_KU + NKU * 16384;      // per buffer: hi [16][128], lo [16][128]
-  static constexpr int OFF_QC = OFF_Q + NQB * 4096;       // row factors [NQB][16]
+  static constexpr int OFF_QRAW = OFF_Q + NQB * 4096;    // next task's rows [16][256 B], scales [16]
+  static constexpr int OFF_QC = OFF_QRAW + RPAD * 256 + 64;  // row factors [NQB][16]
   static constexpr int OFF_SFA = OFF_QC + NQB * 64;       // K-scale staging [NSF][32][16 B]
   static constexpr int OFF_SFB = OFF_SFA + NSF * 512;     // query-scale staging [32][16 B]
   static constexpr int OFF_VTAB = OFF_SFB + 512;          // per consumer warp: [4][32] f16 factors
@@ -79,8 +88,8 @@ struct MxCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;     // tmem base, abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;       // + slack to align the base to 1 KiB
   static constexpr int TMEM_COLS = 128;
-  // S buffers of 32 columns (query rows 0..15 of the hi term, then of the lo term)
-  static constexpr int COL_S = 0, COL_SFA = NSB * 32, COL_SFB = COL_SFA + NSF * 4;
+  // S buffers of 16 columns (query rows 0..15; a split query's two terms accumulate there)
+  static constexpr int COL_S = 0, COL_SFA = NSB * 16, COL_SFB = COL_SFA + NSF * 4;
   static_assert(COL_SFB + 4 <= TMEM_COLS, "tensor memory columns");
   static_assert(NQB >= NSB + 1, "a query buffer is rewritten only after its last reader finished");
   static_assert(NSF == NKU && NKU <= NSB, "K tile and scale reuse wait on one S-buffer phase");
@@ -227,7 +236,9 @@ __device__ void mx_producer(const DecodeParams& p, const CUtensorMap* tmk, const
       // K and V arrive as 64 bytes per token, and 4 + 4 e8m0 bytes
       if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)((nbox - fbox) * box * (64 + 64 + 8)));
       __syncwarp();
-      if (lane >= fbox && lane < nbox) {
+      // (test hook: with drop_first_slice the chunk's first block is announced but never
+      // loaded, so every wait on it runs out and the status word reports the timeout)
+      if (lane >= fbox && lane < nbox && !(p.drop_first_slice && k == 0)) {
         fence_proxy_async();  // the slot was last read through the generic proxy
         const int tok = c0 + lane * box;
         const int srow = tok & page_mask;
@@ -247,41 +258,33 @@ __device__ void mx_producer(const DecodeParams& p, const CUtensorMap* tmk, const
 }
 
 // ---------------------------------------------------------------------------------------
-// MMA warp: the query words of a task's rows (this lane's 4 head dims of each), loaded ahead
-// of their use.
+// MMA warp: a task's query rows (and per-row e4m3 scales) copied ahead of their use into a
+// staging area of 16 rows x 256 bytes with cp.async, so that no register holds them while
+// the task before streams.
 template <class C>
-struct MxQRaw {
-  uint32_t w[C::RPAD][2];
-  float qsc[C::RPAD];
-};
-
-template <class C>
-__device__ __forceinline__ void mx_q_issue(const DecodeParams& p, const MxTask& T, int lane, MxQRaw<C>& q) {
-#pragma unroll
-  for (int r = 0; r < C::RPAD; ++r) {
-    q.w[r][0] = q.w[r][1] = 0u;
-    q.qsc[r] = 0.f;
-    if (r < p.R) {
-      const int h = T.hkv * p.G + r;  // qlen 1: row r is query head hkv * G + r
-      const int64_t row = (int64_t)T.s;
-      const int64_t off = row * p.q_st + (int64_t)h * p.q_sh + 4 * lane;
-      if (p.q_fp8) {
-        q.w[r][0] = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.q) + off);
-        q.qsc[r] = p.q_scale_per_row ? p.q_scale[row * p.Hq + h] : p.q_scale[0];
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + off);
-        q.w[r][0] = v.x;
-        q.w[r][1] = v.y;
-        q.qsc[r] = 1.f;
-      }
-    }
+__device__ __forceinline__ void mx_q_issue(const DecodeParams& p, uint8_t* sm, const MxTask& T, int lane) {
+  uint8_t* st = sm + C::OFF_QRAW;
+  const int rb = p.q_fp8 ? C::D : 2 * C::D;  // bytes of one query row
+  const int per_row = rb >> 4;                // 16-byte pieces per row
+  for (int i = lane; i < p.R * per_row; i += 32) {
+    const int r = i / per_row, c = i - r * per_row;
+    const int h = T.hkv * p.G + r;  // qlen 1: row r is query head hkv * G + r
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
+                         ((int64_t)T.s * p.q_st + (int64_t)h * p.q_sh) * (p.q_fp8 ? 1 : 2) + 16 * c;
+    cp_async16(st + r * 256 + 16 * c, src);
   }
+  if (p.q_fp8 && lane < p.R) {
+    const int h = T.hkv * p.G + lane;
+    cp_async4(st + C::RPAD * 256 + 4 * lane, p.q_scale_per_row ? p.q_scale + (int64_t)T.s * p.Hq + h : p.q_scale);
+  }
+  cp_async_commit();
 }
 
-// The query rows of a task as the B operand in e4m3 (hi, and lo for a bf16 query split
-// exactly) and their logit factors, into query buffer qb.
 template <class C>
-__device__ void mx_load_q(const DecodeParams& p, uint8_t* sm, const MxQRaw<C>& q, int qb, int lane) {
+__device__ void mx_load_q(const DecodeParams& p, uint8_t* sm, int qb, int lane) {
+  cp_async_wait_all();  // this lane's pieces of the staged rows
+  __syncwarp();         // and every other lane's
+  const uint8_t* st = sm + C::OFF_QRAW;
   uint8_t* qh = sm + C::OFF_Q + qb * 4096;
   uint8_t* ql = qh + 2048;
   float* qc = reinterpret_cast<float*>(sm + C::OFF_QC) + qb * C::RPAD;
@@ -290,15 +293,18 @@ __device__ void mx_load_q(const DecodeParams& p, uint8_t* sm, const MxQRaw<C>& q
 #pragma unroll 1
   for (int r = 0; r < C::RPAD; ++r) {
     uint32_t hib = 0, lob = 0;
-    float cr = p.scale_log2 * q.qsc[r] * (1.f / kKFactorBias);  // 0 for padding rows
+    const bool real = r < p.R;  // padding rows: zero words and a zero factor
+    const float qsc = !real ? 0.f : (p.q_fp8 ? reinterpret_cast<const float*>(st + C::RPAD * 256)[r] : 1.f);
+    float cr = p.scale_log2 * qsc * (1.f / kKFactorBias);
     if (p.q_fp8) {
-      hib = q.w[r][0];  // e4m3 as stored, times q_scale in the row factor
+      hib = real ? *reinterpret_cast<const uint32_t*>(st + r * 256 + 4 * lane) : 0u;  // e4m3 as stored
     } else {
+      const uint2 w = real ? *reinterpret_cast<const uint2*>(st + r * 256 + 8 * lane) : make_uint2(0u, 0u);
       float x[4];
-      x[0] = __uint_as_float(q.w[r][0] << 16);
-      x[1] = __uint_as_float(q.w[r][0] & 0xFFFF0000u);
-      x[2] = __uint_as_float(q.w[r][1] << 16);
-      x[3] = __uint_as_float(q.w[r][1] & 0xFFFF0000u);
+      x[0] = __uint_as_float(w.x << 16);
+      x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(w.y << 16);
+      x[3] = __uint_as_float(w.y & 0xFFFF0000u);
       float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
       for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -353,19 +359,18 @@ __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volat
   const bool two_terms = !p.q_fp8 && !p.q_quant;  // a bf16 query split into hi + lo
   // The first task's query rows are converted before the producer starts its copies (the
   // QRDY barrier): once the ring fills, the memory system is busy and a late load waits long.
-  MxQRaw<C> qn;
   int task = mx_next_task<C>(p, sm, tb, tb, te);
   if (task < te) {
-    mx_q_issue<C>(p, mx_task<C>(p, sm, tb, task), lane, qn);
-    mx_load_q<C>(p, sm, qn, 0, lane);
+    mx_q_issue<C>(p, sm, mx_task<C>(p, sm, tb, task), lane);
+    mx_load_q<C>(p, sm, 0, lane);
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars[C::B_QRDY]);
-  // the query scale bytes, once: in every lane quarter, lanes 0..15 (the hi term's 16 query
-  // rows) hold the hi factor and lanes 16..31 (the lo term's) the lo factor
+  // the query scale bytes, once, in every lane of every quarter: byte 0 the hi term's factor,
+  // byte 1 the lo term's (the MMA's scale-byte selector picks one per term)
   {
     uint8_t* st = sm + C::OFF_SFB;
-    const uint32_t w = lane < 16 ? C::SFB_HI * 0x01010101u : C::SFB_LO * 0x01010101u;
+    const uint32_t w = C::SFB_HI | (C::SFB_LO << 8) | (C::SFB_HI << 16) | (C::SFB_LO << 24);
     *reinterpret_cast<uint4*>(st + 16 * lane) = make_uint4(w, w, w, w);
     fence_proxy_async();
     __syncwarp();
@@ -382,9 +387,9 @@ __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volat
     // k - NQB <= k - 1 - NSB (every task in between holds a block); the S buffers of those
     // blocks were released (waited below, in block order) before this point, and a consumer
     // reads a task's row factors before it releases the S buffer of its first block.
-    if (ord > 0) mx_load_q<C>(p, sm, qn, qb, lane);  // the first was converted before the ring filled
-    const int next = mx_next_task<C>(p, sm, tb, task + 1, te);  // its query words load now
-    if (next < te) mx_q_issue<C>(p, mx_task<C>(p, sm, tb, next), lane, qn);
+    if (ord > 0) mx_load_q<C>(p, sm, qb, lane);  // the first was converted before the ring filled
+    const int next = mx_next_task<C>(p, sm, tb, task + 1, te);  // its query rows load now
+    if (next < te) mx_q_issue<C>(p, sm, mx_task<C>(p, sm, tb, next), lane);
     const uint32_t qh = smem_u32(sm + C::OFF_Q + qb * 4096);
     for (int i = 0; i < T.nblk; ++i, ++k) {
       const int sb = k % C::NSB, sf = k % C::NSF;
@@ -400,17 +405,22 @@ __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volat
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a = smem_u32(sm + C::OFF_KU + (k % C::NKU) * 16384);
-        const uint32_t d = tmem + (uint32_t)(C::COL_S + sb * 32);
+        const uint32_t d = tmem + (uint32_t)(C::COL_S + sb * 16);
         const uint32_t sfa = tmem + (uint32_t)(C::COL_SFA + sf * 4), sfb = tmem + (uint32_t)C::COL_SFB;
         // lane quarter q of the tokens reads its scales from column sfa + q
         tmem_cp_32x128b_x4(sfa, umma_desc_noswz(smem_u32(sm + C::OFF_SFA + sf * 512), 128));
-        // the hi and lo query terms are the B operand's rows 0..15 and 16..31 (one MMA of
-        // N = 32 per 32-value block); an e4m3 query has rows 0..15 only
-        const uint32_t n = two_terms ? 32u : 16u;
+        // one MMA of N = 16 query rows per 32-value block; a split query's lo term (rows 16..31
+        // of the buffer, its own scale byte) accumulates into the same columns
 #pragma unroll
         for (int s = 0; s < 4; ++s)
           umma_mxf8f6f4(d, umma_desc(a + 32 * s, 16, 1024), umma_desc(qh + 32 * s, 16, 1024),
-                        umma_idesc_mx(5u, 0u, n, 128u, (uint32_t)s, 0u), sfa, sfb, s > 0);
+                        umma_idesc_mx(5u, 0u, 16u, 128u, (uint32_t)s, 0u), sfa, sfb, s > 0);
+        if (two_terms) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            umma_mxf8f6f4(d, umma_desc(a + 32 * s, 16, 1024), umma_desc(qh + 2048 + 32 * s, 16, 1024),
+                          umma_idesc_mx(5u, 0u, 16u, 128u, (uint32_t)s, 1u), sfa, sfb, true);
+        }
         umma_commit(&bars[C::B_SFULL + sb]);
       }
       __syncwarp();
@@ -672,7 +682,6 @@ __device__ void mx_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
     }
   }
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-  const bool two_terms = !p.q_fp8 && !p.q_quant;  // the scores come as hi + lo terms
   bool ok = true;
   int k = 0, ord = 0;
   for (int task = tb; task < te; ++task) {
@@ -720,8 +729,8 @@ __device__ void mx_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::B_EMPTY + slot]);
         tc_fence_after();
-        uint32_t sraw[16], slo[16];
-        const uint32_t col = tmem + (uint32_t)(C::COL_S + sb * 32);
+        uint32_t sraw[16];
+        const uint32_t col = tmem + (uint32_t)(C::COL_S + sb * 16);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r4[4];
@@ -729,20 +738,7 @@ __device__ void mx_consumer(const DecodeParams& p, uint8_t* sm, uint64_t* bars, 
 #pragma unroll
           for (int e = 0; e < 4; ++e) sraw[4 * c + e] = r4[e];
         }
-        if (two_terms) {  // the lo term's scores, columns 16..31
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r4[4];
-            tmem_ld_16x256b(col + 16 + lane_base + ((uint32_t)(16 * (c >> 1)) << 16) + 8 * (c & 1), r4);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) slo[4 * c + e] = r4[e];
-          }
-        }
         tmem_wait_ld();
-        if (two_terms) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) sraw[e] = __float_as_uint(__uint_as_float(sraw[e]) + __uint_as_float(slo[e]));
-        }
         if (!crow_read) {  // written by the MMA warp before its first commit of the task
           crow[0] = qc[2 * t];
           crow[1] = qc[2 * t + 1];
@@ -934,14 +930,18 @@ __global__ void __launch_bounds__(C::NTHREADS, 1) __maxnreg__(C::MAXREG)
     *reinterpret_cast<int*>(sm + C::OFF_NBLK) = n;
   }
   __syncthreads();
-  if (warp < C::NCONS)
+  if (warp < C::NCONS) {
+    setmaxnreg_inc<C::REG_CONS>();
     mx_consumer<C>(p, sm, bars, abort_flag, tmem, tb, te, warp, lane);
-  else if (warp == C::WPROD)
-    mx_producer<C>(p, &tmk, &tmv, sm, bars, abort_flag, tb, te, lane);
-  else if (warp >= C::WUNP)
-    mx_unpack<C>(p, sm, bars, abort_flag, tb, te, warp - C::WUNP, lane);
-  else
-    mx_mma<C>(p, sm, bars, abort_flag, tmem, tb, te, lane);
+  } else {
+    setmaxnreg_dec<C::REG_HELP>();
+    if (warp == C::WPROD)
+      mx_producer<C>(p, &tmk, &tmv, sm, bars, abort_flag, tb, te, lane);
+    else if (warp >= C::WUNP)
+      mx_unpack<C>(p, sm, bars, abort_flag, tb, te, warp - C::WUNP, lane);
+    else
+      mx_mma<C>(p, sm, bars, abort_flag, tmem, tb, te, lane);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

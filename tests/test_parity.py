@@ -521,6 +521,22 @@ def test_long_context_full_size_sampled(kv):
     assert np.isfinite(got).all()
 
 
+@pytest.mark.parametrize("case", [synth.config3(qlen=1), synth.config3(qlen=4), synth.config2("b")],
+                         ids=lambda c: c.name)
+@pytest.mark.parametrize("kernel", [None, "mma"], ids=lambda k: k or "default")
+def test_stated_sizes_sampled(case, kernel):
+    # the workloads at their stated sizes (batch 16, 2 KV heads, head_dim 256) in the launch
+    # configuration the per-workload timings use; the oracle computes the shortest and the
+    # longest sequence and two more
+    p = synth.make(case)
+    got = run_gpu(p, kernel=kernel)
+    lens = p["context_lens"].tolist()
+    order = sorted(range(case.batch), key=lambda i: lens[i])
+    seqs = sorted({order[0], order[-1], order[case.batch // 2], 5})
+    util.assert_parity(got[seqs], util.oracle_decode(p, seqs=seqs), case.kv, case.name)
+    assert np.isfinite(got).all()
+
+
 @pytest.mark.parametrize("kv", [synth.KV_MXFP4, synth.KV_FP8], ids=["5a_mxfp4", "5b_fp8_token"])
 def test_long_context_fused_merge_sampled(kv):
     case = synth.config5(kv, batch=6, seed=2200)

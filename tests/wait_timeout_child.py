@@ -2,7 +2,8 @@
 PA_DECODE_TEST_DROP_SLICE=1, so that the library's first decode call leaves one ring slot
 per CTA unloaded and that pipeline wait runs out.  It makes that call, then a normal one on
 the same context, and prints one JSON line: both status words and the second call's parity
-against the oracle.  Usage: python -m tests.wait_timeout_child allocated|static"""
+against the oracle.  Usage: python -m tests.wait_timeout_child allocated|static [fp8|mxfp4]
+(fp8 per-token KV runs the tile kernel, MXFP4 KV the block-scaled tcgen05 kernel)."""
 import json
 import os
 import sys
@@ -17,10 +18,11 @@ from paged_attention_decode_02_gb300 import ops, synth  # noqa: E402
 from tests import util  # noqa: E402
 
 
-def main(mode: str):
+def main(mode: str, kv: str):
     assert os.environ.get("PA_DECODE_TEST_DROP_SLICE") == "1"
     ops.load_library()
-    case = synth.config5(synth.KV_FP8, batch=2, context_lens=(20000, 30000), seed=2901)
+    case = synth.config5(synth.KV_FP8 if kv == "fp8" else synth.KV_MXFP4, batch=2,
+                         context_lens=(20000, 30000), seed=2901)
     p = synth.make(case)
     ref = util.oracle_decode(p)  # before the first GPU call
     dev = synth.to_device(p, "cuda")
@@ -47,4 +49,4 @@ def main(mode: str):
 
 
 if __name__ == "__main__":
-    main(sys.argv[1])
+    main(sys.argv[1], sys.argv[2] if len(sys.argv) > 2 else "fp8")
