@@ -336,20 +336,21 @@ def run_ours(a):
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
 
-    def step(ev=None):
-        """One step; with ev, events before the plan, around the tile kernel and after
-        the reduce of each variant (its whole-call time and its tile kernel's time)."""
+    def step(ev=None, what="tile"):
+        """One step; with ev, events around each variant's tile kernel (what="tile") or
+        around its whole call, plan to reduce (what="call"): one kind per pass, so that
+        no event sits between the launches being timed."""
         for k, v in enumerate(variants):
-            if ev is not None:
+            if ev is not None and what == "call":
                 ev[k][0].record(stream)
             ops.pa_decode_plan(v["args"], v["ws"], stream)
-            if ev is not None:
+            if ev is not None and what == "tile":
                 ev[k][1].record(stream)
             ops.pa_decode(v["args"], v["ws"], stream)
-            if ev is not None:
+            if ev is not None and what == "tile":
                 ev[k][2].record(stream)
             ops.pa_decode_reduce(v["args"], v["ws"], stream)
-            if ev is not None:
+            if ev is not None and what == "call":
                 ev[k][3].record(stream)
 
     for _ in range(a.warmup):
@@ -370,9 +371,12 @@ def run_ours(a):
             step()
         end.record(stream)
         torch.cuda.synchronize()
-        # the same steps again with events around each call and each tile kernel
+        # the same steps again with events around each tile kernel, then around each call
         for i in range(a.steps):
-            step(evs[i])
+            step(evs[i], "tile")
+        torch.cuda.synchronize()
+        for i in range(a.steps):
+            step(evs[i], "call")
         torch.cuda.synchronize()
         # the tile kernel launched back to back after one plan (no plan / reduce between)
         b2b = []
