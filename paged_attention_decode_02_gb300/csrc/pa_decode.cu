@@ -233,28 +233,6 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   if (tid == 0) *pp.ntasks = carry_tasks;
   // chunks past the last task hold none
   for (int c = carry_chunk + 1 + tid; c <= pp.budget; c += blockDim.x) pp.chunk_first[c] = carry_tasks;
-  __syncthreads();
-  // Each chunk's first task: its query rows and first 64 block-table entries into L2 now,
-  // while the memory system is quiet (the decode kernel reads them before its first copies).
-  if (pp.q != nullptr) {
-    for (int c = tid; c < pp.budget; c += blockDim.x) {
-      const int t = pp.chunk_first[c];
-      if (t >= carry_tasks) continue;
-      const PlanTask tk = pp.tasks[t];
-      const int hkv = tk.hkv_part & 0xFFFF;
-      const char* bt = reinterpret_cast<const char*>(pp.bt + (int64_t)tk.seq * pp.bt_stride +
-                                                     (int64_t)tk.tile_begin * kTileTokens / pp.S);
-      prefetch_l2(bt);
-      prefetch_l2(bt + 128);
-      const int row_bytes = pp.D * pp.q_bytes;
-      for (int i = 0; i < pp.qlen; ++i)
-        for (int r = 0; r < pp.G; ++r) {
-          const char* q = reinterpret_cast<const char*>(pp.q) +
-                          (((int64_t)tk.seq * pp.qlen + i) * pp.q_st + (int64_t)(hkv * pp.G + r) * pp.q_sh) * pp.q_bytes;
-          for (int b = 0; b < row_bytes; b += 128) prefetch_l2(q + b);
-        }
-    }
-  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -712,14 +690,6 @@ pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* 
   pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
   pp.task_chunk = reinterpret_cast<int*>(w + L.task_chunk);
   pp.chunk_first = reinterpret_cast<int*>(w + L.chunk_first);
-  pp.q = a->query;
-  pp.q_st = a->q_stride_token;
-  pp.q_sh = a->q_stride_head;
-  pp.q_bytes = a->q_dtype == PA_Q_FP8_E4M3 ? 1 : 2;
-  pp.G = a->num_q_heads / a->num_kv_heads;
-  pp.D = a->head_dim;
-  pp.bt = a->block_tables;
-  pp.bt_stride = a->bt_stride;
   int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
   threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
   cudaLaunchConfig_t cfg = {};

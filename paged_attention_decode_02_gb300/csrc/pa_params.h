@@ -81,15 +81,6 @@ struct PlanParams {
   int max_partitions;
   int budget;
   const int32_t* ctx;
-  // for the L2 prefetch of each chunk's first task (its query rows and first block-table
-  // entries), so that the decode kernel's first dependent loads do not wait behind the copies
-  // that every other CTA starts at once
-  const void* q;
-  int64_t q_st, q_sh;  // elements
-  int q_bytes;         // bytes per query element
-  int G, D;
-  const int32_t* bt;
-  int64_t bt_stride;
   int* status;
   int* ntasks;
   int* nparts;
