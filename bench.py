@@ -23,8 +23,9 @@ per_config = every workload of the method, timed one call at a time through the 
          unit, rows written directly and no reduce (us_one_partition).
 roofline = the tile kernel with the largest share of the step, against the measured HBM
          peak; roofline.variants gives, per long-context variant, its tile kernel and its
-         whole call (plan + tile + reduce) in µs and as a fraction of the peak.  The
-         roofline object closes the line.
+         whole call (pa_decode_run: plan + tile + reduce) in µs and as a fraction of the
+         peak -- one call at a time (call_us) and calls back to back.  The roofline
+         object closes the line.
 --impl reference times the fp64 CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
@@ -336,29 +337,23 @@ def run_ours(a):
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
 
-    def step(ev=None, what="tile"):
-        """One step; with ev, events around each variant's tile kernel (what="tile") or
-        around its whole call, plan to reduce (what="call"): one kind per pass, so that
-        no event sits between the launches being timed."""
+    def step(ev=None):
+        """One step; with ev, events around each variant's tile kernel."""
         for k, v in enumerate(variants):
-            if ev is not None and what == "call":
-                ev[k][0].record(stream)
             ops.pa_decode_plan(v["args"], v["ws"], stream)
-            if ev is not None and what == "tile":
-                ev[k][1].record(stream)
+            if ev is not None:
+                ev[k][0].record(stream)
             ops.pa_decode(v["args"], v["ws"], stream)
-            if ev is not None and what == "tile":
-                ev[k][2].record(stream)
+            if ev is not None:
+                ev[k][1].record(stream)
             ops.pa_decode_reduce(v["args"], v["ws"], stream)
-            if ev is not None and what == "call":
-                ev[k][3].record(stream)
 
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
     for v in variants:
         assert ops.pa_decode_read_status(v["ws"]) == 0, "device status"
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in variants]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in variants]
            for _ in range(a.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws_n > 1:
@@ -371,13 +366,33 @@ def run_ours(a):
             step()
         end.record(stream)
         torch.cuda.synchronize()
-        # the same steps again with events around each tile kernel, then around each call
+        # the same steps again with events around each tile kernel
         for i in range(a.steps):
-            step(evs[i], "tile")
+            step(evs[i])
         torch.cuda.synchronize()
-        for i in range(a.steps):
-            step(evs[i], "call")
-        torch.cuda.synchronize()
+        # each variant's whole call (plan, tile, reduce through pa_decode_run): one call at a
+        # time behind a short device-side wait, so that the host's launch time is not counted
+        # and no earlier call overlaps it; and the same calls back to back
+        call_one, call_b2b = [], []
+        for v in variants:
+            one = []
+            for _ in range(a.steps):
+                torch.cuda._sleep(200000)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                ops.pa_decode_run(v["args"], v["ws"], stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                one.append(e0.elapsed_time(e1))
+            call_one.append(one)
+            torch.cuda._sleep(200000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(a.steps):
+                ops.pa_decode_run(v["args"], v["ws"], stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            call_b2b.append(e0.elapsed_time(e1) / a.steps)
         # the tile kernel launched back to back after one plan (no plan / reduce between)
         b2b = []
         for k, v in enumerate(variants):
@@ -394,9 +409,7 @@ def run_ours(a):
     if ws_n > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(end)
-    tile_ms = [[evs[i][k][1].elapsed_time(evs[i][k][2]) for i in range(a.steps)]
-               for k in range(len(variants))]
-    call_ms = [[evs[i][k][0].elapsed_time(evs[i][k][3]) for i in range(a.steps)]
+    tile_ms = [[evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(a.steps)]
                for k in range(len(variants))]
     total_ms = replicas.max_over_ranks(total_ms, dev)
     ms_step = total_ms / a.steps
@@ -488,7 +501,7 @@ def run_ours(a):
     # largest share of the step
     var = {}
     for k, v in enumerate(variants):
-        tile, call = statistics.median(tile_ms[k]), statistics.median(call_ms[k])
+        tile, call, callb = statistics.median(tile_ms[k]), statistics.median(call_one[k]), call_b2b[k]
         med_b2b = statistics.median(b2b[k])
         frac = lambda ms: round(v["bytes"] / (ms * 1e-3) / 1e9 / peak, 4)
         var[v["case"].name] = {
@@ -496,6 +509,7 @@ def run_ours(a):
             "tile_us": round(tile * 1e3, 2), "tile_frac": frac(tile),
             "tile_us_back_to_back": round(med_b2b * 1e3, 2), "tile_frac_back_to_back": frac(med_b2b),
             "call_us": round(call * 1e3, 2), "call_frac": frac(call),
+            "call_us_back_to_back": round(callb * 1e3, 2), "call_frac_back_to_back": frac(callb),
             "share_of_step": round(tile / ms_step, 3), "algorithmic_bytes": v["bytes"]}
     dk = max(range(len(variants)), key=lambda k: statistics.mean(tile_ms[k]))
     dom = variants[dk]
