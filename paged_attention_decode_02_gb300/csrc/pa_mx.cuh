@@ -357,15 +357,17 @@ template <class C>
 __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volatile int* abort_flag,
                        uint32_t tmem, int tb, int te, int lane) {
   const bool two_terms = !p.q_fp8 && !p.q_quant;  // a bf16 query split into hi + lo
-  // The first task's query rows are converted before the producer starts its copies (the
-  // QRDY barrier): once the ring fills, the memory system is busy and a late load waits long.
+  // The first task's query rows are in shared memory before the producer starts its copies
+  // (the QRDY barrier): once the ring fills, the memory system is busy and a late load waits
+  // long.  They are converted while the first blocks land.
   int task = mx_next_task<C>(p, sm, tb, tb, te);
   if (task < te) {
     mx_q_issue<C>(p, sm, mx_task<C>(p, sm, tb, task), lane);
-    mx_load_q<C>(p, sm, 0, lane);
+    cp_async_wait_all();
   }
   __syncwarp();
-  if (lane == 0) mbar_arrive(&bars[C::B_QRDY]);
+  if (lane == 0) mbar_arrive(&bars[C::B_QRDY]);  // the rows are in; they convert while K lands
+  if (task < te) mx_load_q<C>(p, sm, 0, lane);
   // the query scale bytes, once, in every lane of every quarter: byte 0 the hi term's factor,
   // byte 1 the lo term's (the MMA's scale-byte selector picks one per term)
   {
@@ -387,7 +389,7 @@ __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volat
     // k - NQB <= k - 1 - NSB (every task in between holds a block); the S buffers of those
     // blocks were released (waited below, in block order) before this point, and a consumer
     // reads a task's row factors before it releases the S buffer of its first block.
-    if (ord > 0) mx_load_q<C>(p, sm, qb, lane);  // the first was converted before the ring filled
+    if (ord > 0) mx_load_q<C>(p, sm, qb, lane);  // the first was converted at the start
     const int next = mx_next_task<C>(p, sm, tb, task + 1, te);  // its query rows load now
     if (next < te) mx_q_issue<C>(p, sm, mx_task<C>(p, sm, tb, next), lane);
     const uint32_t qh = smem_u32(sm + C::OFF_Q + qb * 4096);
