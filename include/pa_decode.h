@@ -226,8 +226,16 @@ pa_status pa_decode_reduce(const pa_decode_args* args, void* workspace,
 /* plan + decode + reduce in one call, on one stream.  With max_partitions == 1 each
  * (sequence, KV head) unit is a single task, the decode stores its bf16 rows itself and
  * the reduce has nothing to do; this is how the pages' plan-free mode is served here
- * ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary), except that pa_decode_plan still builds
- * the task list first. */
+ * ("[FlyDSL] pa_decode: MXFP4 K/V ...", Summary).
+ * Small problems run as one launch instead, with no plan and no reduce kernel: when every
+ * (sequence, KV head) unit fits the CTA budget and a unit's tiles (bounded by
+ * max_blocks_per_seq * page_size, or by the sliding window) leave at most 3 per CTA, each
+ * unit gets a thread-block cluster of up to 8 CTAs (at most max_partitions), each CTA an
+ * equal run of the unit's tiles, and after a cluster barrier the cluster's CTAs merge the
+ * partials in partition order with the reduce's formula, each CTA a share of the rows.  That launch leaves the workspace without a
+ * plan (no chunk holds a task): a pa_decode or pa_decode_reduce on it needs a new
+ * pa_decode_plan first.  The tcgen05 tile kernel (kernel = PA_KERNEL_TCGEN05) always takes
+ * the planned path. */
 pa_status pa_decode_run(const pa_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);
 

@@ -35,15 +35,6 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int* clamped) {
   return L;
 }
 
-// Tiles of a (sequence, KV head) unit: [*first, ceil(L / 256)), where *first is the tile
-// holding the first token that any query position's sliding window reaches (0 without a
-// window).  Returns the count.
-__device__ __forceinline__ int unit_tiles(int L, int qlen, int window, int* first) {
-  int lo = window > 0 ? L - qlen - window + 1 : 0;
-  lo = lo > 0 ? lo : 0;
-  *first = lo / kTileTokens;
-  return (L + kTileTokens - 1) / kTileTokens - *first;
-}
 
 template <typename T>
 __device__ T block_exclusive_scan(T v, T* total, T* sh) {  // sh: >= 32 elements
@@ -640,72 +631,40 @@ pa_status cache_map_vt(const pa_decode_args* a, int dims, CUtensorMap* m) {
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
-}  // namespace
-
-extern "C" {
-
-int32_t pa_decode_abi_version(void) { return PA_DECODE_ABI_VERSION; }
-
-const char* pa_status_string(pa_status s) {
-  switch (s) {
-    case PA_OK: return "ok";
-    case PA_ERR_INVALID_ARG: return "invalid argument";
-    case PA_ERR_UNSUPPORTED: return "unsupported combination";
-    case PA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
-    case PA_ERR_CUDA: return "CUDA error";
-    default: return "unknown status";
+// Single-launch mode of pa_decode_run for small problems: no plan and no reduce kernel;
+// the tile kernel takes one cluster of `split` CTAs per (sequence, KV head) unit and each
+// CTA a run of the unit's tiles, the cluster's CTAs then merging the partials (rows split
+// among them).  It runs
+// when every unit fits the CTA budget, a unit's tiles (bounded by the block-table width,
+// or by the sliding window) give each CTA at most kSingleLaunchTiles of them, and the
+// caller did not ask for the tcgen05 tile kernel.  Returns the split, or 0 (planned path).
+// The mode leaves the workspace's plan empty (no chunk holds a task, every unit one
+// partition), so a pa_decode or pa_decode_reduce that follows without a new plan finds
+// nothing to do.
+constexpr int kSingleLaunchTiles = 3;
+constexpr int kMaxClusterCtas = 8;  // portable cluster size
+int single_launch_split(const pa_decode_args* a, const WsLayout& L) {
+  if (a->kernel == PA_KERNEL_TCGEN05) return 0;
+  const int64_t units = (int64_t)a->batch * a->num_kv_heads;
+  if (units < 1 || units > L.budget) return 0;
+  const int64_t TT = pa::kTileTokens;
+  int64_t tiles = ((int64_t)a->max_blocks_per_seq * a->page_size + TT - 1) / TT;
+  if (a->sliding_window > 0) {
+    const int64_t wt = ((int64_t)a->sliding_window + a->qlen - 1 + TT - 1) / TT + 1;
+    tiles = wt < tiles ? wt : tiles;
   }
+  if (tiles < 1) tiles = 1;
+  int64_t split = L.budget / units;  // one wave: units * split <= budget CTAs
+  if (split > kMaxClusterCtas) split = kMaxClusterCtas;
+  if (split > tiles) split = tiles;
+  if (split > L.max_partitions) split = L.max_partitions;
+  if (split < 1) split = 1;
+  if (split > 1 && units * split > L.slots) return 0;  // partial slots (units <= budget: never)
+  if ((tiles + split - 1) / split > kSingleLaunchTiles) return 0;
+  return (int)split;
 }
 
-pa_status pa_decode_validate(const pa_decode_args* a) { return validate(a); }
-
-size_t pa_decode_workspace_size(const pa_decode_args* a) {
-  if (validate(a) != PA_OK) return 0;
-  WsLayout L;
-  if (make_layout(a, &L) != PA_OK) return 0;
-  return L.total;
-}
-
-pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
-  pa_status st = validate(a);
-  if (st != PA_OK) return st;
-  WsLayout L;
-  if ((st = check_ws(a, ws, bytes, &L)) != PA_OK) return st;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  pa::PlanParams pp;
-  pp.B = a->batch;
-  pp.Hkv = a->num_kv_heads;
-  pp.W = a->max_blocks_per_seq;
-  pp.S = a->page_size;
-  pp.qlen = a->qlen;
-  pp.window = a->sliding_window;
-  pp.max_partitions = L.max_partitions;
-  pp.budget = L.budget;
-  pp.ctx = a->context_lens;
-  pp.status = reinterpret_cast<int*>(w + L.status);
-  pp.ntasks = reinterpret_cast<int*>(w + L.ntasks);
-  pp.nparts = reinterpret_cast<int*>(w + L.nparts);
-  pp.part_base = reinterpret_cast<int*>(w + L.part_base);
-  pp.counters = reinterpret_cast<int*>(w + L.counters);
-  pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
-  pp.task_chunk = reinterpret_cast<int*>(w + L.task_chunk);
-  pp.chunk_first = reinterpret_cast<int*>(w + L.chunk_first);
-  int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
-  threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(threads);
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pa::pa_plan_kernel, pp) != cudaSuccess) return PA_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-}
-
-pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
+pa_status decode_launch(const pa_decode_args* a, void* ws, size_t bytes, void* stream, int pf_split) {
   pa_status st = validate(a);
   if (st != PA_OK) return st;
   WsLayout L;
@@ -714,8 +673,9 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   const int G = a->num_q_heads / a->num_kv_heads;
   const int R = G * a->qlen;
   const int kind = a->kv_dtype == PA_KV_BF16 ? pa::KIND_BF16 : (a->kv_dtype == PA_KV_FP8_E4M3 ? pa::KIND_FP8 : pa::KIND_FP4);
-  const bool use_tc = tc_kernel_applies(a, R);
-  const bool use_mx = !use_tc && mx_kernel_applies(a);
+  // the single-launch mode runs the mma.sync tile kernel
+  const bool use_tc = pf_split == 0 && tc_kernel_applies(a, R);
+  const bool use_mx = pf_split == 0 && !use_tc && mx_kernel_applies(a);
   int tc = 0, sub = 0, dims = a->head_dim;
   if (use_mx) {
     tc = 128;
@@ -785,8 +745,10 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   p.chunk_first = reinterpret_cast<const int*>(w + L.chunk_first);
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_o = reinterpret_cast<float*>(w + L.part_o);
-  p.counters = a->merge_in_decode ? reinterpret_cast<int*>(w + L.counters) : nullptr;
-  const int grid = L.budget;
+  p.counters = a->merge_in_decode && pf_split == 0 ? reinterpret_cast<int*>(w + L.counters) : nullptr;
+  p.pf_split = pf_split;
+  p.n_chunks = L.budget;
+  const int grid = pf_split > 0 ? a->batch * a->num_kv_heads * pf_split : L.budget;
   int rc;
   if (use_mx) {
     rc = pa::launch_mx_mxfp4(p, tk, tv, grid, stream);
@@ -804,6 +766,75 @@ pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* strea
   else
     rc = pa::launch_tile_mxfp4(p, tk, tv, grid, stream);
   return rc == 0 ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_decode_abi_version(void) { return PA_DECODE_ABI_VERSION; }
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported combination";
+    case PA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case PA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+pa_status pa_decode_validate(const pa_decode_args* a) { return validate(a); }
+
+size_t pa_decode_workspace_size(const pa_decode_args* a) {
+  if (validate(a) != PA_OK) return 0;
+  WsLayout L;
+  if (make_layout(a, &L) != PA_OK) return 0;
+  return L.total;
+}
+
+pa_status pa_decode_plan(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
+  pa_status st = validate(a);
+  if (st != PA_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(a, ws, bytes, &L)) != PA_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  pa::PlanParams pp;
+  pp.B = a->batch;
+  pp.Hkv = a->num_kv_heads;
+  pp.W = a->max_blocks_per_seq;
+  pp.S = a->page_size;
+  pp.qlen = a->qlen;
+  pp.window = a->sliding_window;
+  pp.max_partitions = L.max_partitions;
+  pp.budget = L.budget;
+  pp.ctx = a->context_lens;
+  pp.status = reinterpret_cast<int*>(w + L.status);
+  pp.ntasks = reinterpret_cast<int*>(w + L.ntasks);
+  pp.nparts = reinterpret_cast<int*>(w + L.nparts);
+  pp.part_base = reinterpret_cast<int*>(w + L.part_base);
+  pp.counters = reinterpret_cast<int*>(w + L.counters);
+  pp.tasks = reinterpret_cast<pa::PlanTask*>(w + L.tasks);
+  pp.task_chunk = reinterpret_cast<int*>(w + L.task_chunk);
+  pp.chunk_first = reinterpret_cast<int*>(w + L.chunk_first);
+  int threads = (a->batch + 31) / 32 * 32;  // one thread per sequence, up to 1024
+  threads = threads < 32 ? 32 : (threads > 1024 ? 1024 : threads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pa::pa_plan_kernel, pp) != cudaSuccess) return PA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
+  return decode_launch(a, ws, bytes, stream, 0);
 }
 
 pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
@@ -845,7 +876,13 @@ pa_status pa_decode_reduce(const pa_decode_args* a, void* ws, size_t bytes, void
 }
 
 pa_status pa_decode_run(const pa_decode_args* a, void* ws, size_t bytes, void* stream) {
-  pa_status st = pa_decode_plan(a, ws, bytes, stream);
+  pa_status st = validate(a);
+  if (st != PA_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(a, ws, bytes, &L)) != PA_OK) return st;
+  const int split = single_launch_split(a, L);
+  if (split > 0) return decode_launch(a, ws, bytes, stream, split);
+  st = pa_decode_plan(a, ws, bytes, stream);
   if (st != PA_OK) return st;
   if ((st = pa_decode(a, ws, bytes, stream)) != PA_OK) return st;
   return pa_decode_reduce(a, ws, bytes, stream);

@@ -42,7 +42,21 @@ struct WsLayout {
   int32_t max_partitions;
 };
 
+// Tiles of a (sequence, KV head) unit: [*first, ceil(L / 256)), where *first is the tile
+// holding the first token that any query position's sliding window reaches (0 without a
+// window).  Returns the count.  The plan and the single-launch path both split units by it.
+__device__ __forceinline__ int unit_tiles(int L, int qlen, int window, int* first) {
+  int lo = window > 0 ? L - qlen - window + 1 : 0;
+  lo = lo > 0 ? lo : 0;
+  *first = lo / kTileTokens;
+  return (L + kTileTokens - 1) / kTileTokens - *first;
+}
+
 struct DecodeParams {
+  // single-launch mode (no plan, no reduce kernel): CTAs per (sequence, KV head) unit,
+  // one thread-block cluster per unit, partials merged inside the cluster; 0: planned
+  int pf_split;
+  int n_chunks;  // the workspace's chunk count (its task list has n_chunks + 1 boundaries)
   int B, qlen, Hq, Hkv, G, R, D, S, W, NB;
   int64_t bt_stride;
   float scale_log2;  // softmax_scale * log2(e)

@@ -347,6 +347,7 @@ __device__ void load_q_finish(const DecodeParams& p, uint8_t* smem, const QRaw<C
 // block-table entries of the next slice are fetched one slice early (blk, one per box,
 // held by lanes 0..nbox-1) so that no refill waits on a dependent global load.
 struct SliceIt {
+  const PlanTask* tasks;  // the plan's task list, or the single-launch mode's one record
   int task, c0, t0, t1, s, hkv, L;
   int lo;  // first token of the lowest query position's sliding window (0: none)
   const int32_t* btrow;
@@ -356,7 +357,7 @@ struct SliceIt {
 };
 
 __device__ __forceinline__ void it_load_task(SliceIt& it, const DecodeParams& p) {
-  const PlanTask tk = p.tasks[it.task];
+  const PlanTask tk = it.tasks[it.task];
   it.s = tk.seq;
   it.hkv = tk.hkv_part & 0xFFFF;
   it.L = clamped_context(p, it.s);
@@ -928,10 +929,77 @@ __device__ __forceinline__ void stage_compute(
   }
 }
 
+// Merge partitions [base, base + nparts) of the split unit (s, hkv) in partition order with
+// the reduce kernel's formula and store its bf16 rows [r0, r1); every thread of the CTA
+// takes part.
+template <class C>
+__device__ void merge_partials(const DecodeParams& p, float* obuf, int s, int hkv, int64_t base,
+                               int nparts, int cw, int lane, int r0, int r1) {
+    const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
+    float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= OBW)
+    // one warp per row: lanes over partitions, shuffle-tree max and sum
+    for (int r = r0 + cw; r < r1; r += C::NCW) {
+      float M = -INFINITY;
+      for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&pml[(base + q) * p.R + r]).x);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float mb = M == -INFINITY ? 0.f : M;
+      float W = 0.f;
+      for (int q = lane; q < nparts; q += 32) {
+        const float2 e = __ldcg(&pml[(base + q) * p.R + r]);
+        const float w = e.y * fast_exp2(e.x - mb);
+        wts[r * nparts + q] = w;
+        W += w;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+      if (p.sinks != nullptr && W > 0.f) W += fast_exp2(p.sinks[hkv * p.G + r % p.G] * kLog2e - mb);
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      __syncwarp();
+      for (int q = lane; q < nparts; q += 32) wts[r * nparts + q] *= inv;
+    }
+    named_bar(BAR_CONSUMERS, C::NCW * 32);
+    // float4 columns, partitions in order; loads are independent of the sum
+    const float4* po4 = reinterpret_cast<const float4*>(p.part_o);
+    for (int idx = threadIdx.x + r0 * (C::D / 4); idx < r1 * (C::D / 4); idx += C::NTHREADS) {
+      const int r = idx / (C::D / 4), d4 = idx % (C::D / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      int q = 0;
+      for (; q + 4 <= nparts; q += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcg(&po4[((base + q + u) * p.R + r) * (C::D / 4) + d4]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = wts[r * nparts + q + u];
+          acc.x += w * v[u].x;
+          acc.y += w * v[u].y;
+          acc.z += w * v[u].z;
+          acc.w += w * v[u].w;
+        }
+      }
+      for (; q < nparts; ++q) {
+        const float4 v = __ldcg(&po4[((base + q) * p.R + r) * (C::D / 4) + d4]);
+        const float w = wts[r * nparts + q];
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+      const int i = r / p.G, h = hkv * p.G + r % p.G;
+      __nv_bfloat16* dst = p.out + ((int64_t)s * p.qlen + i) * p.o_st + (int64_t)h * p.o_sh + 4 * d4;
+      dst[0] = __float2bfloat16_rn(acc.x);
+      dst[1] = __float2bfloat16_rn(acc.y);
+      dst[2] = __float2bfloat16_rn(acc.z);
+      dst[3] = __float2bfloat16_rn(acc.w);
+    }
+}
+
 template <class C>
 __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                          uint8_t* smem, uint64_t* full, volatile int* abort_flag, int t_begin,
-                          int t_end, int cw, int lane) {
+                          uint8_t* smem, uint64_t* full, volatile int* abort_flag,
+                          const PlanTask* tasks, int t_begin, int t_end, int pf_nparts,
+                          int pf_pbase, int cw, int lane) {
   const int tg = cw / C::NDW, dw = cw % C::NDW;
   const int g = lane >> 2, t = lane & 3;
   const int r0 = tg * C::TW;  // this warp's slice inside a CTA stage
@@ -981,12 +1049,13 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   QRaw<C> qn;  // query words of the next task to start
   if constexpr (C::Q_EARLY) {
     if (t_begin < t_end) {
-      const PlanTask tk0 = p.tasks[t_begin];
+      const PlanTask tk0 = tasks[t_begin];
       load_q_issue<C>(p, tk0.seq, tk0.hkv_part & 0xFFFF, cw, lane, qn);
     }
   }
   // prologue: fill the ring
   SliceIt ld;
+  ld.tasks = tasks;
   ld.task = t_begin;
   ld.done = ld.task >= t_end;
   ld.blk = 0;
@@ -1019,22 +1088,22 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
   const int wcap = p.window > 0 ? p.window : 0x7FFFFFFF;
 
   for (int task = t_begin; task < t_end; ++task) {
-    const PlanTask tk = p.tasks[task];
+    const PlanTask tk = tasks[task];
     const int s = tk.seq, hkv = tk.hkv_part & 0xFFFF, part = tk.hkv_part >> 16;
     const int L = clamped_context(p, s);
     const int t0 = tk.tile_begin * kTileTokens;
     int t1 = tk.tile_end * kTileTokens;
     t1 = t1 < L ? t1 : L;
     const int unit = s * p.Hkv + hkv;
-    const int nparts = p.nparts[unit];
-    const int64_t slot = nparts > 1 ? (int64_t)p.part_base[unit] + part : 0;
+    const int nparts = p.pf_split > 0 ? pf_nparts : p.nparts[unit];
+    const int64_t slot = nparts > 1 ? (int64_t)(p.pf_split > 0 ? pf_pbase : p.part_base[unit]) + part : 0;
 
     if constexpr (!C::Q_EARLY) load_q_issue<C>(p, s, hkv, cw, lane, qn);
     load_q_finish<C>(p, smem, qn, cw, lane, k_scale_tensor);
     named_bar(BAR_CONSUMERS, C::NCW * 32);
     // The next task's record, read at this task's merge, copied without waiting for it.
     if (C::Q_EARLY && task + 1 < t_end && cw == 0 && lane == 0) {
-      cp_async16(smem + C::OFF_NXT, p.tasks + task + 1);
+      cp_async16(smem + C::OFF_NXT, tasks + task + 1);
       cp_async_commit();
     }
     // Touch this task's output rows now, so that their address translation is not first
@@ -1267,65 +1336,7 @@ __device__ void warp_main(const DecodeParams& p, const CUtensorMap* tmk, const C
       named_bar(BAR_CONSUMERS, C::NCW * 32);
       if (*mflag) {
         __threadfence();
-        const int64_t base = p.part_base[unit];
-        const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
-        float* wts = obuf;  // normalised weights [R][nparts] (nparts <= 128 <= OBW)
-        // one warp per row: lanes over partitions, shuffle-tree max and sum
-        for (int r = cw; r < p.R; r += C::NCW) {
-          float M = -INFINITY;
-          for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(&pml[(base + q) * p.R + r]).x);
-#pragma unroll
-          for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          const float mb = M == -INFINITY ? 0.f : M;
-          float W = 0.f;
-          for (int q = lane; q < nparts; q += 32) {
-            const float2 e = __ldcg(&pml[(base + q) * p.R + r]);
-            const float w = e.y * fast_exp2(e.x - mb);
-            wts[r * nparts + q] = w;
-            W += w;
-          }
-#pragma unroll
-          for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-          if (p.sinks != nullptr && W > 0.f) W += fast_exp2(p.sinks[hkv * p.G + r % p.G] * kLog2e - mb);
-          const float inv = W > 0.f ? 1.f / W : 0.f;
-          __syncwarp();
-          for (int q = lane; q < nparts; q += 32) wts[r * nparts + q] *= inv;
-        }
-        named_bar(BAR_CONSUMERS, C::NCW * 32);
-        // float4 columns, partitions in order; loads are independent of the sum
-        const float4* po4 = reinterpret_cast<const float4*>(p.part_o);
-        for (int idx = threadIdx.x; idx < p.R * (C::D / 4); idx += C::NTHREADS) {
-          const int r = idx / (C::D / 4), d4 = idx % (C::D / 4);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          int q = 0;
-          for (; q + 4 <= nparts; q += 4) {
-            float4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = __ldcg(&po4[((base + q + u) * p.R + r) * (C::D / 4) + d4]);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float w = wts[r * nparts + q + u];
-              acc.x += w * v[u].x;
-              acc.y += w * v[u].y;
-              acc.z += w * v[u].z;
-              acc.w += w * v[u].w;
-            }
-          }
-          for (; q < nparts; ++q) {
-            const float4 v = __ldcg(&po4[((base + q) * p.R + r) * (C::D / 4) + d4]);
-            const float w = wts[r * nparts + q];
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-          }
-          const int i = r / p.G, h = hkv * p.G + r % p.G;
-          __nv_bfloat16* dst = p.out + ((int64_t)s * p.qlen + i) * p.o_st + (int64_t)h * p.o_sh + 4 * d4;
-          dst[0] = __float2bfloat16_rn(acc.x);
-          dst[1] = __float2bfloat16_rn(acc.y);
-          dst[2] = __float2bfloat16_rn(acc.z);
-          dst[3] = __float2bfloat16_rn(acc.w);
-        }
+        merge_partials<C>(p, obuf, s, hkv, p.part_base[unit], nparts, cw, lane, 0, p.R);
       }
     }
   }
@@ -1354,9 +1365,55 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
   pdl_wait_prior();         // the plan's task list is complete and visible from here on
   pdl_launch_dependents();  // the reduce kernel may launch (after the plan completed); it
                             // waits for this grid's results
-  const int t_begin = p.chunk_first[blockIdx.x], t_end = p.chunk_first[blockIdx.x + 1];
-  warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, t_begin, t_end, threadIdx.x >> 5,
-               threadIdx.x & 31);
+  const int cw = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.pf_split == 0) {  // planned: this CTA runs its chunk of the plan's task list
+    const int t_begin = p.chunk_first[blockIdx.x], t_end = p.chunk_first[blockIdx.x + 1];
+    warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, p.tasks, t_begin, t_end, 0, 0, cw, lane);
+    return;
+  }
+  // Single-launch mode (no plan, no reduce kernel): unit blockIdx / split, one cluster of
+  // `split` CTAs per unit, CTA r of it taking the r-th of P = min(split, tiles) equal runs of
+  // the unit's tiles (the plan's equal split, restricted to one unit); after a cluster
+  // barrier the cluster's CTAs merge a split unit's partials, each a share of its rows.
+  const int split = p.pf_split;
+  const int rank = split > 1 ? (int)cluster_ctarank() : 0;
+  const int unit = blockIdx.x / split;
+  const int s = unit / p.Hkv, hkv = unit - s * p.Hkv;
+  int first;
+  const int n = unit_tiles(clamped_context(p, s), p.qlen, p.window, &first);
+  const int P = n < split ? (n > 0 ? n : 1) : split;
+  PlanTask* rec = reinterpret_cast<PlanTask*>(smem + C::OFF_NXT);  // no next task here
+  if (threadIdx.x == 0) {
+    rec->seq = s;
+    rec->hkv_part = hkv | (rank << 16);
+    rec->tile_begin = first + (int)((int64_t)rank * n / P);
+    rec->tile_end = first + (int)((int64_t)(rank + 1) * n / P);
+  }
+  if (blockIdx.x == 0 && cw == 0) {  // the call's status word (a timeout is ORed in only
+    const int cap = p.W * p.S;       // after a wait of 2 s, long after this write)
+    bool clamped = false;
+    for (int q = lane; q < p.B; q += 32) clamped |= p.ctx[q] > cap;
+    clamped = __any_sync(0xffffffffu, clamped);
+    if (lane == 0) *p.status = clamped ? ST_CLAMPED : ST_OK;
+  }
+  if (blockIdx.x == 0) {  // leave no plan behind: empty chunks, one partition per unit
+    for (int c = threadIdx.x; c <= p.n_chunks; c += C::NTHREADS) const_cast<int*>(p.chunk_first)[c] = 0;
+    for (int u = threadIdx.x; u < p.B * p.Hkv; u += C::NTHREADS) const_cast<int*>(p.nparts)[u] = 1;
+  }
+  __syncthreads();
+  warp_main<C>(p, &tmk, &tmv, smem, full, abort_flag, rec, 0, rank < P ? 1 : 0, P, unit * split,
+               cw, lane);
+  if (split > 1) {
+    __threadfence();   // this CTA's partials, before the cluster barrier releases them
+    cluster_sync_all();
+    if (P > 1) {  // every CTA of the cluster merges its share of the rows
+      const int per = (p.R + split - 1) / split;
+      const int r0 = rank * per, r1 = min(p.R, r0 + per);
+      if (r0 < r1)
+        merge_partials<C>(p, reinterpret_cast<float*>(smem + C::OFF_OB), s, hkv, (int64_t)unit * split,
+                          P, cw, lane, r0, r1);
+    }
+  }
 }
 
 // Launch helper: one CTA per plan chunk.
@@ -1377,11 +1434,18 @@ int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap&
   cfg.blockDim = dim3(C::NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.pf_split > 1) {  // single-launch mode: one cluster per (sequence, KV head) unit
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.pf_split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, pa_tile_kernel<C>, p, tk, tv);
   if (e != cudaSuccess) return (int)e;
   return (int)cudaGetLastError();

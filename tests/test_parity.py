@@ -554,3 +554,58 @@ def test_mxfp4_batch_4096_sampled():
     ref = util.oracle_decode(p, seqs=seqs)
     util.assert_parity(got[seqs], ref, case.kv, case.name)
     assert np.isfinite(got).all()
+
+
+SINGLE_LAUNCH = [
+    synth.config1(),                                    # 2 units, 2 CTAs a unit
+    synth.config4(batch=8),                             # 8 units, 8-CTA clusters (MXFP4)
+    synth.config2("a"),                                 # 32 units, 4 CTAs a unit, qlen 4
+    synth.config4(batch=5, context_lens=[2048, 1, 129, 0, 3000], seed=3501),  # empty and 1-token units
+    synth.replace(synth.config1(context_lens=[700, 300], seed=3502), window=200),
+    synth.replace(synth.config3(qlen=1, batch=3, context_lens=(100, 700), seed=3503), sink_mean=1.5),
+]
+
+
+@pytest.mark.parametrize("case", SINGLE_LAUNCH, ids=lambda c: f"{c.name}-s{c.seed}")
+def test_single_launch_and_planned_paths_match_oracle(case):
+    # small problems: pa_decode_run is one launch (a cluster of CTAs per unit merging its
+    # partials, no plan, no reduce kernel); the split API runs the planned path on the same
+    # input; both must match the oracle, and the single launch must leave no plan behind
+    # that a later pa_decode / pa_decode_reduce would act on
+    p = synth.make(case)
+    ref = util.oracle_decode(p)
+    dev = synth.to_device(p, "cuda")
+    shape = tuple(p["query"].shape)
+    q = dev["query"].view(torch.float8_e4m3fn) if dev["query"].dtype == torch.uint8 else dev["query"]
+
+    def args_for(out):
+        return ops.make_args(q, dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                             dev["context_lens"], out, key_scale=dev["key_scale"],
+                             value_scale=dev["value_scale"], q_scale=dev["q_scale"],
+                             softmax_scale=case.scale_qk(), q_quant=case.q_quant,
+                             sliding_window=case.window, sinks=dev.get("sinks"))
+
+    one = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    a1 = args_for(one)
+    ws = ops.alloc_workspace(a1)
+    ops.pa_decode_run(a1, ws)
+    torch.cuda.synchronize()
+    assert ops.pa_decode_read_status(ws) == 0
+    util.assert_parity(one.float().cpu().numpy(), ref, case.kv, case.name + " single launch")
+    # nothing left to act on: a decode and a reduce without a new plan write no row
+    stale = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    a_stale = args_for(stale)
+    ops.pa_decode(a_stale, ws)
+    ops.pa_decode_reduce(a_stale, ws)
+    torch.cuda.synchronize()
+    assert torch.isnan(stale.float()).all()
+
+    split = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    a2 = args_for(split)
+    ws2 = ops.alloc_workspace(a2)
+    ops.pa_decode_plan(a2, ws2)
+    ops.pa_decode(a2, ws2)
+    ops.pa_decode_reduce(a2, ws2)
+    torch.cuda.synchronize()
+    assert ops.pa_decode_read_status(ws2) == 0
+    util.assert_parity(split.float().cpu().numpy(), ref, case.kv, case.name + " planned")
