@@ -952,12 +952,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1) __maxnreg__(C::MAXREG)
 
 template <class C>
 int launch_mx(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, void* stream) {
-  static bool attr_done = false;  // per process; the attribute is per function
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(pa_mx_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per device ordinal
+  if (const int rc = set_smem_attr_once(pa_mx_kernel<C>, C::SMEM, attr_done)) return rc;
   if (grid < 1) grid = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

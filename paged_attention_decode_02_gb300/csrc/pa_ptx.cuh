@@ -4,12 +4,29 @@
 // shared-memory matrix descriptors, MMA issue / commit, TMEM loads and stores).
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace pa {
+
+// Sets a kernel's dynamic shared-memory limit once per device (the attribute belongs to the
+// function on the current device): `done` holds one bit per device ordinal below 64.
+template <typename K>
+int set_smem_attr_once(K kernel, int smem, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return 0;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return (int)e;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -1420,12 +1420,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
 template <class C>
 int launch_tile(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                 void* stream) {
-  static bool attr_done = false;  // per process; the attribute is per function
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(pa_tile_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return (int)e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per device ordinal
+  if (const int rc = set_smem_attr_once(pa_tile_kernel<C>, C::SMEM, attr_done)) return rc;
   if (grid < 1) grid = 1;
   // Programmatic serialisation: this grid launches while the plan kernel runs and waits
   // for it (griddepcontrol.wait) before reading the task list.
