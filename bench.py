@@ -205,7 +205,7 @@ def per_config(device, peak, calls=10, warmup=3):
     decode + reduce on a plan built beforehand (a model plans once per step and reuses the
     plan in every layer; the pages' "planned" timings take the plan as an input too)."""
     cases = [synth.config1(), synth.config2("a"), synth.config2("b"), synth.config3(qlen=1),
-             synth.config3(qlen=4)] + [synth.config4(batch=b) for b in (8, 64, 512, 4096)]
+             synth.config3(qlen=4)] + [synth.config4(batch=b) for b in (8, 32, 64, 128, 256, 512, 4096)]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
     res = {}
