@@ -260,8 +260,7 @@ def per_config(device, peak, calls=10, warmup=3):
         nbytes = synth.algorithmic_bytes(case, p["context_lens"].cpu().tolist())
         med, medg, medp = statistics.median(ts), statistics.median(tg), statistics.median(tp)
         medf = statistics.median(tf)
-        name = f"{case.name}_b{case.batch}" if case.name.startswith("cfg4") else case.name
-        res[name] = {"us": round(med * 1e3, 2), "us_graph": round(medg * 1e3, 2),
+        res[case.name] = {"us": round(med * 1e3, 2), "us_graph": round(medg * 1e3, 2),
                      "us_planned": round(medp * 1e3, 2), "us_one_partition": round(medf * 1e3, 2),
                      "bytes": nbytes, "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
                      "frac": round(nbytes / (med * 1e-3) / 1e9 / peak, 4)}
