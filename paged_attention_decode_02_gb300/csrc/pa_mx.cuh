@@ -3,9 +3,9 @@
 // The MXFP4 page's QK is one scaled MMA per 32-value block: fp4 K against an 8-bit query
 // with K's e8m0 byte as the hardware block scale ("[FlyDSL] pa_decode: MXFP4 K/V in the
 // shared PA tile kernel", kernel description).  On sm_103a that is tcgen05.mma
-// kind::mxf8f6f4.block_scale: K's e2m1 values are used as stored (the MMA warp only spreads
-// each 16-value group into the 16-byte slot the operand layout wants), its e8m0 bytes sit in
-// tensor memory as the A scales, and the query
+// kind::mxf8f6f4.block_scale: K's e2m1 values are used as stored (two unpack warps only
+// spread each 16-value group into the 16-byte slot the operand layout wants), its e8m0 bytes
+// sit in tensor memory as the A scales, and the query
 // is the B operand in e4m3 (as given, quantised, or a bf16 row split exactly into two e4m3
 // terms).  No K value is converted by the CUDA cores.  S^T = K Q^T lands in tensor memory,
 // one lane per token, and the softmax warps read it back in mma-fragment order.  PV stays on
@@ -20,8 +20,9 @@
 //   warp 4*NGRP           producer: block-table page gather with TMA (K, V, and the two
 //                         scale runs) into a ring of NS block slots;
 //   warp 4*NGRP+1         MMA: owns tensor memory, builds each task's query operand and row
-//                         factors, copies each block's staged K scale bytes into tensor
-//                         memory (tcgen05.cp) and issues the block-scaled MMAs.
+//                         factors; its lane 0 copies each block's staged K scale bytes into
+//                         tensor memory (tcgen05.cp) and issues the block-scaled MMAs (this
+//                         loop's issue rate sets the block period).
 //   warps 4*NGRP+2, +3    unpack: each spreads half of every block's K into the MMA operand
 //                         layout (one of NKU tiles) and stages its scale bytes.
 // Each SM sub-partition runs two consumer warps (a warp's TMEM lane quarter fixes its
@@ -393,40 +394,56 @@ __device__ void mx_mma(const DecodeParams& p, uint8_t* sm, uint64_t* bars, volat
     const int next = mx_next_task<C>(p, sm, tb, task + 1, te);  // its query rows load now
     if (next < te) mx_q_issue<C>(p, sm, mx_task<C>(p, sm, tb, next), lane);
     const uint32_t qh = smem_u32(sm + C::OFF_Q + qb * 4096);
-    for (int i = 0; i < T.nblk; ++i, ++k) {
-      const int sb = k % C::NSB, sf = k % C::NSF;
-      if (!mx_wait(&bars[C::B_KFULL + k % C::NKU], (k / C::NKU) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if (k >= C::NSB &&
-          !mx_wait(&bars[C::B_SFREE + sb], ((k - C::NSB) / C::NSB) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t a = smem_u32(sm + C::OFF_KU + (k % C::NKU) * 16384);
+    // The block loop runs on lane 0 alone: this warp's issue rate sets the block period, so
+    // the loop holds no warp-wide step.  Both barriers of a block are probed back to back
+    // (their latencies overlap), and the bounded wait with its abort check runs only when a
+    // probe finds the phase open.
+    if (lane == 0) {
+      const uint64_t db = umma_desc(qh, 16, 1024);
+      // one MMA of N = 16 query rows per 32-value block (K-step s: descriptor start + 32 s
+      // bytes, scale byte s); a split query's lo term (rows 16..31 of the buffer, 2048 bytes
+      // on, its own scale byte) accumulates into the same columns
+      constexpr uint32_t H0 = umma_idesc_mx(5u, 0u, 16u, 128u, 0u, 0u), H1 = umma_idesc_mx(5u, 0u, 16u, 128u, 1u, 0u);
+      constexpr uint32_t H2 = umma_idesc_mx(5u, 0u, 16u, 128u, 2u, 0u), H3 = umma_idesc_mx(5u, 0u, 16u, 128u, 3u, 0u);
+      constexpr uint32_t L0 = umma_idesc_mx(5u, 0u, 16u, 128u, 0u, 1u), L1 = umma_idesc_mx(5u, 0u, 16u, 128u, 1u, 1u);
+      constexpr uint32_t L2 = umma_idesc_mx(5u, 0u, 16u, 128u, 2u, 1u), L3 = umma_idesc_mx(5u, 0u, 16u, 128u, 3u, 1u);
+      for (int i = 0; i < T.nblk; ++i, ++k) {
+        const int sb = k % C::NSB, sf = k % C::NSF, ku = k % C::NKU;
+        const uint32_t kpar = (k / C::NKU) & 1, spar = ((k - C::NSB) / C::NSB) & 1;
+        const bool kready = mbar_try_wait(&bars[C::B_KFULL + ku], kpar);
+        const bool sready = k < C::NSB || mbar_try_wait(&bars[C::B_SFREE + sb], spar);
+        if (!kready && !mx_wait(&bars[C::B_KFULL + ku], kpar, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (!sready && !mx_wait(&bars[C::B_SFREE + sb], spar, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = umma_desc(smem_u32(sm + C::OFF_KU + ku * 16384), 16, 1024);
         const uint32_t d = tmem + (uint32_t)(C::COL_S + sb * 16);
         const uint32_t sfa = tmem + (uint32_t)(C::COL_SFA + sf * 4), sfb = tmem + (uint32_t)C::COL_SFB;
         // lane quarter q of the tokens reads its scales from column sfa + q
         tmem_cp_32x128b_x4(sfa, umma_desc_noswz(smem_u32(sm + C::OFF_SFA + sf * 512), 128));
-        // one MMA of N = 16 query rows per 32-value block; a split query's lo term (rows 16..31
-        // of the buffer, its own scale byte) accumulates into the same columns
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          umma_mxf8f6f4(d, umma_desc(a + 32 * s, 16, 1024), umma_desc(qh + 32 * s, 16, 1024),
-                        umma_idesc_mx(5u, 0u, 16u, 128u, (uint32_t)s, 0u), sfa, sfb, s > 0);
+        // (a descriptor's start address is its low 14 bits, in 16-byte units: + 2 per 32
+        // bytes; shared addresses stay below 227 KiB + 2 KiB, so the field never carries)
+        umma_mxf8f6f4(d, da, db, H0, sfa, sfb, 0u);
+        umma_mxf8f6f4(d, da + 2, db + 2, H1, sfa, sfb, 1u);
+        umma_mxf8f6f4(d, da + 4, db + 4, H2, sfa, sfb, 1u);
+        umma_mxf8f6f4(d, da + 6, db + 6, H3, sfa, sfb, 1u);
         if (two_terms) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            umma_mxf8f6f4(d, umma_desc(a + 32 * s, 16, 1024), umma_desc(qh + 2048 + 32 * s, 16, 1024),
-                          umma_idesc_mx(5u, 0u, 16u, 128u, (uint32_t)s, 1u), sfa, sfb, true);
+          umma_mxf8f6f4(d, da, db + 128, L0, sfa, sfb, 1u);
+          umma_mxf8f6f4(d, da + 2, db + 130, L1, sfa, sfb, 1u);
+          umma_mxf8f6f4(d, da + 4, db + 132, L2, sfa, sfb, 1u);
+          umma_mxf8f6f4(d, da + 6, db + 134, L3, sfa, sfb, 1u);
         }
         umma_commit(&bars[C::B_SFULL + sb]);
       }
-      __syncwarp();
     }
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+    k = __shfl_sync(0xffffffffu, k, 0);
     ++ord;
     task = next;
   }
