@@ -5,7 +5,7 @@ namespace pa {
 
 int launch_mx_mxfp4(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                     void* stream) {
-  return launch_mx<MxCfg<3, 6>>(p, tk, tv, grid, stream);
+  return launch_mx<MxCfg<3, 5>>(p, tk, tv, grid, stream);
 }
 
 }  // namespace pa

@@ -60,10 +60,10 @@ struct MxCfg {
   static constexpr int REG_CONS = ((MAXREG * NTHREADS - REG_HELP * 128) / (NCONS * 32)) / 8 * 8;
   static_assert(REG_HELP <= MAXREG && REG_CONS >= MAXREG && REG_CONS <= 255, "register split");
   static_assert(REG_HELP * 128 + REG_CONS * NCONS * 32 <= MAXREG * NTHREADS, "register split");
-  static constexpr int NSB = 5;  // S buffers in tensor memory (16 columns each)
+  static constexpr int NSB = 6;  // S buffers in tensor memory (16 columns each)
   static constexpr int NSF = 3;  // K-scale buffers in tensor memory (4 columns each)
   static constexpr int NKU = 3;  // unpacked K tiles (the MMA's A operand)
-  static constexpr int NQB = 6;  // query buffers (task ordinal mod NQB); > NSB, see mx_mma
+  static constexpr int NQB = 7;  // query buffers (task ordinal mod NQB); > NSB, see mx_mma
   static constexpr int MAXT = 32;  // task records staged in shared memory (more: global reads)
   // ring slot: K packed [128 tokens][64 B], V [128][64 B] (64-byte swizzle), K and V e8m0
   // words [128][4 B]
