@@ -72,7 +72,7 @@ extern "C" {
 typedef int32_t pa_status;
 #define PA_OK 0
 #define PA_ERR_INVALID_ARG (-1)   /* malformed argument: null pointer, bad shape */
-#define PA_ERR_UNSUPPORTED (-2)   /* well-formed, but not a combination this build serves */
+#define PA_ERR_UNSUPPORTED (-2)   /* well-formed, but not a combination the library serves */
 #define PA_ERR_WORKSPACE (-3)     /* workspace missing, too small or misaligned */
 #define PA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
 
