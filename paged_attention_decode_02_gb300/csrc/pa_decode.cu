@@ -25,7 +25,13 @@ namespace pa {
 // pa_decode: MXFP4 K/V ...", commit messages: planned tasks, direct output with one
 // partition, tasks from a CU budget; max_partitions caps the split).  Equal chunks keep
 // every CTA busy for the same time whatever the mix of context lengths.
+// Splitting is dropped where it buys nothing: when no unit is longer than a chunk plus its
+// gap, the units are also laid out whole (each in the chunk its tiles start in), and that
+// layout is taken if no chunk then carries more than two unit gaps beyond the chunk
+// length (checked for up to one round of sequences, 1024). A split unit costs a second task (its end-of-task merge), the partial writes and
+// a reduce pass, which batches of many short, even sequences do not win back.
 // ------------------------------------------------------------------------------------
+constexpr int kWholeUnitChunks = 2048;  // chunks the whole-unit check covers (more: split)
 __device__ __forceinline__ int clamp_len(int L, int cap, int* clamped) {
   if (L < 0) return 0;
   if (L > cap) {
@@ -108,6 +114,8 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
   __shared__ int sh32b[32];
   __shared__ int shmax, shclamp;
   __shared__ int sh_last[1024];  // chunk of each thread's last task in the current round
+  __shared__ int sh_load[kWholeUnitChunks];  // line positions per chunk, units laid out whole
+  __shared__ int sh_load_max;
   const int tid = threadIdx.x;
   const int cap = pp.W * pp.S;
   // Until the first write this kernel only reads the context lengths, which no kernel of
@@ -150,6 +158,30 @@ __global__ void __launch_bounds__(1024) pa_plan_kernel(const PlanParams pp) {
     if (cg.C < cmin) cg.C = cmin;
   }
   cg.nchunks = T > 0 ? (T + cg.C - 1) / cg.C : 1;
+  // (the condition is the same in every thread: shmax is read after the scan's barriers;
+  // one round of sequences, so the check costs one scan)
+  if (cg.maxp >= 2 && shmax > 0 && (uint32_t)shmax <= cg.C + (uint32_t)w && pp.B <= (int)blockDim.x &&
+      cg.nchunks <= (uint32_t)kWholeUnitChunks) {
+    for (int c = tid; c < (int)cg.nchunks; c += blockDim.x) sh_load[c] = 0;
+    if (tid == 0) sh_load_max = 0;
+    __syncthreads();
+    const int n = tid < pp.B ? n_own : 0;
+    long long all_tiles;
+    const long long before = block_exclusive_scan<long long>((long long)n, &all_tiles, sh64);
+    if (tid < pp.B) {
+      const uint32_t U0 = (uint32_t)(before * pp.Hkv + (long long)w * ((long long)tid * pp.Hkv + 1));
+      for (int h = 0; h < pp.Hkv; ++h) {
+        const uint32_t c = (U0 + (uint32_t)(h * (n + w))) / cg.C;
+        atomicAdd(&sh_load[c < cg.nchunks - 1 ? c : cg.nchunks - 1], n + w);
+      }
+    }
+    __syncthreads();
+    int mx = 0;
+    for (int c = tid; c < (int)cg.nchunks; c += blockDim.x) mx = sh_load[c] > mx ? sh_load[c] : mx;
+    atomicMax(&sh_load_max, mx);
+    __syncthreads();
+    if ((uint32_t)sh_load_max <= cg.C + 2u * (uint32_t)w) cg.maxp = 1;  // whole units
+  }
 
   long long carry_tiles = 0;
   int carry_tasks = 0, carry_slots = 0, carry_chunk = -1;  // chunk of the last task so far

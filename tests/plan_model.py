@@ -8,7 +8,10 @@ offset.  The units are laid end to end on a line, each as a gap of UNIT_COST pos
 chunks of C positions (C = ceil(length / budget), raised when needed so that no unit
 touches more than max_partitions chunks); a unit becomes one partition per chunk its
 tiles touch.  With max_partitions 1, or an empty unit, the unit is one task in the
-chunk its tiles start in.
+chunk its tiles start in.  Splitting is also dropped when no unit is longer than C plus
+its gap and, with every unit laid out whole in the chunk its tiles start in, no chunk
+carries more than C + 2 UNIT_COST positions (up to WHOLE_UNIT_CHUNKS chunks, and for at
+most PLAN_ROUND sequences).
 
 The workspace layout mirrors the library's (256-byte aligned regions): status word and
 task count, then nparts, part_base, counters (int32 per unit), tasks (4 x int32 per
@@ -20,6 +23,8 @@ import numpy as np
 
 TILE = 256
 UNIT_COST = 2  # line positions charged per unit before its tiles
+WHOLE_UNIT_CHUNKS = 2048
+PLAN_ROUND = 1024  # sequences the plan kernel's block holds at once
 
 
 def _align(x, a=256):
@@ -44,6 +49,16 @@ def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_C
     if max_partitions >= 2 and maxt > 0:
         C = max(C, (maxt - 1) // (max_partitions - 1) + 1)
     nchunks = -(-total // C) if total > 0 else 1
+    split = max_partitions >= 2
+    if split and 0 < maxt <= C + unit_cost and len(tiles) <= PLAN_ROUND and nchunks <= WHOLE_UNIT_CHUNKS:
+        load, U = [0] * nchunks, 0
+        for n in tiles:
+            for h in range(hkv):
+                U += unit_cost
+                load[min(U // C, nchunks - 1)] += n + unit_cost
+                U += n
+        if max(load) <= C + 2 * unit_cost:
+            split, max_partitions = False, 1
     tasks, chunks, nparts, part_base, unit_pos = [], [], [], [], []
     U, slot = 0, 0
     for s, n in enumerate(tiles):
@@ -71,7 +86,7 @@ def plan(context_lens, hkv, budget, max_partitions, cap_tokens, unit_cost=UNIT_C
         prev = c
     return {"tiles": tiles, "firsts": firsts, "C": C, "nchunks": nchunks, "tasks": tasks, "chunks": chunks,
             "nparts": nparts, "part_base": part_base, "chunk_first": first, "slots": slot,
-            "length": total, "unit_pos": unit_pos, "hkv": hkv, "unit_cost": unit_cost}
+            "length": total, "unit_pos": unit_pos, "hkv": hkv, "unit_cost": unit_cost, "split": split}
 
 
 def capacity(batch, hkv, budget):

@@ -64,10 +64,19 @@ def test_plan_arithmetic(name, lens, hkv, budget, maxp, qlen, window):
     assert first[-1] == len(m["tasks"]) and all(a <= b for a, b in zip(first, first[1:]))
     for c in range(budget):
         assert all(m["chunks"][t] == c for t in range(first[c], first[c + 1]))
+    # whole units where splitting was allowed but dropped: one task per unit, and no chunk
+    # carries more than two unit gaps beyond C positions of tiles and gaps
+    if maxp >= 2 and not m["split"]:
+        assert all(p == 1 for p in m["nparts"]) and m["slots"] == 0
+        assert m["nchunks"] <= budget
+        carried = np.zeros(m["nchunks"], dtype=np.int64)
+        for (s, hp, b, e), c in zip(m["tasks"], m["chunks"]):
+            carried[c] += e - b + pm.UNIT_COST
+        assert carried.max(initial=0) <= m["C"] + 2 * pm.UNIT_COST
     # balance: with splitting on, every task's tiles lie inside its chunk's range of the
     # line (each unit is a gap of UNIT_COST followed by its tiles), so no chunk runs more
     # than C tiles, and every chunk but the last covers exactly C positions
-    if maxp >= 2:
+    if m["split"]:
         C = m["C"]
         unit_of = {}
         for u, pos in enumerate(m["unit_pos"]):
