@@ -196,7 +196,11 @@ pa_status pa_decode_validate(const pa_decode_args* args);
  * task_budget chunks of equal length (one per tile-kernel CTA), longer when needed so
  * that no unit touches more than max_partitions chunks.  A unit crossing chunk
  * boundaries becomes one partition per chunk it touches; with max_partitions 1 each
- * unit is one task, run by the chunk it starts in.  Clears the device status word.  One
+ * unit is one task, run by the chunk it starts in.  The plan also keeps every unit whole
+ * (as with max_partitions 1) when no unit is longer than a chunk plus its gap and, so laid
+ * out, no chunk carries more than two gaps beyond its length (checked for batches of up
+ * to 1024 sequences): splits there would add tasks, partials and reduce work without
+ * evening out the chunks.  Clears the device status word.  One
  * launch, 1 CTA.  ("[FlyDSL] pa_decode: MXFP4 K/V ...", commit messages: planned tasks,
  * direct output with one partition, tasks from a CU budget.)
  * All launches of this library use programmatic dependent launch: a kernel may begin
