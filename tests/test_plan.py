@@ -17,6 +17,7 @@ MIXES = [
     ("long16", [int(x) for x in np.random.default_rng(5).integers(120000, 131073, 16)], 1),
     ("ragged", [0, 1, 255, 256, 257, 4000, 0, 70000, 3, 131072], 2),
     ("uniform4096", [2048] * 4096, 1),
+    ("even128", [2048] * 128, 1),  # short, even sequences: laid out whole at budget 152
     ("one", [500000], 1),
     ("empty", [0, 0, 0], 4),
     ("mixed", [int(x) for x in np.random.default_rng(9).integers(1, 9000, 37)], 2),
@@ -110,6 +111,25 @@ def test_plan_balance_long_context():
     assert work.max() - work.sum() / 152 <= 1.0
     two = per[starts == 2]
     assert len(two) > 0 and two.max() <= m["C"] - pm.UNIT_COST
+
+
+def test_plan_keeps_short_even_units_whole():
+    # 128 sequences of 8 tiles over 152 chunks: split at chunk edges, every sequence would
+    # become two partial tasks; whole, each chunk runs at most one sequence (10 positions
+    # against C = 9), within the two-gap allowance, so nothing is split
+    m = pm.plan([2048] * 128, 1, 152, 128, 1 << 20)
+    assert not m["split"] and len(m["tasks"]) == 128 and m["slots"] == 0
+    assert pm.chunk_tiles(m).max() == 8
+    # 64 such sequences: C = 5, a chunk would carry two whole sequences (20 positions), so
+    # the split stays
+    m = pm.plan([2048] * 64, 1, 152, 128, 1 << 20)
+    assert m["split"] and pm.chunk_tiles(m).max() <= m["C"]
+    # long contexts are always split: a unit is many chunks long
+    m = pm.plan(MIXES[0][1], 1, 152, 128, 1 << 20)
+    assert m["split"] and max(m["nparts"]) > 1
+    # more sequences than one plan round: the check is not made
+    m = pm.plan([2048] * 1100, 1, 152, 128, 1 << 20)
+    assert m["split"]
 
 
 @pytest.mark.gpu
